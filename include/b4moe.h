@@ -1,0 +1,187 @@
+/*
+ * b4moe.h -- C ABI of the GB300 (sm_103a) fused W4A16 mixture-of-experts layer.
+ *
+ * The layer: 4-bit FP4 weights (NVFP4 or MXFP4), bf16 activations, route
+ * packing, a grouped FC1 GEMM with in-kernel dequantisation and a fused
+ * SiLU-SwiGLU or ReLU^2 epilogue, and a grouped FC2 GEMM whose store folds in
+ * the top-k weighted sum, plus a separate small-m decode path.  It is the
+ * layer described by flashinfer PR #4255, "feat(moe): sync SM12x W4A16 fused
+ * MoE family to b12x HEAD" (Description), restated for GB300.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Pointers are DEVICE pointers unless a parameter says "host".  The caller
+ *   owns every buffer; the library never allocates or frees device memory.
+ * - All GPU work is enqueued on the caller's `stream` (flashinfer PR #4255,
+ *   review comment "Propagate the stream into route packing").  b4_route_pack
+ *   and b4_fused_moe neither allocate nor synchronise, so both may be captured
+ *   into a CUDA graph (b12x PR #136, Summary: caller-owned buffers so decode
+ *   graph capture needs no library scratch arena).
+ * - Argument problems are reported before anything is launched, as a
+ *   b4_status; b4_last_error() then returns a thread-local message.
+ * - Device-side failures (a bounded wait that ran out) are written to a
+ *   status word at the start of the workspace; read it with b4_check_status.
+ * - Only sm_103 devices are accepted (B4_ERR_UNSUPPORTED_DEVICE otherwise);
+ *   there is no fallback path.
+ *
+ * Data types: token ids int32, router weights fp32, activations and output
+ * bf16 (raw 16-bit patterns, row-major), packed FP4 codes uint8 (two codes per
+ * byte, element 2j in the low nibble), block scales uint8 (E4M3 or E8M0 bit
+ * patterns), global scales fp32.
+ */
+#ifndef B4MOE_H
+#define B4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* b4_stream_t;
+
+typedef enum b4_status {
+  B4_OK = 0,
+  B4_ERR_INVALID_ARGUMENT = 1,   /* bad shape, null or misaligned pointer, bad enum */
+  B4_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 */
+  B4_ERR_WORKSPACE_TOO_SMALL = 3,
+  B4_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+  B4_ERR_TIMEOUT = 5             /* a device-side bounded wait ran out */
+} b4_status;
+
+/* Weight source formats (flashinfer PR #4255, Description: NVFP4 weights and
+ * "a new fp4_e8m0_k32 (MXFP4 K/32) weight source format").
+ * NVFP4: E2M1 codes, one FP8-E4M3 block scale per 16 elements along K, and
+ *        one fp32 global scale per expert (ModelOpt layout).
+ * MXFP4: E2M1 codes, one E8M0 power-of-two scale 2^(e-127) per 32 elements
+ *        along K, no global scale.  K need not be a multiple of 128 (the
+ *        "scale tail" of tensor-parallel shards). */
+typedef enum b4_format { B4_NVFP4_E4M3_K16 = 0, B4_MXFP4_E8M0_K32 = 1 } b4_format;
+
+/* FC1 epilogue activations (flashinfer PR #4255, Performance: relu2, silu).
+ * SILU_SWIGLU: W13 has 2*inter rows, rows [0, inter) gate and [inter, 2*inter)
+ *              up; h = silu(gate) * up.
+ * RELU2:       W1 has inter rows; h = max(a, 0)^2. */
+typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activation;
+
+/* Execution path of b4_fused_moe.  AUTO takes the decode path for m <= 4
+ * (the cap flashinfer PR #4255, Reviewer Notes, chose) and the route-packed
+ * grouped path otherwise.  DECODE is accepted for m <= B4_DECODE_MAX_M. */
+typedef enum b4_path { B4_PATH_AUTO = 0, B4_PATH_DECODE = 1, B4_PATH_GROUPED = 2 } b4_path;
+
+#define B4_DECODE_MAX_M 64
+#define B4_MAX_LOCAL_EXPERTS 1024
+
+/* Problem shape.  All fields are plain values except expert_map. */
+typedef struct b4_moe_config {
+  int32_t m;                  /* tokens, >= 0 */
+  int32_t top_k;              /* routes per token, 1..32 */
+  int32_t num_global_experts; /* E_g: valid ids are [0, E_g) */
+  int32_t num_local_experts;  /* E_l: experts whose weights are passed, 1..B4_MAX_LOCAL_EXPERTS */
+  int32_t hidden;             /* H: multiple of 64 */
+  int32_t inter;              /* I: multiple of 32 (NVFP4: 16 suffices for K, 32 for tiling) */
+  int32_t format;             /* b4_format */
+  int32_t path;               /* b4_path */
+  /* Device int32 [E_g] mapping a global expert id to a local expert, or -1;
+   * NULL means the identity (then E_g must equal E_l).  flashinfer PR #4255,
+   * Tests: "covering expert_map, invalid expert ids". */
+  const int32_t* expert_map;
+} b4_moe_config;
+
+/* Token capacity the packing and workspace are sized to: next_pow2(max(m, 1))
+ * (flashinfer PR #4255, Description: "specialize on a power-of-two capacity
+ * instead of the exact token count").  Never fails. */
+int32_t b4_route_capacity_tokens(int32_t m);
+
+/* Bytes of workspace b4_fused_moe needs for this configuration and
+ * activation.  Depends on m only through b4_route_capacity_tokens(m), so one
+ * workspace serves every m up to the next power of two (flashinfer PR #4255,
+ * Description: "The W4A16 workspaces are sized to the same capacity").
+ * Returns 0 for an invalid configuration (see b4_last_error). */
+size_t b4_workspace_bytes(const b4_moe_config* cfg, int32_t activation);
+
+/* Sizes of the prepared (serving-layout) weights of one tensor:
+ * which = 0: W13 (SwiGLU) or W1 (ReLU^2), [E_l, N1, H];  which = 1: W2, [E_l, H, I].
+ * Writes the code and scale byte counts to *code_bytes and *scale_bytes (host). */
+b4_status b4_prepared_sizes(const b4_moe_config* cfg, int32_t which, int32_t activation,
+                            size_t* code_bytes, size_t* scale_bytes);
+
+/* Converts checkpoint-layout weights of one tensor into the serving layout
+ * b4_fused_moe reads (flashinfer PR #4255, CodeRabbit walkthrough: weight
+ * preparation "with layout normalization, ... scale packing, and W13
+ * rotation").
+ *
+ * src_codes  [E_l, N, K/2] uint8, two E2M1 codes per byte, element 2j low nibble.
+ * src_scales [E_l, N, K/g] uint8 (E4M3 for NVFP4, g = 16; E8M0 for MXFP4, g = 32).
+ * dst_codes, dst_scales: b4_prepared_sizes bytes each, 16-byte aligned.
+ * The serving layout tiles rows by 128 and K by 64, pads both with zeros,
+ * interleaves gate/up rows in groups of 16 for SwiGLU, re-encodes each E2M1
+ * nibble for a table-lookup dequantiser, and re-encodes the block scales.
+ * Blocks whose scale decodes to zero are stored with zero codes (the product
+ * is zero either way); a negative E4M3 scale is folded into the code signs.
+ *
+ * Offline: this call synchronises `stream` to report invalid scale codes
+ * (E4M3 NaN; E8M0 codes of 192 and above, or below 65 in a block with a
+ * nonzero code -- scales outside 2^-62 .. 2^64 are outside the range the
+ * bf16 dequantiser reproduces exactly) as B4_ERR_INVALID_ARGUMENT.
+ * Not capture-safe. */
+b4_status b4_prepare_weights(const b4_moe_config* cfg, int32_t which, int32_t activation,
+                             const uint8_t* src_codes, const uint8_t* src_scales, uint8_t* dst_codes,
+                             uint8_t* dst_scales, b4_stream_t stream);
+
+/* Route packing (flashinfer PR #4255, Description: shape-stable route
+ * packing; Tests: expert_map, invalid ids, preallocated buffers).
+ *
+ * topk_ids [m, top_k] int32.  A route r = t*top_k + j is valid iff
+ * 0 <= id < E_g and the local expert l = expert_map[id] (or id) lies in
+ * [0, E_l); invalid routes are dropped, never an error.
+ * Outputs (caller-allocated):
+ *   counts        [E_l]     int32: valid routes per local expert;
+ *   offsets       [E_l + 1] int32: exclusive scan of counts, offsets[E_l] = valid routes;
+ *   sorted_routes [R_cap]   int32, R_cap = b4_route_capacity_tokens(m) * top_k:
+ *                 sorted_routes[offsets[l] + i] = i-th valid route of expert l in
+ *                 ascending r (stable); entries past offsets[E_l] are -1.
+ * One launch on `stream`; no allocation, no synchronisation (capture-safe). */
+b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                        int32_t* sorted_routes, b4_stream_t stream);
+
+/* The fused layer: out = sum_j w[t,j] * FC2_e(act(FC1_e(x[t]))) for the valid
+ * routes (t, j), e = local expert of route (t, j), rounded to bf16 once.
+ *
+ * x             [m, H] bf16.
+ * w13, s13      prepared FC1 weights (b4_prepare_weights, which = 0).
+ * gs13          [E_l] fp32 global scales of FC1 (NVFP4); must be NULL for MXFP4.
+ * w2, s2, gs2   the same for FC2 (which = 1).
+ * topk_ids      [m, top_k] int32; topk_weights [m, top_k] fp32.
+ * activation    b4_activation (must match the one the weights were prepared for).
+ * out           [m, H] bf16, written in full (tokens without a valid route get 0).
+ * workspace     >= b4_workspace_bytes(cfg, activation) bytes, 256-byte aligned;
+ *               its contents on entry do not matter.  It holds the status word
+ *               read by b4_check_status.
+ * FC1 accumulates gs13 * (x . w13) in fp32, applies the activation in fp32 and
+ * rounds h to bf16; FC2 accumulates in fp32, multiplies by gs2 and the router
+ * weight and sums the routes of a token in fp32 before one bf16 rounding.
+ * Enqueues 3-4 launches on `stream`; no allocation, no synchronisation. */
+b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                       const float* gs13, const uint8_t* w2, const uint8_t* s2, const float* gs2,
+                       const int32_t* topk_ids, const float* topk_weights, int32_t activation, uint16_t* out,
+                       void* workspace, size_t workspace_bytes, b4_stream_t stream);
+
+/* Synchronises `stream`, then reads the device status word of `workspace`
+ * (written by b4_fused_moe's kernels): B4_OK, or B4_ERR_TIMEOUT if a bounded
+ * device wait ran out.  Resets the word to B4_OK.  Not capture-safe. */
+b4_status b4_check_status(void* workspace, b4_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* b4_status_string(int32_t status);
+
+/* Thread-local message describing the last error returned on this thread. */
+const char* b4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B4MOE_H */

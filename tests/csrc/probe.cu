@@ -1,0 +1,122 @@
+// Test-only probes of the library's device building blocks (not part of
+// libb4moe): a single tcgen05.mma with A in tensor memory and B in the
+// library's shared-memory layout, and a dump of the register dequantiser.
+// They pin the layout assumptions the GEMM kernel is built on.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dequant.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+using namespace b4;
+
+// D[128][N] = A[128][64] x B[N][64]^T, A via tcgen05.st into TMEM, B in the
+// no-swizzle K-major core-matrix layout (LBO 128 B, SBO 1024 B), four K=16
+// MMAs, one commit.
+__global__ void probe_mma_kernel(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t* status) {
+  __shared__ __align__(1024) uint8_t sB[256 * 128];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const Abort ab{status, &abort_flag};
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem, 512);
+    tmem_relinquish();
+  }
+  for (int idx = tid; idx < N * 8; idx += blockDim.x) {
+    const int n = idx >> 3, kc = idx & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(B + n * 64 + kc * 8);
+    *reinterpret_cast<uint4*>(sB + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t base = tmem;
+  uint32_t r[32];
+  for (int c = 0; c < 32; ++c) r[c] = (uint32_t)A[tid * 64 + 2 * c] | ((uint32_t)A[tid * 64 + 2 * c + 1] << 16);
+  tmem_st32(base + ((uint32_t)(32 * warp) << 16), r);
+  tmem_st_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16_m128((uint32_t)N);
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ts(base + 128, base + kk * 8, smem_desc_noswizzle(smem_u32(sB) + kk * 256, 128, 1024), idesc,
+                  kk > 0 ? 1u : 0u);
+    mma_commit(&bar);
+  }
+  const bool ok = mbar_wait(&bar, 0, ab, 100);
+  tc_fence_after();
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(base + ((uint32_t)(32 * warp) << 16) + 128 + c0, v);
+      tmem_ld_wait();
+      for (int j = 0; j < 16; ++j) D[tid * N + c0 + j] = __uint_as_float(v[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(base, 512);
+}
+
+// Dequantise serving-layout blocks (one 128-row x 64-element stage each).
+template <int FMT>
+__global__ void probe_dequant_kernel(const uint8_t* codes, const uint8_t* scales, uint16_t* out) {
+  const int blk = blockIdx.x, r = threadIdx.x;
+  constexpr int SB = scale_bytes_per_row(FMT);
+  const uint8_t* cs = codes + (size_t)blk * kCodeBytesPerStage;
+  const uint4 c0 = *reinterpret_cast<const uint4*>(cs + r * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(cs + 2048 + r * 16);
+  const uint8_t* ss = scales + ((size_t)blk * kTileRows + r) * SB;
+  uint32_t sc = 0;
+  for (int b = 0; b < SB; ++b) sc |= (uint32_t)ss[b] << (8 * b);
+  uint32_t v[32];
+  dequant_stage<FMT>(c0, c1, sc, v);
+  uint16_t* o = out + ((size_t)blk * kTileRows + r) * kBK;
+  for (int c = 0; c < 32; ++c) {
+    o[2 * c] = (uint16_t)(v[c] & 0xFFFF);
+    o[2 * c + 1] = (uint16_t)(v[c] >> 16);
+  }
+}
+
+// bf16x2 multiply on chosen bit patterns (subnormal-input behaviour).
+__global__ void probe_bf16_mul_kernel(const uint32_t* a, const uint32_t* b, uint32_t* d, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) d[i] = bf16x2_mul(a[i], b[i]);
+}
+
+extern "C" {
+
+int probe_mma_ts(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t* status) {
+  if (N < 16 || N > 256 || N % 16) return -1;
+  probe_mma_kernel<<<1, 128>>>(A, B, N, D, status);
+  cudaError_t e = cudaDeviceSynchronize();
+  return (int)e;
+}
+
+int probe_dequant(const uint8_t* codes, const uint8_t* scales, int fmt, int nblocks, uint16_t* out) {
+  if (nblocks <= 0) return -1;
+  if (fmt == 0) probe_dequant_kernel<0><<<nblocks, 128>>>(codes, scales, out);
+  else probe_dequant_kernel<1><<<nblocks, 128>>>(codes, scales, out);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_bf16_mul(const uint32_t* a, const uint32_t* b, uint32_t* d, int n) {
+  if (n <= 0) return -1;
+  probe_bf16_mul_kernel<<<(n + 127) / 128, 128>>>(a, b, d, n);
+  return (int)cudaDeviceSynchronize();
+}
+
+}  // extern "C"

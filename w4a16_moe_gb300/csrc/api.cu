@@ -1,0 +1,438 @@
+// extern "C" entry points of libb4moe (declared in include/b4moe.h):
+// argument validation, workspace carve-up, path choice and kernel launches.
+// Every launch goes to the caller's stream; nothing here allocates device
+// memory or synchronises, except b4_prepare_weights and b4_check_status,
+// which are documented as synchronous.
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "b4moe.h"
+#include "kernels.cuh"
+
+namespace b4 {
+template <int MODE, int FMT>
+cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_finalize(const FinalizeParams& p, bool grouped, int num_sms, cudaStream_t stream);
+cudaError_t launch_route_pack(const RoutePackParams& p, cudaStream_t stream);
+size_t route_pack_smem_bytes(int num_local_experts);
+cudaError_t launch_prepare(const PrepareParams& p, int num_sms, cudaStream_t stream);
+}  // namespace b4
+
+using namespace b4;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+b4_status fail(b4_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+b4_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(B4_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kDecodeAutoMaxM = 4;  // flashinfer PR #4255, Reviewer Notes: decode path up to m = 4
+constexpr int kMaxSplits = 8;
+
+int32_t next_pow2(int64_t n) {
+  int64_t p = 1;
+  while (p < n) p <<= 1;
+  return (int32_t)p;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------ validation
+b4_status check_config(const b4_moe_config* cfg, int32_t act) {
+  if (!cfg) return fail(B4_ERR_INVALID_ARGUMENT, "cfg is NULL");
+  if (cfg->m < 0) return fail(B4_ERR_INVALID_ARGUMENT, "m = %d < 0", cfg->m);
+  if (cfg->m > (1 << 20)) return fail(B4_ERR_INVALID_ARGUMENT, "m = %d exceeds 2^20", cfg->m);
+  if (cfg->top_k < 1 || cfg->top_k > 32) return fail(B4_ERR_INVALID_ARGUMENT, "top_k = %d not in [1, 32]", cfg->top_k);
+  if (cfg->num_local_experts < 1 || cfg->num_local_experts > B4_MAX_LOCAL_EXPERTS)
+    return fail(B4_ERR_INVALID_ARGUMENT, "num_local_experts = %d not in [1, %d]", cfg->num_local_experts,
+                B4_MAX_LOCAL_EXPERTS);
+  if (cfg->num_global_experts < 1 || cfg->num_global_experts > (1 << 20))
+    return fail(B4_ERR_INVALID_ARGUMENT, "num_global_experts = %d out of range", cfg->num_global_experts);
+  if (!cfg->expert_map && cfg->num_global_experts != cfg->num_local_experts)
+    return fail(B4_ERR_INVALID_ARGUMENT, "without expert_map, num_global_experts must equal num_local_experts");
+  if (cfg->format != B4_NVFP4_E4M3_K16 && cfg->format != B4_MXFP4_E8M0_K32)
+    return fail(B4_ERR_INVALID_ARGUMENT, "format = %d unknown", cfg->format);
+  if (cfg->path < B4_PATH_AUTO || cfg->path > B4_PATH_GROUPED)
+    return fail(B4_ERR_INVALID_ARGUMENT, "path = %d unknown", cfg->path);
+  if (act != B4_ACT_SILU_SWIGLU && act != B4_ACT_RELU2)
+    return fail(B4_ERR_INVALID_ARGUMENT, "activation = %d unknown", act);
+  const int g = cfg->format == B4_NVFP4_E4M3_K16 ? 16 : 32;
+  if (cfg->hidden < g || cfg->hidden % g || cfg->hidden > (1 << 16))
+    return fail(B4_ERR_INVALID_ARGUMENT, "hidden = %d must be a positive multiple of %d (<= 65536)", cfg->hidden, g);
+  if (cfg->inter < g || cfg->inter % g || cfg->inter > (1 << 16))
+    return fail(B4_ERR_INVALID_ARGUMENT, "inter = %d must be a positive multiple of %d (<= 65536)", cfg->inter, g);
+  if (cfg->path == B4_PATH_DECODE && cfg->m > B4_DECODE_MAX_M)
+    return fail(B4_ERR_INVALID_ARGUMENT, "decode path takes m <= %d, got %d", B4_DECODE_MAX_M, cfg->m);
+  return B4_OK;
+}
+
+// ------------------------------------------------------------- workspace
+struct WsLayout {
+  size_t status, counts, offsets, sorted, chunks, chunk_count, h, acc, p, q, total;
+  int t_cap, r_cap, max_chunks, inter_pad, wnat, dec_splits;
+  bool decode_ok;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
+  WsLayout L{};
+  L.t_cap = next_pow2(cfg->m > 0 ? cfg->m : 1);
+  L.r_cap = L.t_cap * cfg->top_k;
+  L.max_chunks = L.r_cap / kChunkRows + cfg->num_local_experts + 1;
+  L.inter_pad = round_up(cfg->inter, kBK);
+  L.wnat = fc1_natural_width(act == B4_ACT_SILU_SWIGLU ? 0 : 1, L.inter_pad);
+  L.decode_ok = L.t_cap <= B4_DECODE_MAX_M;
+  // decode partial buffers are sized for min(T_cap, B4_DECODE_MAX_M) tokens,
+  // which keeps the total monotone in T_cap
+  const int dec_rcap = (L.t_cap < B4_DECODE_MAX_M ? L.t_cap : B4_DECODE_MAX_M) * cfg->top_k;
+  int s = 256 / dec_rcap;
+  L.dec_splits = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.status = take(256);
+  L.counts = take(sizeof(int32_t) * cfg->num_local_experts);
+  L.offsets = take(sizeof(int32_t) * (cfg->num_local_experts + 1));
+  L.sorted = take(sizeof(int32_t) * L.r_cap);
+  L.chunks = take(sizeof(int4) * L.max_chunks);
+  L.chunk_count = take(sizeof(int32_t));
+  L.h = take(sizeof(uint16_t) * (size_t)L.r_cap * L.inter_pad);
+  L.acc = take(sizeof(float) * (size_t)L.t_cap * cfg->hidden);
+  L.p = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * L.wnat);
+  L.q = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * cfg->hidden);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------- device
+struct DevInfo {
+  bool ok = false;
+  int sms = 0;
+};
+
+b4_status device_info(DevInfo& info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(B4_ERR_UNSUPPORTED_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+  static std::mutex mu;
+  static DevInfo cache[64];
+  static bool known[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && known[dev]) {
+    info = cache[dev];
+  } else {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    info.ok = major == 10 && minor == 3;
+    info.sms = sms;
+    if (dev < 64) {
+      cache[dev] = info;
+      known[dev] = true;
+    }
+  }
+  if (!info.ok) return fail(B4_ERR_UNSUPPORTED_DEVICE, "device is not sm_103 (GB300); no fallback path exists");
+  return B4_OK;
+}
+
+int pick_splits(int64_t base_units, int k_stages, int grid, int cap) {
+  int best = 1;
+  double best_eff = -1;
+  for (int s = 1; s <= cap; ++s) {
+    if (k_stages / s < 4 && s > 1) break;
+    const int64_t units = base_units * s;
+    const int64_t waves = (units + grid - 1) / grid;
+    const double eff = (double)units / (double)(waves * grid);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+template <int MODE>
+cudaError_t launch_mode(int fmt, const GemmParams& p, int grid, bool pdl, cudaStream_t st) {
+  return fmt == 0 ? launch_gemm<MODE, 0>(p, grid, pdl, st) : launch_gemm<MODE, 1>(p, grid, pdl, st);
+}
+
+}  // namespace
+
+// device-side counter of invalid scale codes found by b4_prepare_weights
+static __device__ int g_prepare_bad;
+
+extern "C" {
+
+int32_t b4_route_capacity_tokens(int32_t m) { return next_pow2(m > 0 ? m : 1); }
+
+size_t b4_workspace_bytes(const b4_moe_config* cfg, int32_t activation) {
+  if (check_config(cfg, activation) != B4_OK) return 0;
+  return ws_layout(cfg, activation).total;
+}
+
+b4_status b4_prepared_sizes(const b4_moe_config* cfg, int32_t which, int32_t activation, size_t* code_bytes,
+                            size_t* scale_bytes) {
+  b4_status st = check_config(cfg, activation);
+  if (st != B4_OK) return st;
+  if (which != 0 && which != 1) return fail(B4_ERR_INVALID_ARGUMENT, "which = %d must be 0 (W13) or 1 (W2)", which);
+  if (!code_bytes || !scale_bytes) return fail(B4_ERR_INVALID_ARGUMENT, "null output pointer");
+  const TensorGeom g = tensor_geom(which, activation, cfg->hidden, cfg->inter);
+  const size_t stages = (size_t)cfg->num_local_experts * g.n_tiles * g.k_stages;
+  *code_bytes = stages * kCodeBytesPerStage;
+  *scale_bytes = stages * scale_bytes_per_stage(cfg->format);
+  return B4_OK;
+}
+
+b4_status b4_prepare_weights(const b4_moe_config* cfg, int32_t which, int32_t activation, const uint8_t* src_codes,
+                             const uint8_t* src_scales, uint8_t* dst_codes, uint8_t* dst_scales, b4_stream_t stream) {
+  size_t cb = 0, sb = 0;
+  b4_status st = b4_prepared_sizes(cfg, which, activation, &cb, &sb);
+  if (st != B4_OK) return st;
+  if (!src_codes || !src_scales || !dst_codes || !dst_scales)
+    return fail(B4_ERR_INVALID_ARGUMENT, "null weight pointer");
+  if (!aligned(dst_codes, 16) || !aligned(dst_scales, 16))
+    return fail(B4_ERR_INVALID_ARGUMENT, "prepared buffers must be 16-byte aligned");
+  DevInfo dev;
+  if ((st = device_info(dev)) != B4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int zero = 0;
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_prepare_bad, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare: reset");
+  int* bad = nullptr;
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&bad), g_prepare_bad);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare: symbol");
+  PrepareParams p{};
+  p.src_codes = src_codes;
+  p.src_scales = src_scales;
+  p.dst_codes = dst_codes;
+  p.dst_scales = dst_scales;
+  p.num_experts = cfg->num_local_experts;
+  p.which = which;
+  p.act = activation;
+  p.fmt = cfg->format;
+  p.hidden = cfg->hidden;
+  p.inter = cfg->inter;
+  p.bad = bad;
+  if ((e = launch_prepare(p, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "prepare: launch");
+  int nbad = 0;
+  e = cudaMemcpyFromSymbolAsync(&nbad, g_prepare_bad, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare: readback");
+  if (nbad)
+    return fail(B4_ERR_INVALID_ARGUMENT,
+                "%d block scale(s) are NaN or outside the supported range (E8M0: 65..191 for nonzero blocks)", nbad);
+  return B4_OK;
+}
+
+b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                        int32_t* sorted_routes, b4_stream_t stream) {
+  b4_status st = check_config(cfg, B4_ACT_SILU_SWIGLU);
+  if (st != B4_OK) return st;
+  if ((cfg->m > 0 && !topk_ids) || !counts || !offsets || !sorted_routes)
+    return fail(B4_ERR_INVALID_ARGUMENT, "null pointer argument");
+  DevInfo dev;
+  if ((st = device_info(dev)) != B4_OK) return st;
+  RoutePackParams p{};
+  p.topk_ids = topk_ids;
+  p.expert_map = cfg->expert_map;
+  p.m = cfg->m;
+  p.top_k = cfg->top_k;
+  p.num_global_experts = cfg->num_global_experts;
+  p.num_local_experts = cfg->num_local_experts;
+  p.route_cap = b4_route_capacity_tokens(cfg->m) * cfg->top_k;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.sorted_routes = sorted_routes;
+  cudaError_t e = launch_route_pack(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? B4_OK : cuda_fail(e, "route_pack");
+}
+
+b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                       const float* gs13, const uint8_t* w2, const uint8_t* s2, const float* gs2,
+                       const int32_t* topk_ids, const float* topk_weights, int32_t activation, uint16_t* out,
+                       void* workspace, size_t workspace_bytes, b4_stream_t stream) {
+  b4_status st = check_config(cfg, activation);
+  if (st != B4_OK) return st;
+  if (cfg->m == 0) return B4_OK;  // nothing to compute, nothing launched
+  if (!x || !w13 || !s13 || !w2 || !s2 || !topk_ids || !topk_weights || !out || !workspace)
+    return fail(B4_ERR_INVALID_ARGUMENT, "null pointer argument");
+  const bool nv = cfg->format == B4_NVFP4_E4M3_K16;
+  if (nv && (!gs13 || !gs2)) return fail(B4_ERR_INVALID_ARGUMENT, "NVFP4 needs gs13 and gs2");
+  if (!nv && (gs13 || gs2)) return fail(B4_ERR_INVALID_ARGUMENT, "MXFP4 takes no global scales (pass NULL)");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(w13, 16) || !aligned(s13, 16) || !aligned(w2, 16) ||
+      !aligned(s2, 16))
+    return fail(B4_ERR_INVALID_ARGUMENT, "x, out and the weight buffers must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(B4_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if (!aligned(topk_ids, 4) || !aligned(topk_weights, 4) || (gs13 && !aligned(gs13, 4)) || (gs2 && !aligned(gs2, 4)))
+    return fail(B4_ERR_INVALID_ARGUMENT, "misaligned 32-bit array");
+  const WsLayout L = ws_layout(cfg, activation);
+  if (workspace_bytes < L.total)
+    return fail(B4_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, L.total);
+  DevInfo dev;
+  if ((st = device_info(dev)) != B4_OK) return st;
+
+  const int act = activation == B4_ACT_SILU_SWIGLU ? 0 : 1;
+  const int fmt = cfg->format;
+  bool decode = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && cfg->m <= kDecodeAutoMaxM);
+  if (decode && !L.decode_ok) decode = false;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const TensorGeom g1 = tensor_geom(0, act, cfg->hidden, cfg->inter);
+  const TensorGeom g2 = tensor_geom(1, act, cfg->hidden, cfg->inter);
+
+  GemmParams base{};
+  base.m = cfg->m;
+  base.top_k = cfg->top_k;
+  base.num_global_experts = cfg->num_global_experts;
+  base.num_local_experts = cfg->num_local_experts;
+  base.hidden = cfg->hidden;
+  base.inter = cfg->inter;
+  base.inter_pad = L.inter_pad;
+  base.act = act;
+  base.topk_ids = topk_ids;
+  base.topk_weights = topk_weights;
+  base.expert_map = cfg->expert_map;
+  base.x = x;
+  base.status = status;
+  base.max_chunks = L.max_chunks;
+
+  GemmParams p1 = base, p2 = base;
+  p1.wcodes = w13;
+  p1.wscales = s13;
+  p1.gs = gs13;
+  p1.n_tiles = g1.n_tiles;
+  p1.k_stages = g1.k_stages;
+  p2.wcodes = w2;
+  p2.wscales = s2;
+  p2.gs = gs2;
+  p2.n_tiles = g2.n_tiles;
+  p2.k_stages = g2.k_stages;
+
+  FinalizeParams fp{};
+  fp.m = cfg->m;
+  fp.top_k = cfg->top_k;
+  fp.hidden = cfg->hidden;
+  fp.num_global_experts = cfg->num_global_experts;
+  fp.num_local_experts = cfg->num_local_experts;
+  fp.topk_ids = topk_ids;
+  fp.expert_map = cfg->expert_map;
+  fp.out = out;
+
+  cudaError_t e;
+  if (decode) {
+    const int R = cfg->m * cfg->top_k;
+    const int grid_cap = 2 * dev.sms;
+    const int s1 = pick_splits((int64_t)R * g1.n_tiles, g1.k_stages, grid_cap, L.dec_splits);
+    const int s2v = pick_splits((int64_t)R * g2.n_tiles, g2.k_stages, grid_cap, L.dec_splits);
+    float* pbuf = reinterpret_cast<float*>(ws + L.p);
+    float* qbuf = reinterpret_cast<float*>(ws + L.q);
+    p1.splits = s1;
+    p1.part_out = pbuf;
+    p2.splits = s2v;
+    p2.part_out = qbuf;
+    p2.p_in = pbuf;
+    p2.splits_in = s1;
+    const int64_t u1 = (int64_t)R * g1.n_tiles * s1, u2 = (int64_t)R * g2.n_tiles * s2v;
+    const int grid1 = (int)(u1 < grid_cap ? u1 : grid_cap), grid2 = (int)(u2 < grid_cap ? u2 : grid_cap);
+    p1.clear_status = 1;
+    if ((e = launch_mode<kFc1Decode>(fmt, p1, grid1, false, s)) != cudaSuccess) return cuda_fail(e, "fc1 decode");
+    if ((e = launch_mode<kFc2Decode>(fmt, p2, grid2, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 decode");
+    fp.q = qbuf;
+    fp.splits = s2v;
+    if ((e = launch_finalize(fp, false, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize decode");
+    return B4_OK;
+  }
+
+  RoutePackParams rp{};
+  rp.topk_ids = topk_ids;
+  rp.expert_map = cfg->expert_map;
+  rp.m = cfg->m;
+  rp.top_k = cfg->top_k;
+  rp.num_global_experts = cfg->num_global_experts;
+  rp.num_local_experts = cfg->num_local_experts;
+  rp.route_cap = L.r_cap;
+  rp.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  rp.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  rp.sorted_routes = reinterpret_cast<int32_t*>(ws + L.sorted);
+  rp.chunks = reinterpret_cast<int4*>(ws + L.chunks);
+  rp.chunk_count = reinterpret_cast<int32_t*>(ws + L.chunk_count);
+  rp.chunk_rows = kChunkRows;
+  rp.status = status;
+  if ((e = launch_route_pack(rp, s)) != cudaSuccess) return cuda_fail(e, "route pack");
+
+  uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.h);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  for (GemmParams* pp : {&p1, &p2}) {
+    pp->sorted_routes = rp.sorted_routes;
+    pp->chunk_count = rp.chunk_count;
+    pp->chunks = rp.chunks;
+  }
+  p1.h_out = hbuf;
+  p1.acc_out = acc;
+  p1.acc_zero_floats = (size_t)cfg->m * cfg->hidden;
+  p1.pdl_wait_first = 1;
+  p2.h = hbuf;
+  p2.acc_out = acc;
+  if ((e = launch_mode<kFc1Grouped>(fmt, p1, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc1 grouped");
+  if ((e = launch_mode<kFc2Grouped>(fmt, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");
+  fp.acc = acc;
+  if ((e = launch_finalize(fp, true, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize grouped");
+  return B4_OK;
+}
+
+b4_status b4_check_status(void* workspace, b4_stream_t stream) {
+  if (!workspace) return fail(B4_ERR_INVALID_ARGUMENT, "workspace is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "check_status");
+  if (word[0] != 0) {
+    const uint32_t zero[2] = {0, 0};
+    e = cudaMemcpyAsync(workspace, zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "check_status reset");
+    return fail(static_cast<b4_status>(word[0]), "device reported status %u at wait site %u", word[0], word[1]);
+  }
+  return B4_OK;
+}
+
+const char* b4_status_string(int32_t status) {
+  switch (status) {
+    case B4_OK: return "B4_OK";
+    case B4_ERR_INVALID_ARGUMENT: return "B4_ERR_INVALID_ARGUMENT";
+    case B4_ERR_UNSUPPORTED_DEVICE: return "B4_ERR_UNSUPPORTED_DEVICE";
+    case B4_ERR_WORKSPACE_TOO_SMALL: return "B4_ERR_WORKSPACE_TOO_SMALL";
+    case B4_ERR_CUDA: return "B4_ERR_CUDA";
+    case B4_ERR_TIMEOUT: return "B4_ERR_TIMEOUT";
+    default: return "B4_UNKNOWN_STATUS";
+  }
+}
+
+const char* b4_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

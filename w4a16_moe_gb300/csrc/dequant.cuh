@@ -1,0 +1,59 @@
+// E2M1 x block-scale dequantisation to bf16 in registers (sm_103a).
+//
+// Shared by the GEMM kernels; it reads the serving layout that the prepare
+// kernel writes (prepare.cu).
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace b4 {
+
+// One thread, one weight row, one 64-element stage: 32 bytes of codes in the
+// serving layout (two 16-byte chunks) and the re-encoded block scales ->
+// 32 registers of packed bf16 pairs (column c holds elements 2c, 2c+1).
+//
+// Serving layout of a 32-bit code word (8 elements, pairs j = 0..3 at shifts
+// 0, 2, 16, 18): the low element of pair j keeps (e0, m) of its E2M1 code at
+// bits [1:0] and (s, e1) at [5:4]; the high element at [9:8] and [13:12].
+// With 0x4040 or-ed in, the 16 bits are a PRMT selector whose byte lookups in
+// the table {00,40,80,C0 | 00,01,80,81} assemble the bf16 bit pattern
+// s<<15 | e1<<8 | e0<<7 | m<<6 of each element: the E2M1 value times 2^-126.
+// One bf16x2 multiply by (scale * 2^63) then yields value * scale * 2^-63.
+__device__ __forceinline__ uint32_t fp4x2_lookup(uint32_t sel) {
+  return __byte_perm(0xC0804000u, 0x81800100u, (sel & 0x3333u) | 0x4040u);
+}
+
+template <int FMT>
+__device__ __forceinline__ void dequant_stage(const uint4& c0, const uint4& c1, uint32_t sc, uint32_t (&r)[32]) {
+  uint32_t s[4];
+  if constexpr (FMT == 0) {
+    // NVFP4: byte b' -> bf16 bits (b' << 4) + 0x5800 == E4M3 value * 2^63
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t bits = (((sc >> (8 * b)) & 0xFFu) << 4) + 0x5800u;
+      s[b] = bits * 0x10001u;
+    }
+  } else {
+    // MXFP4: E8M0 e -> bf16 bits (e + 63) << 7 == 2^(e-127) * 2^63
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t bits = (((sc >> (8 * b)) & 0xFFu) + 63u) << 7;
+      s[b] = bits * 0x10001u;
+    }
+    s[2] = s[3] = 0;
+  }
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t sq = FMT == 0 ? s[q >> 1] : s[q >> 2];
+    const uint32_t v = w[q];
+    r[4 * q + 0] = bf16x2_mul(fp4x2_lookup(v), sq);
+    r[4 * q + 1] = bf16x2_mul(fp4x2_lookup(v >> 2), sq);
+    r[4 * q + 2] = bf16x2_mul(fp4x2_lookup(v >> 16), sq);
+    r[4 * q + 3] = bf16x2_mul(fp4x2_lookup(v >> 18), sq);
+  }
+}
+
+}  // namespace b4

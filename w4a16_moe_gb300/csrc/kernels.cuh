@@ -1,0 +1,122 @@
+// Kernel parameter blocks and layout constants shared by the host dispatch
+// and the CUDA kernels of the fused W4A16 MoE layer.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace b4 {
+
+// ---------------------------------------------------------------- tiling
+constexpr int kTileRows = 128;   // weight rows per tile (tcgen05 M)
+constexpr int kBK = 64;          // K elements per pipeline stage
+constexpr int kCodeBytesPerStage = kTileRows * kBK / 2;  // 4096: [2 chunks][128 rows][16 B]
+constexpr int kChunkRows = 192;  // max routes of one expert per grouped work unit (tcgen05 N)
+
+__host__ __device__ constexpr int scale_bytes_per_row(int fmt) { return fmt == 0 ? kBK / 16 : kBK / 32; }
+__host__ __device__ constexpr int scale_bytes_per_stage(int fmt) { return kTileRows * scale_bytes_per_row(fmt); }
+__host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int round_up(int a, int b) { return cdiv(a, b) * b; }
+
+// Serving-layout geometry of one tensor.
+struct TensorGeom {
+  int rows_valid;  // N of the source tensor
+  int k_valid;     // K of the source tensor
+  int n_tiles;     // 128-row tiles
+  int k_stages;    // 64-element stages
+};
+
+// which: 0 = W13/W1, 1 = W2.  act: 0 = SwiGLU, 1 = ReLU^2.
+__host__ __device__ inline TensorGeom tensor_geom(int which, int act, int hidden, int inter) {
+  TensorGeom g;
+  const int inter_pad = round_up(inter, kBK);
+  if (which == 0) {
+    g.rows_valid = act == 0 ? 2 * inter : inter;
+    g.k_valid = hidden;
+    g.n_tiles = act == 0 ? inter_pad / 64 : cdiv(inter, kTileRows);
+    g.k_stages = cdiv(hidden, kBK);
+  } else {
+    g.rows_valid = hidden;
+    g.k_valid = inter;
+    g.n_tiles = cdiv(hidden, kTileRows);
+    g.k_stages = inter_pad / kBK;
+  }
+  return g;
+}
+
+enum GemmMode : int { kFc1Grouped = 0, kFc2Grouped = 1, kFc1Decode = 2, kFc2Decode = 3 };
+
+struct GemmParams {
+  // prepared weights of this GEMM
+  const uint8_t* wcodes;
+  const uint8_t* wscales;
+  const float* gs;      // [E_l] or null (MXFP4)
+  int n_tiles, k_stages;
+  // layer shape
+  int m, top_k, num_global_experts, num_local_experts, hidden, inter, inter_pad;
+  int act;              // 0 SwiGLU, 1 ReLU^2
+  // routing inputs
+  const int32_t* topk_ids;
+  const float* topk_weights;
+  const int32_t* expert_map;  // or null
+  // grouped schedule (from the route-pack kernel)
+  const int32_t* sorted_routes;
+  const int32_t* chunk_count;
+  const int4* chunks;   // (expert, first slot, rows, 0)
+  int max_chunks;
+  // B operand sources
+  const uint16_t* x;    // [m, H] bf16 (FC1)
+  const uint16_t* h;    // [R_cap, I_pad] bf16 (FC2 grouped)
+  const float* p_in;    // decode FC1 partials (FC2 decode)
+  int splits_in;        // number of FC1 partial splits (FC2 decode)
+  // outputs
+  uint16_t* h_out;      // FC1 grouped
+  float* acc_out;       // FC2 grouped: [T_cap, H] fp32, zeroed by FC1 grouped
+  size_t acc_zero_floats;  // FC1 grouped: floats of acc_out to clear
+  float* part_out;      // decode partials: FC1 -> p [S][R][N1nat], FC2 -> q [S][R][H]
+  int splits;           // split count of this decode GEMM
+  uint32_t* status;     // device status word(s)
+  int pdl_wait_first;   // all threads wait on the previous grid before starting
+  int clear_status;     // block 0 resets the status word (first kernel of a call)
+};
+
+struct RoutePackParams {
+  const int32_t* topk_ids;
+  const int32_t* expert_map;
+  int m, top_k, num_global_experts, num_local_experts;
+  int route_cap;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_routes;
+  // optional grouped-GEMM schedule
+  int4* chunks;
+  int32_t* chunk_count;
+  int chunk_rows;
+  uint32_t* status;     // reset to 0 (first kernel of a grouped call), or null
+};
+
+struct FinalizeParams {
+  int m, top_k, hidden, num_global_experts, num_local_experts;
+  const int32_t* topk_ids;
+  const int32_t* expert_map;
+  const float* acc;     // grouped: [m, H]
+  const float* q;       // decode: [S][R][H]
+  int splits;
+  uint16_t* out;
+};
+
+struct PrepareParams {
+  const uint8_t* src_codes;
+  const uint8_t* src_scales;
+  uint8_t* dst_codes;
+  uint8_t* dst_scales;
+  int num_experts, which, act, fmt, hidden, inter;
+  int* bad;             // device counter of invalid scale codes
+};
+
+// decode-split partial layout (FC1): natural index of a prepared row
+__host__ __device__ inline int fc1_natural_width(int act, int inter_pad) {
+  return act == 0 ? 2 * inter_pad : inter_pad;
+}
+
+}  // namespace b4

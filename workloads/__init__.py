@@ -64,16 +64,27 @@ class Workload:
         return dataclasses.replace(self, act=act)
 
     def scaled(self, hidden=None, inter=None, experts=None, top_k=None) -> "Workload":
-        """Same structure, smaller sizes (for fast parity cases)."""
+        """Same structure, smaller sizes (for fast parity cases).
+
+        A workload that drops global experts keeps the same number of drops,
+        spread over the smaller global range.
+        """
         e = experts or self.num_local_experts
-        eg = e + (self.num_global_experts - self.num_local_experts)
+        n_drop = len(self.drop_globals)
+        eg = e + n_drop
+        drops = ()
+        if n_drop:
+            step = max(1, eg // n_drop)
+            drops = tuple(range(min(3, step - 1), eg, step))[:n_drop]
         return dataclasses.replace(
             self,
             hidden=hidden or self.hidden,
             inter=inter or self.inter,
             num_local_experts=e,
             num_global_experts=eg,
+            drop_globals=drops,
             top_k=top_k or self.top_k,
+            hot_experts=min(self.hot_experts, e // 2),
         )
 
 
