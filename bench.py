@@ -1,0 +1,481 @@
+#!/usr/bin/env python
+"""Benchmark of the fused W4A16 MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one call of the whole layer (route handling, FC1 + activation, FC2 +
+top-k combine) on one batch of synthetic inputs.  The headline workload is
+the decode MoE (NVFP4, E=128, top_k=8, H=4096, I=1536, ReLU^2, m=1); the
+metric is microseconds per call (lower is better).  Timed with CUDA events
+around CUDA-graph replays of the call on the launching stream, L2 flushed
+(a 512 MiB write) before every timed step, inputs already resident in HBM.
+
+Besides the headline it reports, in "secondary", the same measurement for
+the other workloads (decode m=2, 4; small-batch m=16, 64; prefill m=2048 with
+SwiGLU and ReLU^2; MXFP4 m=512), each with its weight-stream TB/s and bf16
+TFLOP/s, "roofline" for the dominant kernel (the W4A16 GEMM, timed per launch
+with the library's timing events), "cpu_baseline" (the float64 CPU oracle on a
+bounded sample), "e2e" (the same call through the Python API with inputs
+copied from pinned host memory and the result read back every step) and the
+SM clocks sampled during the timed region.
+
+Replicas only: under torchrun every rank runs the same workload on its own GPU
+with no collective on the data path; rank 0 prints the max over ranks.
+``--impl reference`` times the CPU oracle instead (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused W4A16 MoE µs/call; weight-stream TB/s (m≤16), bf16 TFLOPS (m=2048)"
+HEADLINE = ("decode", "relu2", 1)
+SECONDARY = [("decode", "relu2", 2), ("decode", "relu2", 4), ("small", "silu", 16), ("small", "silu", 64),
+             ("prefill", "silu", 2048), ("prefill", "relu2", 2048), ("mxfp4", "silu", 512)]
+L2_FLUSH_BYTES = 512 << 20
+DRAWS = 8  # independent routing / activation draws cycled through the steps
+
+
+def describe(wl, m):
+    return (f"{wl.name} {'NVFP4' if wl.fmt.startswith('nvfp4') else 'MXFP4'} MoE: E_g={wl.num_global_experts} "
+            f"E_l={wl.num_local_experts} top_k={wl.top_k} H={wl.hidden} I={wl.inter} "
+            f"{'SiLU-SwiGLU' if wl.act == 'silu' else 'ReLU^2'} m={m}")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# --------------------------------------------------------------- accounting
+def tensor_bytes(wl, which):
+    """Unpadded bytes of one expert's codes + scales (+ fp32 global scale)."""
+    n, k = (wl.n1, wl.hidden) if which == 0 else (wl.hidden, wl.inter)
+    return n * k // 2 + n * k // wl.group + (4 if wl.fmt.startswith("nvfp4") else 0)
+
+
+def local_experts_np(wl, ids, em):
+    ids = np.asarray(ids, dtype=np.int64)
+    valid = (ids >= 0) & (ids < wl.num_global_experts)
+    loc = np.where(valid, ids, 0)
+    if em is not None:
+        loc = np.asarray(em, dtype=np.int64)[loc]
+    valid &= (loc >= 0) & (loc < wl.num_local_experts)
+    return np.where(valid, loc, -1)
+
+
+def call_accounting(wl, m, ids, em):
+    loc = local_experts_np(wl, ids, em)
+    hit = np.unique(loc[loc >= 0])
+    r_valid = int((loc >= 0).sum())
+    b13 = len(hit) * tensor_bytes(wl, 0)
+    b2 = len(hit) * tensor_bytes(wl, 1)
+    io = m * wl.hidden * 2 * 2 + m * wl.top_k * 8  # x, out, ids, router weights
+    f13 = 2.0 * r_valid * wl.n1 * wl.hidden
+    f2 = 2.0 * r_valid * wl.hidden * wl.inter
+    return {"bytes": b13 + b2 + io, "weight_bytes": b13 + b2, "fc1_bytes": b13 + m * wl.hidden * 2,
+            "fc2_bytes": b2, "flops": f13 + f2, "experts_hit": int(len(hit)), "routes": r_valid}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            return
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+class Bench:
+    def __init__(self, wl, m, seed=7):
+        import torch
+
+        import w4a16_moe_gb300 as b4
+        import workloads as W
+
+        self.torch, self.b4, self.W = torch, b4, W
+        self.wl, self.m = wl, m
+        self.act = b4.ACTIVATIONS[wl.act]
+        self.em_np = W.expert_map(wl)
+        em = None if self.em_np is None else torch.from_numpy(self.em_np).cuda()
+        self.cfg = b4.MoEConfig(m, wl.top_k, wl.num_global_experts, wl.num_local_experts, wl.hidden, wl.inter,
+                                format=b4.FORMATS[wl.fmt], expert_map=em)
+        self.host = {}
+        dev = {}
+        for which, name in ((0, "13"), (1, "2")):
+            c, s, g = W.random_codes(wl, seed, which)
+            self.host["c" + name], self.host["s" + name], self.host["g" + name] = c, s, g
+            wc, ws = b4.prepare_weights(self.cfg, which, self.act, torch.from_numpy(c).cuda(),
+                                        torch.from_numpy(s).cuda())
+            dev["w" + name], dev["s" + name] = wc, ws
+            dev["g" + name] = None if g is None else torch.from_numpy(g).cuda()
+        self.dev = dev
+        self.draws = []
+        for d in range(DRAWS):
+            xb, x = W.activations(wl, m, seed=100 + d)
+            ids, wts = W.routing(wl, m, seed=100 + d)
+            self.draws.append({
+                "x_bits": xb, "x": x, "ids": ids, "wts": wts,
+                "xd": torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16),
+                "idsd": torch.from_numpy(ids).cuda(), "wtsd": torch.from_numpy(wts).cuda(),
+                "acct": call_accounting(wl, m, ids, self.em_np)})
+        self.ws = torch.empty(b4.workspace_bytes(self.cfg, self.act), dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(m, wl.hidden, dtype=torch.bfloat16, device="cuda")
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.stream = torch.cuda.Stream()
+        self.decode = m <= 4
+        self.n_kernels = 3 if self.decode else 4
+
+    def call(self, d, stream=None):
+        dv = self.dev
+        self.b4.fused_moe(self.cfg, d["xd"], dv["w13"], dv["s13"], dv["g13"], dv["w2"], dv["s2"], dv["g2"], d["idsd"],
+                          d["wtsd"], self.act, self.out, self.ws, stream=stream)
+
+    def capture(self, timing_events=None):
+        torch = self.torch
+        graphs = []
+        with torch.cuda.stream(self.stream):
+            for d in self.draws:  # eager warm-up (sets kernel attributes before capture)
+                self.call(d, self.stream)
+        self.stream.synchronize()
+        self.b4.check_status(self.ws, self.stream)
+        if timing_events is not None:
+            self.b4.set_timing_events(timing_events)
+        try:
+            for d in self.draws:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    self.call(d, self.stream)
+                graphs.append(g)
+        finally:
+            if timing_events is not None:
+                self.b4.set_timing_events(None)
+        return graphs
+
+    def time_steps(self, graphs, steps, warmup, barrier=None, kernel_events=None):
+        torch = self.torch
+        for i in range(warmup):
+            with torch.cuda.stream(self.stream):
+                self.flush.zero_()
+                graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        kern = []
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            for i in range(steps):
+                self.flush.zero_()
+                starts[i].record(self.stream)
+                graphs[i % len(graphs)].replay()
+                ends[i].record(self.stream)
+                if kernel_events is not None:
+                    self.stream.synchronize()
+                    kern.append([kernel_events[j].elapsed_time(kernel_events[j + 1])
+                                 for j in range(len(kernel_events) - 1)])
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        wall = time.perf_counter() - t_wall
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return ms, kern, wall
+
+    def run(self, steps, warmup, barrier=None, with_e2e=False, with_clocks=False, gpu_index=0):
+        torch = self.torch
+        graphs = self.capture()
+        clocks = None
+        if with_clocks:
+            with ClockSampler(gpu_index) as cs:
+                ms, _, wall = self.time_steps(graphs, steps, warmup, barrier)
+            clocks = cs.summary()
+        else:
+            ms, _, wall = self.time_steps(graphs, steps, warmup, barrier)
+        # per-kernel durations: the same graphs with timing events between kernels
+        kev = [torch.cuda.Event(enable_timing=True) for _ in range(self.n_kernels + 1)]
+        tgraphs = self.capture(timing_events=kev)
+        _, kern, _ = self.time_steps(tgraphs, steps, 1, None, kernel_events=kev)
+        accts = [self.draws[i % DRAWS]["acct"] for i in range(steps)]
+        res = {"ms": ms, "kern": kern, "accts": accts, "wall": wall, "clocks": clocks}
+        if with_e2e:
+            res["e2e_s"] = self.e2e_timed(steps, warmup)
+        return res
+
+    def e2e_timed(self, steps, warmup):
+        torch = self.torch
+        pins = []
+        for d in self.draws:
+            pins.append({"x": torch.from_numpy(d["x_bits"].view(np.int16).copy()).pin_memory(),
+                         "ids": torch.from_numpy(d["ids"].copy()).pin_memory(),
+                         "wts": torch.from_numpy(d["wts"].copy()).pin_memory()})
+        out_h = torch.empty(self.m, self.wl.hidden, dtype=torch.int16).pin_memory()
+        xd = torch.empty(self.m, self.wl.hidden, dtype=torch.int16, device="cuda")
+        idsd = torch.empty(self.m, self.wl.top_k, dtype=torch.int32, device="cuda")
+        wtsd = torch.empty(self.m, self.wl.top_k, dtype=torch.float32, device="cuda")
+        dv, s = self.dev, self.stream
+
+        def one(i):
+            p = pins[i % len(pins)]
+            with torch.cuda.stream(s):
+                xd.copy_(p["x"], non_blocking=True)
+                idsd.copy_(p["ids"], non_blocking=True)
+                wtsd.copy_(p["wts"], non_blocking=True)
+                self.b4.fused_moe(self.cfg, xd.view(torch.bfloat16), dv["w13"], dv["s13"], dv["g13"], dv["w2"],
+                                  dv["s2"], dv["g2"], idsd, wtsd, self.act, self.out, self.ws, stream=s)
+                out_h.copy_(self.out.view(torch.int16), non_blocking=True)
+            s.synchronize()
+
+        for i in range(warmup):
+            one(i)
+        total = 0.0
+        for i in range(steps):
+            with torch.cuda.stream(s):
+                self.flush.zero_()
+            s.synchronize()
+            ta = time.perf_counter()
+            one(i)
+            total += time.perf_counter() - ta
+        h2d = self.m * self.wl.hidden * 2 + self.m * self.wl.top_k * 8
+        d2h = self.m * self.wl.hidden * 2
+        return {"seconds": total, "h2d": h2d, "d2h": d2h}
+
+
+def summarize(b: Bench, res, peaks):
+    wl, m = b.wl, b.m
+    ms = res["ms"]
+    us = 1e3 * statistics.mean(ms)
+    acct_bytes = statistics.mean(a["bytes"] for a in res["accts"])
+    acct_flops = statistics.mean(a["flops"] for a in res["accts"])
+    wbytes = statistics.mean(a["weight_bytes"] for a in res["accts"])
+    # GEMM kernels: decode kernels 0 (FC1) and 1 (FC2); grouped kernels 1 and 2
+    gi = (0, 1) if b.decode else (1, 2)
+    kern = res["kern"]
+    gemm_ms = [k[gi[0]] + k[gi[1]] for k in kern]
+    gemm_s = 1e-3 * statistics.mean(gemm_ms)
+    g_bytes = statistics.mean(a["fc1_bytes"] + a["fc2_bytes"] for a in res["accts"])
+    out = {
+        "workload": describe(wl, m),
+        "us_per_call": round(us, 3),
+        "us_per_call_median": round(1e3 * statistics.median(ms), 3),
+        "tokens_per_s": round(m / (us * 1e-6), 1),
+        "weight_stream_TBps": round(wbytes / (us * 1e-6) / 1e12, 4),
+        "algorithmic_TBps": round(acct_bytes / (us * 1e-6) / 1e12, 4),
+        "bf16_TFLOPs": round(acct_flops / (us * 1e-6) / 1e12, 2),
+        "experts_hit_mean": round(statistics.mean(a["experts_hit"] for a in res["accts"]), 2),
+        "kernel_us_mean": [round(1e3 * statistics.mean(k[j] for k in kern), 3) for j in range(len(kern[0]))],
+        "gemm_us": round(gemm_s * 1e6, 3),
+    }
+    if b.decode or m <= 64:
+        ach = g_bytes / gemm_s / 1e9
+        out["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                           "peak_src": peaks["src"]}
+    else:
+        ach = acct_flops / gemm_s / 1e12
+        out["roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+                           "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
+                           "peak_src": peaks["src"]}
+    return out
+
+
+def cpu_baseline(b: Bench, budget_s=15.0, max_calls=20):
+    """The float64 oracle as it stands on the host cores, on a bounded sample of the headline workload."""
+    from oracle import moe as M
+
+    h, wl = b.host, b.wl
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_calls and (time.perf_counter() - t0) < budget_s:
+        d = b.draws[n % DRAWS]
+        M.fused_moe(d["x"], h["c13"], h["s13"], h["g13"], h["c2"], h["s2"], h["g2"], d["ids"], d["wts"], wl.act,
+                    wl.fmt, wl.num_global_experts, expert_map=b.em_np)
+        n += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(dt / n * 1e6, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
+            "sample": f"{n} full calls of the headline workload ({describe(wl, b.m)}), float64 numpy, "
+                      f"{dt:.1f} s; numpy/BLAS default threading on {cores} host cores"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, as it stands, on a bounded sample of the headline workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import workloads as W
+    from oracle import moe as M
+
+    name, act, m = HEADLINE
+    wl = W.WORKLOADS[name].with_act(act)
+    c13, s13, g13 = W.random_codes(wl, 7, 0)
+    c2, s2, g2 = W.random_codes(wl, 7, 1)
+    em = W.expert_map(wl)
+    draws = [(W.activations(wl, m, 100 + d)[1],) + W.routing(wl, m, 100 + d) for d in range(DRAWS)]
+
+    def step(i):
+        x, ids, wts = draws[i % DRAWS]
+        M.fused_moe(x, c13, s13, g13, c2, s2, g2, ids, wts, wl.act, wl.fmt, wl.num_global_experts, expert_map=em)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    us = dt / args.steps * 1e6
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/call", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(wl, m), "weights": "random E2M1 codes, plausible block scales"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full calls of the headline workload after {args.warmup} warm-up"},
+        "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    barrier = None
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = dist.barrier
+
+    import workloads as W
+
+    peaks = load_peaks()
+    name, act, m = HEADLINE
+    b = Bench(W.WORKLOADS[name].with_act(act), m)
+    res = b.run(args.steps, args.warmup, barrier, with_e2e=True, with_clocks=True, gpu_index=local)
+    head = summarize(b, res, peaks)
+    us = head["us_per_call"]
+    if dist is not None:
+        t = torch.tensor([us], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us = float(t.item())
+    e2e = res["e2e_s"]
+    e2e_us = e2e["seconds"] / args.steps * 1e6
+    line = {
+        "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1e3, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random FP4 codes, softmax top-k routing)",
+        "config": {"workload": head["workload"], "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step (512 MiB write)", "launch": "CUDA graph per call",
+                   "tokens_per_s": round(head["tokens_per_s"] * world, 1),
+                   "weight_stream_TBps": head["weight_stream_TBps"], "bf16_TFLOPs": head["bf16_TFLOPs"]},
+        "roofline": {k: v for k, v in head["roofline"].items() if k != "peak_src"},
+        "roofline_note": f"dominant kernel: W4A16 GEMM (FC1 + FC2 launches), peak of {head['roofline']['peak_src']} "
+                         f"MEASURED_PEAKS.json",
+        "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": b.n_kernels * args.steps,
+        "clocks": res["clocks"],
+        "kernel_us_mean": head["kernel_us_mean"],
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(b)
+    if not args.no_secondary:
+        sec = []
+        for nm, ac, mm in SECONDARY:
+            bb = Bench(W.WORKLOADS[nm].with_act(ac), mm)
+            r = bb.run(min(args.steps, 10), 3, barrier)
+            sec.append(summarize(bb, r, peaks))
+            del bb
+            torch.cuda.empty_cache()
+        line["secondary"] = sec
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

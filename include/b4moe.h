@@ -169,6 +169,17 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
                        const int32_t* topk_ids, const float* topk_weights, int32_t activation, uint16_t* out,
                        void* workspace, size_t workspace_bytes, b4_stream_t stream);
 
+/* Optional per-kernel timing.  events: host array of n cudaEvent_t handles
+ * (created by the caller), or NULL to turn timing off.  While set, each
+ * b4_fused_moe call on this thread records events[0] on its stream before its
+ * first kernel and events[i+1] after kernel i, so n must be at least the
+ * number of kernels plus one: the decode path launches 3 kernels (FC1, FC2,
+ * finalize), the grouped path 4 (route pack, FC1, FC2, finalize).  An event
+ * recorded between two kernels removes their programmatic overlap, so timed
+ * calls can be slightly slower than untimed ones; use this for measurement.
+ * Returns B4_ERR_INVALID_ARGUMENT when 0 < n < 4 or events is NULL with n > 0. */
+b4_status b4_set_timing_events(void* const* events, int32_t n);
+
 /* Synchronises `stream`, then reads the device status word of `workspace`
  * (written by b4_fused_moe's kernels): B4_OK, or B4_ERR_TIMEOUT if a bounded
  * device wait ran out.  Resets the word to B4_OK.  Not capture-safe. */

@@ -1,6 +1,6 @@
 """Parity of b4_fused_moe with the oracle.
 
-Tolerance (fixed by the benchmark spec): max|gpu - oracle| <= 1e-2 * max|oracle|
+Tolerance: max|gpu - oracle| <= 1e-2 * max|oracle|
 and sum|gpu - oracle| / sum|oracle| <= 5e-3, per call.
 
 * scaled-down workloads with N(0, 0.02) weights quantised by the oracle,

@@ -79,6 +79,7 @@ def _load():
         "b4_route_pack": (I32, [CP, P, P, P, P, P]),
         "b4_fused_moe": (I32, [CP, P, P, P, P, P, P, P, P, P, I32, P, P, S, P]),
         "b4_check_status": (I32, [P, P]),
+        "b4_set_timing_events": (I32, [ctypes.POINTER(P), I32]),
         "b4_status_string": (ctypes.c_char_p, [I32]),
         "b4_last_error": (ctypes.c_char_p, []),
     }
@@ -98,6 +99,7 @@ EXPORTED = (
     "b4_route_pack",
     "b4_fused_moe",
     "b4_check_status",
+    "b4_set_timing_events",
     "b4_status_string",
     "b4_last_error",
 )
@@ -229,6 +231,21 @@ def fused_moe_raw(cfg: MoEConfig, ptrs: dict, activation: int, workspace_ptr: in
     return int(_lib.b4_fused_moe(ctypes.byref(c), ptrs["x"], ptrs["w13"], ptrs["s13"], ptrs.get("gs13"), ptrs["w2"],
                                  ptrs["s2"], ptrs.get("gs2"), ptrs["topk_ids"], ptrs["topk_weights"], int(activation),
                                  ptrs["out"], workspace_ptr, workspace_bytes_, stream_handle))
+
+
+_timing_keepalive = None
+
+
+def set_timing_events(events):
+    """Per-kernel timing: a list of torch.cuda.Event(enable_timing=True), or None to stop."""
+    global _timing_keepalive
+    if events is None:
+        _timing_keepalive = None
+        _check(_lib.b4_set_timing_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _timing_keepalive = arr
+    _check(_lib.b4_set_timing_events(arr, len(events)))
 
 
 def check_status(workspace, stream=None):

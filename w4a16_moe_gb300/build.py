@@ -62,7 +62,10 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
     if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
         return LIB
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    # one CUDA runtime per process: link the shared cudart (the one torch and
+    # other CUDA libraries load), so streams under graph capture, events and
+    # contexts are the same objects on both sides
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
@@ -77,7 +80,7 @@ def build_probe() -> str:
     out = os.path.join(ROOT, "tests", "csrc", "libb4probe.so")
     if os.path.exists(out) and os.path.getmtime(out) >= max(os.path.getmtime(src), _newest_header()):
         return out
-    cmd = [nvcc(), *ARCH, *FLAGS, "-shared", src, "-o", out + ".tmp"]
+    cmd = [nvcc(), *ARCH, *FLAGS, "-shared", "-cudart", "shared", src, "-o", out + ".tmp"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{res.stdout}\n{res.stderr}")

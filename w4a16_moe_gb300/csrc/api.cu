@@ -29,6 +29,14 @@ using namespace b4;
 namespace {
 
 thread_local std::string g_last_error;
+thread_local void* const* g_events = nullptr;  // b4_set_timing_events
+thread_local int g_num_events = 0;
+
+// Records timing event i (if timing is on).
+cudaError_t mark(int i, cudaStream_t s) {
+  if (!g_events || i >= g_num_events) return cudaSuccess;
+  return cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_events[i]), s);
+}
 
 b4_status fail(b4_status st, const char* fmt, ...) {
   char buf[512];
@@ -359,11 +367,15 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     const int64_t u1 = (int64_t)R * g1.n_tiles * s1, u2 = (int64_t)R * g2.n_tiles * s2v;
     const int grid1 = (int)(u1 < grid_cap ? u1 : grid_cap), grid2 = (int)(u2 < grid_cap ? u2 : grid_cap);
     p1.clear_status = 1;
+    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     if ((e = launch_mode<kFc1Decode>(fmt, p1, grid1, false, s)) != cudaSuccess) return cuda_fail(e, "fc1 decode");
+    if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     if ((e = launch_mode<kFc2Decode>(fmt, p2, grid2, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 decode");
+    if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     fp.q = qbuf;
     fp.splits = s2v;
     if ((e = launch_finalize(fp, false, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize decode");
+    if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     return B4_OK;
   }
 
@@ -382,7 +394,9 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   rp.chunk_count = reinterpret_cast<int32_t*>(ws + L.chunk_count);
   rp.chunk_rows = kChunkRows;
   rp.status = status;
+  if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   if ((e = launch_route_pack(rp, s)) != cudaSuccess) return cuda_fail(e, "route pack");
+  if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
 
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.h);
   float* acc = reinterpret_cast<float*>(ws + L.acc);
@@ -398,9 +412,19 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   p2.h = hbuf;
   p2.acc_out = acc;
   if ((e = launch_mode<kFc1Grouped>(fmt, p1, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc1 grouped");
+  if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   if ((e = launch_mode<kFc2Grouped>(fmt, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");
+  if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   fp.acc = acc;
   if ((e = launch_finalize(fp, true, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize grouped");
+  if ((e = mark(4, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+  return B4_OK;
+}
+
+b4_status b4_set_timing_events(void* const* events, int32_t n) {
+  if (n > 0 && (!events || n < 4)) return fail(B4_ERR_INVALID_ARGUMENT, "need NULL or at least 4 events");
+  g_events = n > 0 ? events : nullptr;
+  g_num_events = n > 0 ? n : 0;
   return B4_OK;
 }
 
