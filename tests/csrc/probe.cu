@@ -9,6 +9,7 @@
 #include "dequant.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tma.cuh"
 
 using namespace b4;
 
@@ -71,6 +72,295 @@ __global__ void probe_mma_kernel(const uint16_t* A, const uint16_t* B, int N, fl
   if (warp == 0) tmem_dealloc(base, 512);
 }
 
+// D[128][16] = A[128][64] x B^T where B's row 0 is the contiguous 64-element
+// row `x` held in natural order and the descriptor uses a 16-byte K stride and
+// a zero N stride (the decode path's single-row B operand).  Rows 1..15 of B
+// then read shifted / repeated data: only column 0 (and its copy, column 8)
+// is meaningful.
+__global__ void probe_mma_rowb_kernel(const uint16_t* A, const uint16_t* x, float* D, uint32_t* status) {
+  __shared__ __align__(1024) uint8_t sB[128 + 256];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const Abort ab{status, &abort_flag};
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem, 256);
+    tmem_relinquish();
+  }
+  for (int i = tid; i < (128 + 256) / 2; i += blockDim.x)
+    reinterpret_cast<uint16_t*>(sB)[i] = i < 64 ? x[i] : (uint16_t)0x7FC0;  // NaN slack
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t base = tmem;
+  uint32_t r[32];
+  for (int c = 0; c < 32; ++c) r[c] = (uint32_t)A[tid * 64 + 2 * c] | ((uint32_t)A[tid * 64 + 2 * c + 1] << 16);
+  tmem_st32(base + ((uint32_t)(32 * warp) << 16), r);
+  tmem_st_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16_m128(16);
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ts(base + 128, base + kk * 8, smem_desc_noswizzle(smem_u32(sB) + kk * 32, 16, 0), idesc,
+                  kk > 0 ? 1u : 0u);
+    mma_commit(&bar);
+  }
+  const bool ok = mbar_wait(&bar, 0, ab, 101);
+  tc_fence_after();
+  if (ok) {
+    uint32_t v[16];
+    tmem_ld16(base + ((uint32_t)(32 * warp) << 16) + 128, v);
+    tmem_ld_wait();
+    for (int j = 0; j < 16; ++j) D[tid * 16 + j] = __uint_as_float(v[j]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(base, 256);
+}
+
+// Latency microbenchmark of the tensor-memory building blocks (cycles):
+// out[0] tcgen05.st 32x32b.x32 + wait::st, out[1] tcgen05.ld 32x32b.x16 +
+// wait::ld (both per warp, averaged), out[2] four M128 N16 K16 MMAs + commit
+// observed on the mbarrier, out[3] the same with N = 160.
+__global__ void probe_tmem_latency_kernel(long long* out, uint32_t* status) {
+  __shared__ __align__(1024) uint8_t sB[160 * 128];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Abort ab{status, &abort_flag};
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem, 512);
+    tmem_relinquish();
+  }
+  for (int i = tid; i < 160 * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sB)[i] = 0;
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t base = tmem;
+  const uint32_t lb = (uint32_t)(32 * warp) << 16;
+  uint32_t r[32];
+  for (int c = 0; c < 32; ++c) r[c] = 0x3F803F80u;
+  long long t_st = 0, t_ld = 0;
+  for (int it = 0; it < 64; ++it) {
+    const long long t0 = clock64();
+    tmem_st32(base + lb + (it % 6) * 32, r);
+    tmem_st_wait();
+    const long long t1 = clock64();
+    uint32_t v[16];
+    tmem_ld16(base + lb + 256, v);
+    tmem_ld_wait();
+    const long long t2 = clock64();
+    t_st += t1 - t0;
+    t_ld += t2 - t1;
+    r[it & 31] ^= v[it & 15] & 1u;
+  }
+  if (lane == 0) {
+    atomicAdd(reinterpret_cast<unsigned long long*>(&out[0]), (unsigned long long)(t_st / 64));
+    atomicAdd(reinterpret_cast<unsigned long long*>(&out[1]), (unsigned long long)(t_ld / 64));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    uint32_t phase = 0;
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t n = which == 0 ? 16u : 160u;
+      const uint32_t idesc = idesc_bf16_m128(n);
+      long long tot = 0;
+      for (int it = 0; it < 32 && !ab.raised(); ++it) {
+        const long long t0 = clock64();
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts(base + 192, base + kk * 8, smem_desc_noswizzle(smem_u32(sB) + kk * 256, 128, 1024), idesc,
+                      kk > 0 ? 1u : 0u);
+        mma_commit(&bar);
+        if (!mbar_wait(&bar, phase, ab, 102)) break;
+        phase ^= 1;
+        tot += clock64() - t0;
+      }
+      out[2 + which] = tot / 32;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(base, 512);
+}
+
+// TMA probes: a 2-D tile box and a gather4 (4 rows) into 128-byte-swizzled
+// shared memory, dumped raw so the test can check the swizzle pattern.
+__global__ void probe_tma_kernel(const __grid_constant__ CUtensorMap tm, int mode, int c0, int r0, int r1, int r2,
+                                 int r3, int box_rows, int dst_off, uint8_t* out, uint32_t* status) {
+  __shared__ __align__(1024) uint8_t s[256 * 128];
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const Abort ab{status, &abort_flag};
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 256 * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(s)[i] = 0xA5A5A5A5u;
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    if (mode == 0) {
+      mbar_arrive_expect_tx(&bar, (uint32_t)box_rows * 128);
+      tma_load_2d(s + dst_off, &tm, c0, r0, &bar);
+    } else {
+      mbar_arrive_expect_tx(&bar, 4 * 128);
+      tma_gather4(s + dst_off, &tm, c0, r0, r1, r2, r3, &bar);
+    }
+  }
+  const bool ok = mbar_wait(&bar, 0, ab, 110);
+  __syncthreads();
+  if (ok)
+    for (int i = tid; i < 256 * 128; i += blockDim.x) out[i] = s[i];
+}
+
+// D[128][N] = A[128][64] x B[N][64]^T with B loaded by one TMA box into the
+// 128-byte-swizzled K-major layout and read through a swizzled descriptor.
+__global__ void probe_mma_sw128_kernel(const __grid_constant__ CUtensorMap tm, const uint16_t* A, int N, float* D,
+                                       uint32_t* status) {
+  __shared__ __align__(1024) uint8_t sB[256 * 128];
+  __shared__ uint64_t bar, bar2;
+  __shared__ uint32_t tmem;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const Abort ab{status, &abort_flag};
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    mbar_init(&bar2, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t base = tmem;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)N * 128);
+    tma_load_2d(sB, &tm, 0, 0, &bar);
+  }
+  uint32_t r[32];
+  for (int c = 0; c < 32; ++c) r[c] = (uint32_t)A[tid * 64 + 2 * c] | ((uint32_t)A[tid * 64 + 2 * c + 1] << 16);
+  tmem_st32(base + ((uint32_t)(32 * warp) << 16), r);
+  tmem_st_wait();
+  tc_fence_before();
+  bool ok = mbar_wait(&bar, 0, ab, 111);
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {
+    const uint32_t idesc = idesc_bf16_m128((uint32_t)N);
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ts(base + 128, base + kk * 8, smem_desc_sw128(smem_u32(sB) + kk * 32), idesc, kk > 0 ? 1u : 0u);
+    mma_commit(&bar2);
+  }
+  ok = mbar_wait(&bar2, 0, ab, 112) && ok;
+  tc_fence_after();
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(base + ((uint32_t)(32 * warp) << 16) + 128 + c0, v);
+      tmem_ld_wait();
+      for (int j = 0; j < 16; ++j) D[tid * N + c0 + j] = __uint_as_float(v[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(base, 512);
+}
+
+// MMA issue throughput: 64 stages of `per` K=16 MMAs, one commit every
+// `per_commit` MMAs (0: none until the end), timed from the first issue to
+// the completion of the last (cycles).  variant bit 0: N = 160 (else 16);
+// bit 1: A from shared memory (else TMEM); bit 2: per stage, also wait on an
+// already-completed mbarrier and fence; bit 3: N = 256.
+__global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long long* out, uint32_t* status) {
+  __shared__ __align__(1024) uint8_t sB[256 * 128];  // B rows (N <= 256); A in shared memory reuses rows 0..127
+  uint8_t* sA = sB;
+  __shared__ uint64_t bar_stage, bar_done, bar_ready;
+  __shared__ uint32_t tmem;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const Abort ab{status, &abort_flag};
+  for (int i = tid; i < 256 * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sB)[i] = 0;
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_stage, 1);
+    mbar_init(&bar_done, 1);
+    mbar_init(&bar_ready, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem, 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t base = tmem;
+  if (tid == 0) {
+    mbar_arrive(&bar_ready);  // phase 0 complete: waits on it return at once
+    const uint32_t n = (variant & 8) ? 256u : (variant & 1) ? 160u : 16u;
+    const uint32_t idesc = idesc_bf16_m128(n);
+    const long long t0 = clock64();
+    for (int s = 0; s < 64; ++s) {
+      if (variant & 4) {
+        mbar_wait(&bar_ready, 0, ab, 113);
+        tc_fence_after();
+      }
+      for (int kk = 0; kk < per; ++kk) {
+        const uint64_t bdesc = smem_desc_noswizzle(smem_u32(sB) + (kk & 3) * 256, 128, 1024);
+        if (variant & 2) {
+          const uint64_t adesc = smem_desc_noswizzle(smem_u32(sA) + (kk & 3) * 256, 128, 1024);
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(base + 192),
+              "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)(s > 0 || kk > 0))
+              : "memory");
+        } else {
+          mma_bf16_ts(base + 192, base + (kk & 3) * 8, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (per_commit > 0 && ((s * per + kk + 1) % per_commit) == 0) mma_commit(&bar_stage);
+      }
+    }
+    const long long t1 = clock64();
+    mma_commit(&bar_done);
+    mbar_wait(&bar_done, 0, ab, 114);
+    const long long t2 = clock64();
+    out[0] = t1 - t0;  // issue time of 64 stages
+    out[1] = t2 - t0;  // until the last completes
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(base, 512);
+}
+
 // Dequantise serving-layout blocks (one 128-row x 64-element stage each).
 template <int FMT>
 __global__ void probe_dequant_kernel(const uint8_t* codes, const uint8_t* scales, uint16_t* out) {
@@ -104,6 +394,38 @@ int probe_mma_ts(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t
   probe_mma_kernel<<<1, 128>>>(A, B, N, D, status);
   cudaError_t e = cudaDeviceSynchronize();
   return (int)e;
+}
+
+int probe_mma_rowb(const uint16_t* A, const uint16_t* x, float* D, uint32_t* status) {
+  probe_mma_rowb_kernel<<<1, 128>>>(A, x, D, status);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_tmem_latency(long long* out, uint32_t* status) {
+  probe_tmem_latency_kernel<<<1, 128>>>(out, status);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_tma(const uint16_t* src, int rows, int cols, int mode, int c0, const int* r4, int box_rows, int dst_off,
+              uint8_t* out, uint32_t* status) {
+  CUtensorMap tm;
+  if (!make_tmap_bf16_2d(&tm, src, (uint64_t)rows, (uint64_t)cols, mode == 0 ? (uint32_t)box_rows : 1u)) return -2;
+  probe_tma_kernel<<<1, 128>>>(tm, mode, c0, r4[0], r4[1], r4[2], r4[3], box_rows, dst_off, out, status);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_mma_sw128(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t* status) {
+  if (N < 16 || N > 256 || N % 16) return -1;
+  CUtensorMap tm;
+  if (!make_tmap_bf16_2d(&tm, B, (uint64_t)N, 64, (uint32_t)N)) return -2;
+  probe_mma_sw128_kernel<<<1, 128>>>(tm, A, N, D, status);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_mma_tput(int variant, int per, int per_commit, long long* out, uint32_t* status) {
+  if (per < 1 || per > 16) return -1;
+  probe_mma_tput_kernel<<<1, 128>>>(variant, per, per_commit, out, status);
+  return (int)cudaDeviceSynchronize();
 }
 
 int probe_dequant(const uint8_t* codes, const uint8_t* scales, int fmt, int nblocks, uint16_t* out) {

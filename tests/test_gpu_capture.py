@@ -35,6 +35,12 @@ def test_capture_and_replay(name, wl, m, path):
     ref = oracle_out(hl)
     assert_parity(bf16_to_np(eager), ref, f"{name} eager")
 
+    # torch's first capture in a process registers its RNG state on the device;
+    # do that with a throwaway graph so the check below sees only this call
+    warm = torch.cuda.CUDAGraph()
+    scratch = torch.zeros(4, device="cuda")
+    with torch.cuda.graph(warm, stream=s):
+        scratch.add_(1)
     torch.cuda.synchronize()
     before = torch.cuda.memory_allocated()
     g = torch.cuda.CUDAGraph()

@@ -32,7 +32,8 @@ def probe():
     if not os.path.exists(PROBE):
         pytest.fail("tests/csrc/libb4probe.so missing: run __graft_entry__.build()")
     lib = ctypes.CDLL(PROBE)
-    for name in ("probe_mma_ts", "probe_dequant", "probe_bf16_mul"):
+    for name in ("probe_mma_ts", "probe_mma_rowb", "probe_dequant", "probe_bf16_mul", "probe_tma", "probe_mma_sw128",
+                 "probe_mma_tput"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -59,6 +60,86 @@ def test_tcgen05_mma_a_in_tmem_matches_matmul(probe, n):
     want = a @ b.T
     got = D.cpu().numpy().astype(np.float64)
     assert np.allclose(got, want, rtol=1e-5, atol=1e-4), np.abs(got - want).max()
+
+
+def test_tcgen05_single_row_b_descriptor(probe):
+    """The decode path's B operand: one natural-order row, K stride 16 B, N stride 0."""
+    rng = np.random.default_rng(5)
+    a = F.bf16_rn(rng.standard_normal((128, 64)))
+    x = F.bf16_rn(rng.standard_normal(64))
+    A = dev(F.bf16_bits(a).view(np.int16))
+    X = dev(F.bf16_bits(x).view(np.int16))
+    D = torch.full((128, 16), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert probe.probe_mma_rowb(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(X.data_ptr()),
+                                ctypes.c_void_p(D.data_ptr()), ctypes.c_void_p(status.data_ptr())) == 0
+    assert status.cpu().tolist() == [0, 0]
+    got = D.cpu().numpy().astype(np.float64)
+    want = a @ x
+    assert np.allclose(got[:, 0], want, rtol=1e-5, atol=1e-4), np.abs(got[:, 0] - want).max()
+    assert np.array_equal(got[:, 8], got[:, 0])  # rows 8..15 repeat rows 0..7
+
+
+def _sw128_expect(rows_data, first_slot):
+    """128-byte swizzle: 16-byte chunk c of the row in atom slot q lands at chunk c ^ (q % 8)."""
+    out = {}
+    for j, row in enumerate(rows_data):
+        q = first_slot + j
+        for c in range(8):
+            out[(q, c ^ (q % 8))] = row[8 * c: 8 * c + 8]
+    return out
+
+
+def _tma_call(probe, src, mode, c0, rows4, box_rows, dst_off):
+    out = torch.zeros(256 * 128, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    r4 = (ctypes.c_int * 4)(*rows4)
+    rc = probe.probe_tma(ctypes.c_void_p(src.data_ptr()), src.shape[0], src.shape[1], mode, c0, r4, box_rows, dst_off,
+                         ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(status.data_ptr()))
+    assert rc == 0 and status.cpu().tolist() == [0, 0], rc
+    return out.cpu().numpy().view(np.uint16)  # 16-bit elements
+
+
+def test_tma_tile_box_lands_in_128b_swizzle(probe):
+    rng = np.random.default_rng(7)
+    src_np = rng.integers(0, 1 << 16, size=(300, 128), dtype=np.uint16)
+    src = dev(src_np.view(np.int16))
+    for r0, c0, box in ((100, 64, 40), (280, 0, 32)):  # second box runs past the last row
+        got = _tma_call(probe, src, 0, c0, (r0, 0, 0, 0), box, 0)
+        rows = [src_np[r0 + j, c0:c0 + 64] if r0 + j < 300 else np.zeros(64, np.uint16) for j in range(box)]
+        for (q, c), want in _sw128_expect(rows, 0).items():
+            assert np.array_equal(got[q * 64 + c * 8: q * 64 + c * 8 + 8], want), (r0, q, c)
+
+
+@pytest.mark.parametrize("dst_off", [0, 512])
+def test_tma_gather4_rows(probe, dst_off):
+    rng = np.random.default_rng(8)
+    src_np = rng.integers(0, 1 << 16, size=(300, 128), dtype=np.uint16)
+    src = dev(src_np.view(np.int16))
+    rows4 = (5, 250, 17, 99)
+    got = _tma_call(probe, src, 1, 64, rows4, 1, dst_off)
+    rows = [src_np[r, 64:128] for r in rows4]
+    addr_based = all(np.array_equal(got[q * 64 + c * 8: q * 64 + c * 8 + 8], w)
+                     for (q, c), w in _sw128_expect(rows, dst_off // 128).items())
+    box_based = all(np.array_equal(got[(dst_off // 128 + j) * 64 + (c ^ j) * 8:(dst_off // 128 + j) * 64 + (c ^ j) * 8 + 8],
+                                   rows[j][8 * c:8 * c + 8]) for j in range(4) for c in range(8))
+    assert addr_based, f"swizzle follows the shared-memory address: {addr_based}; follows the box row: {box_based}"
+
+
+@pytest.mark.parametrize("n", [16, 128, 160])
+def test_tcgen05_mma_with_sw128_b(probe, n):
+    rng = np.random.default_rng(9 + n)
+    a = F.bf16_rn(rng.standard_normal((128, 64)))
+    b = F.bf16_rn(rng.standard_normal((n, 64)))
+    A = dev(F.bf16_bits(a).view(np.int16))
+    B = dev(F.bf16_bits(b).view(np.int16))
+    D = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert probe.probe_mma_sw128(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()), n,
+                                 ctypes.c_void_p(D.data_ptr()), ctypes.c_void_p(status.data_ptr())) == 0
+    assert status.cpu().tolist() == [0, 0]
+    got = D.cpu().numpy().astype(np.float64)
+    assert np.allclose(got, a @ b.T, rtol=1e-5, atol=1e-4), np.abs(got - a @ b.T).max()
 
 
 def test_bf16_mul_keeps_subnormal_inputs(probe):

@@ -80,6 +80,7 @@ def _load():
         "b4_fused_moe": (I32, [CP, P, P, P, P, P, P, P, P, P, I32, P, P, S, P]),
         "b4_check_status": (I32, [P, P]),
         "b4_set_timing_events": (I32, [ctypes.POINTER(P), I32]),
+        "b4_set_trace": (I32, [P, S]),
         "b4_status_string": (ctypes.c_char_p, [I32]),
         "b4_last_error": (ctypes.c_char_p, []),
     }
@@ -100,6 +101,7 @@ EXPORTED = (
     "b4_fused_moe",
     "b4_check_status",
     "b4_set_timing_events",
+    "b4_set_trace",
     "b4_status_string",
     "b4_last_error",
 )
@@ -243,9 +245,21 @@ def set_timing_events(events):
         _timing_keepalive = None
         _check(_lib.b4_set_timing_events(None, 0))
         return
+    for e in events:  # torch creates the CUDA event at its first record
+        if not e.cuda_event:
+            e.record(torch.cuda.current_stream())
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _timing_keepalive = arr
     _check(_lib.b4_set_timing_events(arr, len(events)))
+
+
+def set_trace(buffer):
+    """Kernel timeline (see b4_set_trace): an int64 CUDA tensor of >= 20480 entries, or None."""
+    if buffer is None:
+        _check(_lib.b4_set_trace(None, 0))
+    else:
+        _need(buffer, torch.int64, "trace buffer")
+        _check(_lib.b4_set_trace(buffer.data_ptr(), buffer.numel() * 8))
 
 
 def check_status(workspace, stream=None):

@@ -14,11 +14,15 @@
 
 #include "b4moe.h"
 #include "kernels.cuh"
+#include "tma.cuh"
 
 namespace b4 {
 template <int MODE, int FMT>
 cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, bool grouped, int num_sms, cudaStream_t stream);
+template <int MODE, int FMT>
+cudaError_t launch_decode_gemv(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_route_pack(const RoutePackParams& p, cudaStream_t stream);
 size_t route_pack_smem_bytes(int num_local_experts);
 cudaError_t launch_prepare(const PrepareParams& p, int num_sms, cudaStream_t stream);
@@ -31,11 +35,19 @@ namespace {
 thread_local std::string g_last_error;
 thread_local void* const* g_events = nullptr;  // b4_set_timing_events
 thread_local int g_num_events = 0;
+thread_local long long* g_trace = nullptr;     // b4_set_trace
 
 // Records timing event i (if timing is on).
+// Under stream capture a plain record only orders streams inside the graph;
+// an external record becomes an event-record node that replays can time.
 cudaError_t mark(int i, cudaStream_t s) {
   if (!g_events || i >= g_num_events) return cudaSuccess;
-  return cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_events[i]), s);
+  cudaEvent_t ev = reinterpret_cast<cudaEvent_t>(g_events[i]);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, s);
 }
 
 b4_status fail(b4_status st, const char* fmt, ...) {
@@ -94,7 +106,7 @@ b4_status check_config(const b4_moe_config* cfg, int32_t act) {
 
 // ------------------------------------------------------------- workspace
 struct WsLayout {
-  size_t status, counts, offsets, sorted, chunks, chunk_count, h, acc, p, q, total;
+  size_t status, counts, offsets, sorted, chunks, chunk_count, h, acc, p, q, xp, total;
   int t_cap, r_cap, max_chunks, inter_pad, wnat, dec_splits;
   bool decode_ok;
 };
@@ -113,7 +125,11 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   // which keeps the total monotone in T_cap
   const int dec_rcap = (L.t_cap < B4_DECODE_MAX_M ? L.t_cap : B4_DECODE_MAX_M) * cfg->top_k;
   int s = 256 / dec_rcap;
-  L.dec_splits = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+  s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+  // a decode unit covers at most 128 K stages, so long K needs that many splits
+  const int kst = cdiv(cfg->hidden > L.inter_pad ? cfg->hidden : L.inter_pad, kBK);
+  const int need = (kst + 127) / 128;
+  L.dec_splits = s > need ? s : need;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -128,6 +144,7 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.chunk_count = take(sizeof(int32_t));
   L.h = take(sizeof(uint16_t) * (size_t)L.r_cap * L.inter_pad);
   L.acc = take(sizeof(float) * (size_t)L.t_cap * cfg->hidden);
+  L.xp = take(sizeof(uint16_t) * (size_t)L.r_cap * cfg->hidden);
   L.p = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * L.wnat);
   L.q = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * cfg->hidden);
   L.total = off;
@@ -167,10 +184,12 @@ b4_status device_info(DevInfo& info) {
 }
 
 int pick_splits(int64_t base_units, int k_stages, int grid, int cap) {
-  int best = 1;
+  // a decode unit holds its B slice in shared memory: at most 128 stages
+  const int min_s = (k_stages + 127) / 128;
+  int best = min_s;
   double best_eff = -1;
-  for (int s = 1; s <= cap; ++s) {
-    if (k_stages / s < 4 && s > 1) break;
+  for (int s = min_s; s <= cap; ++s) {
+    if (k_stages / s < 4 && s > min_s) break;
     const int64_t units = base_units * s;
     const int64_t waves = (units + grid - 1) / grid;
     const double eff = (double)units / (double)(waves * grid);
@@ -329,6 +348,8 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   base.max_chunks = L.max_chunks;
 
   GemmParams p1 = base, p2 = base;
+  p1.trace = g_trace;
+  p2.trace = g_trace ? g_trace + 5 * kTraceLen : nullptr;
   p1.wcodes = w13;
   p1.wscales = s13;
   p1.gs = gs13;
@@ -368,9 +389,13 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     const int grid1 = (int)(u1 < grid_cap ? u1 : grid_cap), grid2 = (int)(u2 < grid_cap ? u2 : grid_cap);
     p1.clear_status = 1;
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    if ((e = launch_mode<kFc1Decode>(fmt, p1, grid1, false, s)) != cudaSuccess) return cuda_fail(e, "fc1 decode");
+    if ((e = fmt == 0 ? launch_decode_gemv<kFc1Decode, 0>(p1, grid1, false, s)
+                      : launch_decode_gemv<kFc1Decode, 1>(p1, grid1, false, s)) != cudaSuccess)
+      return cuda_fail(e, "fc1 decode");
     if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    if ((e = launch_mode<kFc2Decode>(fmt, p2, grid2, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 decode");
+    if ((e = fmt == 0 ? launch_decode_gemv<kFc2Decode, 0>(p2, grid2, true, s)
+                      : launch_decode_gemv<kFc2Decode, 1>(p2, grid2, true, s)) != cudaSuccess)
+      return cuda_fail(e, "fc2 decode");
     if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     fp.q = qbuf;
     fp.splits = s2v;
@@ -405,12 +430,21 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     pp->chunk_count = rp.chunk_count;
     pp->chunks = rp.chunks;
   }
+  uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);
+  if (!make_tmap_bf16_2d(&p1.tmap_b, xp, (uint64_t)L.r_cap, (uint64_t)cfg->hidden, 32))
+    return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the packed-x map");
+  if (!make_tmap_bf16_2d(&p2.tmap_b, hbuf, (uint64_t)L.r_cap, (uint64_t)L.inter_pad, 32))
+    return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the h map");
   p1.h_out = hbuf;
   p1.acc_out = acc;
   p1.acc_zero_floats = (size_t)cfg->m * cfg->hidden;
   p1.pdl_wait_first = 1;
   p2.h = hbuf;
   p2.acc_out = acc;
+  GemmParams pp = p1;  // permute: x rows -> packed-route order
+  pp.xp = xp;
+  pp.valid_count = rp.offsets + cfg->num_local_experts;
+  if ((e = launch_permute_x(pp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "permute x");
   if ((e = launch_mode<kFc1Grouped>(fmt, p1, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc1 grouped");
   if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   if ((e = launch_mode<kFc2Grouped>(fmt, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");
@@ -418,6 +452,13 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   fp.acc = acc;
   if ((e = launch_finalize(fp, true, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize grouped");
   if ((e = mark(4, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+  return B4_OK;
+}
+
+b4_status b4_set_trace(void* device_buffer, size_t bytes) {
+  if (device_buffer && bytes < 10 * kTraceLen * sizeof(long long))
+    return fail(B4_ERR_INVALID_ARGUMENT, "trace buffer needs %zu bytes", 10 * kTraceLen * sizeof(long long));
+  g_trace = static_cast<long long*>(device_buffer);
   return B4_OK;
 }
 

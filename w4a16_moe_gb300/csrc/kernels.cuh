@@ -2,6 +2,8 @@
 // and the CUDA kernels of the fused W4A16 MoE layer.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -11,7 +13,7 @@ namespace b4 {
 constexpr int kTileRows = 128;   // weight rows per tile (tcgen05 M)
 constexpr int kBK = 64;          // K elements per pipeline stage
 constexpr int kCodeBytesPerStage = kTileRows * kBK / 2;  // 4096: [2 chunks][128 rows][16 B]
-constexpr int kChunkRows = 192;  // max routes of one expert per grouped work unit (tcgen05 N)
+constexpr int kChunkRows = 160;  // max routes of one expert per grouped work unit (tcgen05 N)
 
 __host__ __device__ constexpr int scale_bytes_per_row(int fmt) { return fmt == 0 ? kBK / 16 : kBK / 32; }
 __host__ __device__ constexpr int scale_bytes_per_stage(int fmt) { return kTileRows * scale_bytes_per_row(fmt); }
@@ -47,6 +49,9 @@ __host__ __device__ inline TensorGeom tensor_geom(int which, int act, int hidden
 enum GemmMode : int { kFc1Grouped = 0, kFc2Grouped = 1, kFc1Decode = 2, kFc2Decode = 3 };
 
 struct GemmParams {
+  // TMA map of the grouped B operand: packed x rows (FC1) or h rows (FC2),
+  // box 64 columns x 32 rows, 128-byte swizzle
+  CUtensorMap tmap_b;
   // prepared weights of this GEMM
   const uint8_t* wcodes;
   const uint8_t* wscales;
@@ -66,6 +71,8 @@ struct GemmParams {
   int max_chunks;
   // B operand sources
   const uint16_t* x;    // [m, H] bf16 (FC1)
+  uint16_t* xp;         // [R_cap, H] bf16: x rows in packed-route order (grouped FC1)
+  const int32_t* valid_count;  // number of valid routes (offsets[E_l] of the route pack)
   const uint16_t* h;    // [R_cap, I_pad] bf16 (FC2 grouped)
   const float* p_in;    // decode FC1 partials (FC2 decode)
   int splits_in;        // number of FC1 partial splits (FC2 decode)
@@ -78,7 +85,14 @@ struct GemmParams {
   uint32_t* status;     // device status word(s)
   int pdl_wait_first;   // all threads wait on the previous grid before starting
   int clear_status;     // block 0 resets the status word (first kernel of a call)
+  // Optional timeline of CTA 0 (clock64 cycles), or null: [kind][index] with
+  // kinds 0 weight stage issued, 1 A stage stored to tensor memory, 2 MMA
+  // stage issued, 3 B stage (grouped) or row (decode) ready, 4 epilogue of a
+  // unit done; kTraceLen entries per kind.
+  long long* trace;
 };
+
+constexpr int kTraceLen = 2048;
 
 struct RoutePackParams {
   const int32_t* topk_ids;

@@ -1,32 +1,35 @@
 // Grouped W4A16 GEMMs of the fused MoE layer on tcgen05 (sm_103a).
 //
-// One persistent, warp-specialised kernel serves the four GEMMs of the layer
+// One persistent, warp-specialised kernel serves the two route-packed GEMMs
 // (flashinfer PR #4255, Description: "Cooperative persistent launches for the
-// fused FC1/FC2 kernel", "A tensor-core decode path for small batches ...
-// folding the top-k sum into the FC2 store epilogue"):
+// fused FC1/FC2 kernel", "folding the top-k sum into the FC2 store
+// epilogue"):
 //
-//   FC1 grouped  routes packed by expert; B = gathered x rows; epilogue applies
-//                the SiLU-SwiGLU or ReLU^2 activation and stores bf16 h.
-//   FC2 grouped  B = h rows; epilogue multiplies by gs2 and the router weight
-//                and adds into an fp32 [tokens, H] accumulator (the top-k sum).
-//   FC1 decode   one route per work unit, K split across units; epilogue
-//                stores fp32 partial sums.
-//   FC2 decode   B = activation of the summed FC1 partials (computed while
-//                loading); epilogue stores gs2 * w * y partials.
+//   FC1  B = x rows of the routes of one expert chunk, copied into
+//        packed-route order by permute_x_kernel; the epilogue applies
+//        SiLU-SwiGLU or ReLU^2 and stores bf16 h in the same order.
+//   FC2  B = h rows of the chunk; the epilogue multiplies by gs2 and the
+//        router weight and adds into an fp32 [tokens, H] accumulator (the
+//        top-k sum), which finalize_grouped_kernel rounds to bf16.
 //
-// The tensor-core operation is swapped: the 128 weight rows of a tile are the
-// M operand, the routes are N.  Weights are dequantised from E2M1 codes and
-// E4M3 / E8M0 block scales to bf16 by four dequant warps (one thread per
-// weight row) and written straight into tensor memory with tcgen05.st, where
-// tcgen05.mma reads them as its A operand; B (activations) is staged in
-// shared memory.  Roles, one CTA of 12 warps:
+// A work unit is (expert chunk of <= 160 routes, 128-row weight tile).  The
+// tensor-core operation is swapped: the 128 weight rows are the M operand, the
+// chunk's routes are N (rounded up to 16).  Weights are dequantised from E2M1
+// codes and E4M3 / E8M0 block scales to bf16 by eight dequant warps (one
+// thread per weight row) and written straight into tensor memory with
+// tcgen05.st, where tcgen05.mma reads them as its A operand; B sits in shared
+// memory in the 128-byte-swizzled K-major layout, loaded by TMA in 32-row 2-D
+// boxes (both B operands are contiguous in packed-route order).  Roles, one
+// CTA of 16 warps:
 //   warp 0       bulk-copy (TMA engine) producer of packed codes and scales
 //   warp 1       TMEM allocator and the single MMA-issuing thread
-//   warps 2-3    B loaders (cp.async gathers, or computed rows in FC2 decode)
-//   warps 4-7    dequantisers: shared memory codes -> bf16 -> tensor memory
-//   warps 8-11   epilogue: tensor memory accumulators -> outputs
-// Four mbarrier rings connect them (weights, A slots in TMEM, B stages,
-// double-buffered accumulators); every wait is bounded (ptx.cuh).
+//   warp 2       B producer (TMA tile loads)
+//   warps 4-11   dequantisers (two groups of four taking alternate stages)
+//   warps 12-15  epilogue: tensor-memory accumulators -> outputs
+// Rings: weights (10 stages); A slots in TMEM and B stages (6, one index, one
+// release commit per stage); two accumulators, so the epilogue of one unit
+// overlaps the next mainloop.
+// Every wait is bounded (ptx.cuh).
 //
 // Dequantised weights carry a factor 2^-63 so that every product of an E2M1
 // code and a block scale is a normal bf16; the epilogue multiplies by 2^63.
@@ -36,91 +39,60 @@
 #include "dequant.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tma.cuh"
 
 namespace b4 {
 
-constexpr int kNumA = 4;          // A slots (K stages) held in tensor memory
-constexpr int kThreads = 384;
-constexpr int kAColsPerSlot = kBK / 2;  // 32 columns of packed bf16 pairs
+constexpr int kNumA = 6;                 // A slots (K stages) held in tensor memory
+constexpr int kThreads = 512;
+constexpr int kAColsPerSlot = kBK / 2;   // 32 columns of packed bf16 pairs
+constexpr int kNW = 10;                  // weight stages in flight
+constexpr int kNB = 6;                   // B stages in flight
+constexpr int kBN = kChunkRows;          // max tcgen05 N
+constexpr int kBStage = kBN * kBK * 2;   // 160 rows x 128 bytes, swizzled
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol0 = kNumA * kAColsPerSlot;  // 192: two accumulators of kBN columns follow
 constexpr float kTwo63 = 9.223372036854775808e18f;
+static_assert(kAccCol0 + 2 * kBN <= kTmemCols, "tensor memory budget");
+static_assert(kBStage % 1024 == 0, "swizzle atoms of B stages must stay 1024-byte aligned");
+static_assert(kNB == kNumA, "A slots and B stages share one ring index and one release barrier");
 
-template <int MODE>
-struct ModeTraits {
-  static constexpr bool kGrouped = MODE == kFc1Grouped || MODE == kFc2Grouped;
-  static constexpr bool kFc1 = MODE == kFc1Grouped || MODE == kFc1Decode;
-  static constexpr int kNW = kGrouped ? 8 : 16;       // weight stages
-  static constexpr int kNB = 4;                        // B stages
-  static constexpr int kBN = kGrouped ? kChunkRows : 16;  // max tcgen05 N
-  static constexpr uint32_t kTmemCols = kGrouped ? 512 : 256;
-  static constexpr uint32_t kAccCol0 = kNumA * kAColsPerSlot;  // 128
-  static constexpr int kLag = kGrouped ? 2 : 1;       // cp.async stages in flight per loader
-};
-
-template <int MODE, int FMT>
+template <int FMT>
 struct SmemLayout {
-  using T = ModeTraits<MODE>;
   static constexpr int kScaleStage = scale_bytes_per_stage(FMT);
-  static constexpr int kBStage = T::kBN * kBK * 2;
-  static constexpr size_t codes = 0;
-  static constexpr size_t scales = codes + (size_t)T::kNW * kCodeBytesPerStage;
-  static constexpr size_t b = round_up((int)(scales + (size_t)T::kNW * kScaleStage), 128);
-  static constexpr size_t bars = b + (size_t)T::kNB * kBStage;
-  static constexpr int kNumBars = 2 * T::kNW + 2 * kNumA + 2 * T::kNB + 4 + 1;
+  static constexpr size_t b = 0;  // offset from the 1024-aligned base
+  static constexpr size_t codes = b + (size_t)kNB * kBStage;
+  static constexpr size_t scales = codes + (size_t)kNW * kCodeBytesPerStage;
+  static constexpr size_t bars = round_up((int)(scales + (size_t)kNW * kScaleStage), 8);
+  static constexpr int kNumBars = 2 * kNW + 3 * kNumA + 4 + 1;
   static constexpr size_t misc = bars + 8 * kNumBars;
   static constexpr size_t rows = misc + 16;
-  static constexpr size_t total = rows + 4 * T::kBN + 64;
+  static constexpr size_t total = rows + 8 * kBN + 1024;  // + alignment slack
 };
 
 struct Unit {
-  int expert, tile, kbeg, kend, slot0, rows, route, split;
+  int expert, tile, slot0, rows;
 };
 
-__device__ __forceinline__ int local_expert_of(const GemmParams& p, int route) {
-  const int id = __ldg(p.topk_ids + route);
-  if (id < 0 || id >= p.num_global_experts) return -1;
-  const int l = p.expert_map ? __ldg(p.expert_map + id) : id;
-  return (l >= 0 && l < p.num_local_experts) ? l : -1;
-}
-
-template <int MODE>
 __device__ __forceinline__ int num_units(const GemmParams& p) {
-  if constexpr (ModeTraits<MODE>::kGrouped) {
-    int c = *(volatile const int32_t*)p.chunk_count;
-    c = c < 0 ? 0 : (c > p.max_chunks ? p.max_chunks : c);
-    return c * p.n_tiles;
-  } else {
-    return p.m * p.top_k * p.n_tiles * p.splits;
-  }
+  int c = *(volatile const int32_t*)p.chunk_count;
+  c = c < 0 ? 0 : (c > p.max_chunks ? p.max_chunks : c);
+  return c * p.n_tiles;
 }
 
-// Returns false for a unit with nothing to do (a dropped route in decode).
-template <int MODE>
 __device__ __forceinline__ bool get_unit(const GemmParams& p, int u, Unit& U) {
-  if constexpr (ModeTraits<MODE>::kGrouped) {
-    const int c = u / p.n_tiles;
-    U.tile = u - c * p.n_tiles;
-    const int4 ch = p.chunks[c];
-    U.expert = ch.x;
-    U.slot0 = ch.y;
-    U.rows = ch.z;
-    U.kbeg = 0;
-    U.kend = p.k_stages;
-    U.route = -1;
-    U.split = 0;
-    return U.rows > 0;
-  } else {
-    const int per_route = p.n_tiles * p.splits;
-    U.route = u / per_route;
-    const int rem = u - U.route * per_route;
-    U.tile = rem / p.splits;
-    U.split = rem - U.tile * p.splits;
-    U.kbeg = (int)((long long)U.split * p.k_stages / p.splits);
-    U.kend = (int)((long long)(U.split + 1) * p.k_stages / p.splits);
-    U.slot0 = U.route;
-    U.rows = 1;
-    U.expert = local_expert_of(p, U.route);
-    return U.expert >= 0 && U.kend > U.kbeg;
-  }
+  const int c = u / p.n_tiles;
+  U.tile = u - c * p.n_tiles;
+  const int4 ch = p.chunks[c];
+  U.expert = ch.x;
+  U.slot0 = ch.y;
+  U.rows = ch.z;
+  return U.rows > 0;
+}
+
+// Timeline hook: CTA 0 records clock64() of event `kind` number `idx`.
+__device__ __forceinline__ void trace_mark(const GemmParams& p, int kind, uint32_t idx) {
+  if (p.trace && blockIdx.x == 0 && idx < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + idx] = clock64();
 }
 
 // Warp-uniform bounded wait.
@@ -129,7 +101,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
@@ -138,24 +109,24 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 // ------------------------------------------------------------------ kernel
 template <int MODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using T = ModeTraits<MODE>;
-  using L = SmemLayout<MODE, FMT>;
-  constexpr int NW = T::kNW, NB = T::kNB, BN = T::kBN;
+  using L = SmemLayout<FMT>;
+  constexpr int NW = kNW, NB = kNB;
   constexpr int SB = scale_bytes_per_row(FMT);
   constexpr int kScaleStage = L::kScaleStage;
 
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled B stages need 1024-byte alignment of the shared address
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* s_b = smem + L::b;
   uint8_t* s_codes = smem + L::codes;
   uint8_t* s_scales = smem + L::scales;
-  uint8_t* s_b = smem + L::b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
   uint64_t* full_w = bars;
   uint64_t* empty_w = full_w + NW;
   uint64_t* full_a = empty_w + NW;
-  uint64_t* empty_a = full_a + kNumA;
-  uint64_t* full_b = empty_a + kNumA;
-  uint64_t* empty_b = full_b + NB;
-  uint64_t* full_acc = empty_b + NB;
+  uint64_t* stage_free = full_a + kNumA;  // A slot and B stage of a ring index, freed by one commit
+  uint64_t* full_b = stage_free + kNumA;
+  uint64_t* full_acc = full_b + NB;
   uint64_t* empty_acc = full_acc + 2;
   uint64_t* drain = empty_acc + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::misc);
@@ -167,10 +138,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   const Abort ab{p.status, s_abort};
 
   if (threadIdx.x == 0) {
-    if (p.clear_status && blockIdx.x == 0 && p.status) {
-      p.status[0] = 0;
-      p.status[1] = 0;
-    }
     *s_abort = 0;
     for (int i = 0; i < NW; ++i) {
       mbar_init(&full_w[i], 1);
@@ -178,11 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(&full_a[i], 4);
-      mbar_init(&empty_a[i], 1);
-    }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(&full_b[i], 64);
-      mbar_init(&empty_b[i], 1);
+      mbar_init(&stage_free[i], 1);
+      mbar_init(&full_b[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&full_acc[i], 1);
@@ -192,14 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(s_tmem, T::kTmemCols);
+    tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
-  }
-  // B stages start as zeros: rows beyond a unit's routes then stay finite.
-  if (warp == 2 || warp == 3) {
-    uint4* z = reinterpret_cast<uint4*>(s_b);
-    for (int i = threadIdx.x - 64; i < NB * L::kBStage / 16; i += 64) z[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -209,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   if (p.pdl_wait_first) pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  const int n_units = num_units<MODE>(p);
+  const int n_units = num_units(p);
   const size_t wtile_codes = (size_t)p.k_stages * kCodeBytesPerStage;
   const size_t wtile_scales = (size_t)p.k_stages * kScaleStage;
 
@@ -219,17 +177,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (lane == 0) {
       for (int u = blockIdx.x; u < n_units && !ab.raised(); u += gridDim.x) {
         Unit U;
-        if (!get_unit<MODE>(p, u, U)) continue;
+        if (!get_unit(p, u, U)) continue;
         const size_t tile_id = (size_t)U.expert * p.n_tiles + U.tile;
         const uint8_t* gc = p.wcodes + tile_id * wtile_codes;
         const uint8_t* gsc = p.wscales + tile_id * wtile_scales;
-        for (int s = U.kbeg; s < U.kend; ++s, ++ws) {
+        for (int s = 0; s < p.k_stages; ++s, ++ws) {
           const uint32_t slot = ws % NW;
           if (!mbar_wait(&empty_w[slot], ((ws / NW) & 1) ^ 1, ab, 1)) break;
           mbar_arrive_expect_tx(&full_w[slot], kCodeBytesPerStage + kScaleStage);
           bulk_g2s(s_codes + slot * kCodeBytesPerStage, gc + (size_t)s * kCodeBytesPerStage, kCodeBytesPerStage,
                    &full_w[slot]);
           bulk_g2s(s_scales + slot * kScaleStage, gsc + (size_t)s * kScaleStage, kScaleStage, &full_w[slot]);
+          trace_mark(p, 0, ws);
         }
       }
       if (ab.raised()) {
@@ -250,15 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const uint32_t b_base = smem_u32(s_b);
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         Unit U;
-        if (!get_unit<MODE>(p, u, U)) continue;
+        if (!get_unit(p, u, U)) continue;
         const uint32_t abuf = acc_i & 1;
         if (!mbar_wait(&empty_acc[abuf], ((acc_i >> 1) & 1) ^ 1, ab, 2)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + T::kAccCol0 + abuf * BN;
-        const uint32_t n16 = T::kGrouped ? (uint32_t)round_up(U.rows, 16) : 16u;
-        const uint32_t idesc = idesc_bf16_m128(n16);
+        const uint32_t d_tmem = tmem_base + kAccCol0 + abuf * kBN;
+        const uint32_t idesc = idesc_bf16_m128((uint32_t)round_up(U.rows, 16));
         bool ok = true;
-        for (int s = U.kbeg; s < U.kend; ++s, ++as, ++bs) {
+        for (int s = 0; s < p.k_stages; ++s, ++as, ++bs) {
           const uint32_t aslot = as % kNumA, bslot = bs % NB;
           if (!mbar_wait(&full_a[aslot], (as / kNumA) & 1, ab, 3) ||
               !mbar_wait(&full_b[bslot], (bs / NB) & 1, ab, 4)) {
@@ -269,11 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t a_tmem = tmem_base + aslot * kAColsPerSlot + kk * 8;
-            const uint64_t bdesc = smem_desc_noswizzle(b_base + bslot * L::kBStage + kk * 256, 128, 1024);
-            mma_bf16_ts(d_tmem, a_tmem, bdesc, idesc, (s > U.kbeg || kk > 0) ? 1u : 0u);
+            const uint64_t bdesc = smem_desc_sw128(b_base + bslot * kBStage + kk * 32);
+            mma_bf16_ts(d_tmem, a_tmem, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&empty_a[aslot]);
-          mma_commit(&empty_b[bslot]);
+          mma_commit(&stage_free[aslot]);
+          trace_mark(p, 2, as);
         }
         if (!ok) break;
         mma_commit(&full_acc[abuf]);
@@ -286,106 +244,55 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       }
     }
     __syncwarp();
-  } else if (warp == 2 || warp == 3) {
-    // -------------------------------------------------------- B loaders
-    const int lt = threadIdx.x - 64;
-    const uint32_t b_base = smem_u32(s_b);
-    uint32_t bs = 0, arrived = 0;
-    if (MODE == kFc2Grouped || MODE == kFc2Decode) pdl_wait();  // h / FC1 partials come from FC1
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  } else if (warp == 2) {
+    // --------------------------------------------------------- B producer
+    if (MODE == kFc2Grouped) pdl_wait();  // h comes from FC1 (FC1 waited for its inputs at entry)
+    uint32_t bs = 0;
+    for (int u = blockIdx.x; u < n_units && !ab.raised(); u += gridDim.x) {
       Unit U;
-      if (!get_unit<MODE>(p, u, U)) continue;
-      if constexpr (T::kGrouped) {
-        named_bar_sync(1, 64);  // previous unit's row table no longer read
-        for (int i = lt; i < U.rows; i += 64) {
-          const int slot = U.slot0 + i;
-          s_rows[i] = MODE == kFc1Grouped ? __ldg(p.sorted_routes + slot) / p.top_k : slot;
-        }
-        named_bar_sync(1, 64);
-      }
+      if (!get_unit(p, u, U)) continue;
+      const int nload = cdiv(U.rows, 32);
+      const uint32_t bytes = (uint32_t)nload * 4096u;
       bool ok = true;
-      for (int s = U.kbeg; s < U.kend; ++s, ++bs) {
+      for (int s = 0; s < p.k_stages; ++s, ++bs) {
         const uint32_t slot = bs % NB;
-        if (!warp_wait(&empty_b[slot], ((bs / NB) & 1) ^ 1, ab, 5)) {
+        if (!warp_wait(&stage_free[slot], ((bs / NB) & 1) ^ 1, ab, 5)) {
           ok = false;
           break;
         }
-        const uint32_t stage = b_base + slot * L::kBStage;
-        const int k0 = s * kBK;
-        if constexpr (MODE == kFc2Decode) {
-          // h[i] = act(gs13 * 2^63 * sum of FC1 partials) for i = k0 + lt
-          const int i = k0 + lt;
-          const int R = p.m * p.top_k;
-          const int wnat = fc1_natural_width(p.act, p.inter_pad);
-          const float* pr = p.p_in + (size_t)U.route * wnat;
-          float g = 0.f, up = 0.f;
-          for (int sp = 0; sp < p.splits_in; ++sp) {
-            const float* q = pr + (size_t)sp * R * wnat;
-            g += q[i];
-            if (p.act == 0) up += q[p.inter_pad + i];
-          }
-          // gs13 travels in p_in's companion: p.gs here is the FC2 scale, so
-          // the FC1 scale was folded into the partials by the FC1 epilogue.
-          const float hv = p.act == 0 ? silu_f(g) * up : (g > 0.f ? g * g : 0.f);
-          const uint16_t hb = float_to_bf16_bits(hv);
-          const uint32_t off = (uint32_t)(lt >> 3) * 128 + (lt & 7) * 2;
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage + off), "h"(hb) : "memory");
-          fence_proxy_async_smem();
-          mbar_arrive(&full_b[slot]);
-          ++arrived;
-        } else {
-          const int kc = lt >> 3;    // 16-byte chunk along K: 0..7
-          const int nlo = lt & 7;    // row within an 8-row group
-          const int ke = k0 + kc * 8;
-          const int kvalid = MODE == kFc1Grouped || MODE == kFc1Decode ? p.hidden : p.inter_pad;
-          const uint32_t src_bytes = ke < kvalid ? 16u : 0u;
-          const int nrows = T::kGrouped ? U.rows : 1;
-          const int ngroups = cdiv(nrows, 8);
-          for (int gi = 0; gi < ngroups; ++gi) {
-            const int n = gi * 8 + nlo;
-            if (n >= nrows) break;
-            const uint16_t* row;
-            if constexpr (MODE == kFc1Grouped) row = p.x + (size_t)s_rows[n] * p.hidden;
-            else if constexpr (MODE == kFc2Grouped) row = p.h + (size_t)s_rows[n] * p.inter_pad;
-            else row = p.x + (size_t)(U.route / p.top_k) * p.hidden;
-            const uint16_t* src = src_bytes ? row + ke : p.x;
-            cp_async16(stage + gi * 1024 + kc * 128 + nlo * 16, src, src_bytes);
-          }
-          if constexpr (T::kGrouped) {
-            // zero-fill rows [rows, roundup16(rows)) so the padded columns stay finite
-            const int n16 = round_up(U.rows, 16);
-            for (int n = U.rows + nlo - (U.rows & 7); n < n16; n += 8) {
-              if (n >= U.rows) cp_async16(stage + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16, p.x, 0);
-            }
-          }
-          cp_async_commit();
-          // delayed arrival: stage bs - kLag has landed once <= kLag groups remain
-          if (bs + 1 - arrived > (uint32_t)T::kLag) {
-            cp_async_wait<T::kLag>();
-            fence_proxy_async_smem();
-            mbar_arrive(&full_b[arrived % NB]);
-            ++arrived;
-          }
-        }
+        uint8_t* stage = s_b + slot * kBStage;
+        if (lane == 0) mbar_arrive_expect_tx(&full_b[slot], bytes);
+        __syncwarp();
+        for (int i = lane; i < nload; i += 32)
+          tma_load_2d(stage + i * 4096, &p.tmap_b, s * kBK, U.slot0 + 32 * i, &full_b[slot]);
+        if (lane == 0) trace_mark(p, 3, bs);
       }
       if (!ok) break;
     }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    while (arrived < bs && !ab.raised()) {
-      mbar_arrive(&full_b[arrived % NB]);
-      ++arrived;
+    if (ab.raised() && lane == 0) {
+      // let issued loads land before the CTA exits
+      const uint32_t n = bs < (uint32_t)NB ? bs : (uint32_t)NB;
+      for (uint32_t i = bs - n; i < bs; ++i) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(&full_b[i % NB], (i / NB) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
     }
-  } else if (warp >= 4 && warp < 8) {
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------ dequantisers
-    const int row = threadIdx.x - 128;  // == 32 * (warp % 4) + lane
+    // two groups of four warps take alternate stages, so one group's tensor
+    // memory store drains while the other group computes
+    const int half = (warp - 4) >> 2;
+    const int row = 32 * (warp & 3) + lane;  // TMEM lane == weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    uint32_t ws = 0, as = 0;
+    uint32_t ws = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
-      if (!get_unit<MODE>(p, u, U)) continue;
+      if (!get_unit(p, u, U)) continue;
       bool ok = true;
-      for (int s = U.kbeg; s < U.kend; ++s, ++ws, ++as) {
+      for (int s = 0; s < p.k_stages; ++s, ++ws) {
+        if ((ws & 1) != (uint32_t)half) continue;
         const uint32_t wslot = ws % NW;
         if (!warp_wait(&full_w[wslot], (ws / NW) & 1, ab, 6)) {
           ok = false;
@@ -401,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&empty_w[wslot]);
         uint32_t r[32];
         dequant_stage<FMT>(c0, c1, sc, r);
-        const uint32_t aslot = as % kNumA;
-        if (!warp_wait(&empty_a[aslot], ((as / kNumA) & 1) ^ 1, ab, 7)) {
+        const uint32_t aslot = ws % kNumA;
+        if (!warp_wait(&stage_free[aslot], ((ws / kNumA) & 1) ^ 1, ab, 7)) {
           ok = false;
           break;
         }
@@ -411,33 +318,48 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[aslot]);
+        if (lane == 0) {
+          mbar_arrive(&full_a[aslot]);
+          trace_mark(p, 1, ws);
+        }
       }
       if (!ok) break;
     }
-  } else {
+  } else if (warp >= 12) {
     // ---------------------------------------------------------- epilogue
     const int q4 = warp & 3;
     const int er = 32 * q4 + lane;  // TMEM lane == weight row in the tile
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int et = threadIdx.x - 384;  // 0..127
+    int32_t* s_tok = s_rows;                                   // FC2: token of each column
+    float* s_wt = reinterpret_cast<float*>(s_rows + kBN);     // FC2: router weight of each column
     if constexpr (MODE == kFc1Grouped) {
       // clear the FC2 accumulator (FC2 waits for this grid before adding)
       float4* z = reinterpret_cast<float4*>(p.acc_out);
       const size_t n4 = p.acc_zero_floats / 4;
-      for (size_t i = (size_t)blockIdx.x * 128 + (threadIdx.x - 256); i < n4; i += (size_t)gridDim.x * 128)
+      for (size_t i = (size_t)blockIdx.x * 128 + et; i < n4; i += (size_t)gridDim.x * 128)
         z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if constexpr (MODE == kFc2Grouped) pdl_wait();  // acc_out cleared by FC1
     uint32_t acc_i = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
-      if (!get_unit<MODE>(p, u, U)) continue;
+      if (!get_unit(p, u, U)) continue;
       const uint32_t abuf = acc_i & 1;
+      if constexpr (MODE == kFc2Grouped) {
+        // the unit's routes: token and router weight, resolved before the wait
+        for (int i = et; i < U.rows; i += 128) {
+          const int route = __ldg(p.sorted_routes + U.slot0 + i);
+          s_tok[i] = route / p.top_k;
+          s_wt[i] = __ldg(p.topk_weights + route);
+        }
+        named_bar_sync(2, 128);
+      }
       if (!warp_wait(&full_acc[abuf], (acc_i >> 1) & 1, ab, 8)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + lane_base + T::kAccCol0 + abuf * BN;
+      const uint32_t taddr = tmem_base + lane_base + kAccCol0 + abuf * kBN;
       const float gsv = (p.gs ? __ldg(p.gs + U.expert) : 1.0f) * kTwo63;
-      const int ncols = T::kGrouped ? round_up(U.rows, 16) : 16;
+      const int ncols = round_up(U.rows, 16);
       for (int c0 = 0; c0 < ncols; c0 += 16) {
         uint32_t v[16];
         tmem_ld16(taddr + c0, v);
@@ -472,44 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 p.h_out[(size_t)(U.slot0 + col) * p.inter_pad + i] = float_to_bf16_bits(a > 0.f ? a * a : 0.f);
             }
           }
-        } else if constexpr (MODE == kFc2Grouped) {
+        } else {
           const int n = U.tile * kTileRows + er;
+          if (n < p.hidden) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < U.rows) {
-              const int route = __ldg(p.sorted_routes + U.slot0 + col);
-              const float wt = __ldg(p.topk_weights + route);
-              if (n < p.hidden)
-                red_add_f32(p.acc_out + (size_t)(route / p.top_k) * p.hidden + n,
-                            __uint_as_float(v[j]) * gsv * wt);
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < U.rows)
+                red_add_f32(p.acc_out + (size_t)s_tok[col] * p.hidden + n, __uint_as_float(v[j]) * gsv * s_wt[col]);
             }
           }
-        } else if constexpr (MODE == kFc1Decode) {
-          // natural index of this prepared row; partials carry gs13 * 2^63
-          const int R = p.m * p.top_k;
-          const int wnat = fc1_natural_width(p.act, p.inter_pad);
-          int nat;
-          if (p.act == 0) {
-            const int i = U.tile * 64 + q4 * 16 + (lane & 15);
-            nat = lane >= 16 ? p.inter_pad + i : i;
-          } else {
-            nat = U.tile * kTileRows + er;
-            if (nat >= p.inter_pad) nat = -1;
-          }
-          if (nat >= 0)
-            p.part_out[((size_t)U.split * R + U.route) * wnat + nat] = __uint_as_float(v[0]) * gsv;
-        } else {
-          const int R = p.m * p.top_k;
-          const int n = U.tile * kTileRows + er;
-          const float wt = __ldg(p.topk_weights + U.route);
-          if (n < p.hidden)
-            p.part_out[((size_t)U.split * R + U.route) * p.hidden + n] = __uint_as_float(v[0]) * gsv * wt;
         }
       }
       tc_fence_before();
+      if constexpr (MODE == kFc2Grouped) named_bar_sync(2, 128);  // route table free for the next unit
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_acc[abuf]);
+      if (lane == 0) {
+        mbar_arrive(&empty_acc[abuf]);
+        if (warp == 12) trace_mark(p, 4, acc_i);
+      }
       ++acc_i;
     }
   }
@@ -517,56 +420,45 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, T::kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// ------------------------------------------------------------- finalize
-// Grouped: out = bf16(acc).  Decode: out[t, n] = bf16(sum_j sum_split q).
-__global__ void finalize_grouped_kernel(const __grid_constant__ FinalizeParams p) {
-  pdl_wait();
-  const size_t total = (size_t)p.m * p.hidden;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i * 4 < total;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(p.acc)[i];
-    ushort4 o;
-    o.x = float_to_bf16_bits(a.x);
-    o.y = float_to_bf16_bits(a.y);
-    o.z = float_to_bf16_bits(a.z);
-    o.w = float_to_bf16_bits(a.w);
-    reinterpret_cast<ushort4*>(p.out)[i] = o;
+// --------------------------------------------------------- permute x rows
+// xp[slot] = x[token of the route at packed slot], for the valid slots: the
+// FC1 B operand becomes contiguous per expert chunk.  One warp per row, 16-byte
+// copies; slots past the valid count are left untouched (never loaded).
+__global__ void permute_x_kernel(const __grid_constant__ GemmParams p) {
+  pdl_wait();  // sorted routes come from the route-pack kernel
+  pdl_launch_dependents();
+  const int valid = *p.valid_count;
+  const int chunks = p.hidden / 8;  // 16-byte pieces of a row
+  const int wpb = blockDim.x / 32;
+  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < valid; r += gridDim.x * wpb) {
+    const int tok = __ldg(p.sorted_routes + r) / p.top_k;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.hidden);
+    uint4* dst = reinterpret_cast<uint4*>(p.xp + (size_t)r * p.hidden);
+    for (int c = threadIdx.x & 31; c < chunks; c += 32) dst[c] = __ldg(src + c);
   }
 }
 
-__global__ void finalize_decode_kernel(const __grid_constant__ FinalizeParams p) {
-  pdl_wait();
-  const int R = p.m * p.top_k;
-  const size_t total = (size_t)p.m * p.hidden;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / p.hidden);
-    const int n = (int)(i - (size_t)t * p.hidden);
-    float acc = 0.f;
-    for (int j = 0; j < p.top_k; ++j) {
-      const int route = t * p.top_k + j;
-      const int id = p.topk_ids[route];
-      if (id < 0 || id >= p.num_global_experts) continue;
-      const int l = p.expert_map ? p.expert_map[id] : id;
-      if (l < 0 || l >= p.num_local_experts) continue;
-      for (int sp = 0; sp < p.splits; ++sp) acc += p.q[((size_t)sp * R + route) * p.hidden + n];
-    }
-    p.out[i] = float_to_bf16_bits(acc);
-  }
+cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4 * num_sms);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, permute_x_kernel, p);
 }
 
 // ----------------------------------------------------- host-side launchers
 template <int MODE, int FMT>
-size_t gemm_smem_bytes() {
-  return SmemLayout<MODE, FMT>::total;
-}
-
-template <int MODE, int FMT>
 cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream) {
   auto kern = moe_gemm_kernel<MODE, FMT>;
-  const size_t smem = SmemLayout<MODE, FMT>::total;
+  const size_t smem = SmemLayout<FMT>::total;
   static bool configured = false;  // attribute set once per process (idempotent)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -586,33 +478,9 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-cudaError_t launch_finalize(const FinalizeParams& p, bool grouped, int num_sms, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  const size_t total = grouped ? (size_t)p.m * p.hidden / 4 : (size_t)p.m * p.hidden;
-  int blocks = (int)((total + 255) / 256);
-  if (blocks > 4 * num_sms) blocks = 4 * num_sms;
-  if (blocks < 1) blocks = 1;
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return grouped ? cudaLaunchKernelEx(&cfg, finalize_grouped_kernel, p)
-                 : cudaLaunchKernelEx(&cfg, finalize_decode_kernel, p);
-}
-
 template cudaError_t launch_gemm<kFc1Grouped, 0>(const GemmParams&, int, bool, cudaStream_t);
 template cudaError_t launch_gemm<kFc2Grouped, 0>(const GemmParams&, int, bool, cudaStream_t);
-template cudaError_t launch_gemm<kFc1Decode, 0>(const GemmParams&, int, bool, cudaStream_t);
-template cudaError_t launch_gemm<kFc2Decode, 0>(const GemmParams&, int, bool, cudaStream_t);
 template cudaError_t launch_gemm<kFc1Grouped, 1>(const GemmParams&, int, bool, cudaStream_t);
 template cudaError_t launch_gemm<kFc2Grouped, 1>(const GemmParams&, int, bool, cudaStream_t);
-template cudaError_t launch_gemm<kFc1Decode, 1>(const GemmParams&, int, bool, cudaStream_t);
-template cudaError_t launch_gemm<kFc2Decode, 1>(const GemmParams&, int, bool, cudaStream_t);
-template size_t gemm_smem_bytes<kFc1Grouped, 0>();
-template size_t gemm_smem_bytes<kFc1Decode, 0>();
 
 }  // namespace b4

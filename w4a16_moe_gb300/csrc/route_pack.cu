@@ -26,6 +26,7 @@ namespace b4 {
 
 constexpr int kPackThreads = 1024;
 constexpr int kPackWarps = kPackThreads / 32;
+constexpr int kKeys = 16;  // 32-route batches whose keys a warp loads together
 
 __device__ __forceinline__ int pack_local_expert(const RoutePackParams& p, int r) {
   const int id = p.topk_ids[r];
@@ -83,14 +84,24 @@ __global__ void __launch_bounds__(kPackThreads, 1) route_pack_kernel(const __gri
   for (int i = threadIdx.x; i < kPackWarps * E; i += kPackThreads) s_hist[i] = 0;
   __syncthreads();
 
-  // pass 1: per-warp histograms
+  // pass 1: per-warp histograms.  Keys of kKeys batches are loaded before
+  // any is used, so the id and expert_map loads of a warp overlap.
   int* my_hist = s_hist + warp * E;
-  for (int b = beg; b < end; b += 32) {
-    const int r = b + lane;
-    const int key = r < end ? pack_local_expert(p, r) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
-    __syncwarp();
+  for (int b0 = beg; b0 < end; b0 += 32 * kKeys) {
+    int keys[kKeys];
+#pragma unroll
+    for (int i = 0; i < kKeys; ++i) {
+      const int r = b0 + 32 * i + lane;
+      keys[i] = r < end ? pack_local_expert(p, r) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kKeys; ++i) {
+      if (b0 + 32 * i >= end) break;
+      const int key = keys[i];
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -131,17 +142,27 @@ __global__ void __launch_bounds__(kPackThreads, 1) route_pack_kernel(const __gri
   __syncthreads();
 
   // pass 3: scatter
-  for (int b = beg; b < end; b += 32) {
-    const int r = b + lane;
-    const int key = r < end ? pack_local_expert(p, r) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0) {
-      const int pos = s_off[key] + my_hist[key] + __popc(peers & lt_mask);
-      p.sorted_routes[pos] = r;
+  for (int b0 = beg; b0 < end; b0 += 32 * kKeys) {
+    int keys[kKeys];
+#pragma unroll
+    for (int i = 0; i < kKeys; ++i) {
+      const int r = b0 + 32 * i + lane;
+      keys[i] = r < end ? pack_local_expert(p, r) : -1;
     }
-    __syncwarp();
-    if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kKeys; ++i) {
+      if (b0 + 32 * i >= end) break;
+      const int r = b0 + 32 * i + lane;
+      const int key = keys[i];
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0) {
+        const int pos = s_off[key] + my_hist[key] + __popc(peers & lt_mask);
+        p.sorted_routes[pos] = r;
+      }
+      __syncwarp();
+      if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
+      __syncwarp();
+    }
   }
   // tail of the capacity: -1
   const int valid = s_valid;
