@@ -195,6 +195,54 @@ b4_status b4_set_trace(void* device_buffer, size_t bytes);
  * device wait ran out.  Resets the word to B4_OK.  Not capture-safe. */
 b4_status b4_check_status(void* workspace, b4_stream_t stream);
 
+/* Allocation-free variant of b4_fused_moe.  The paper has no counterpart:
+ * the layer it describes always takes its scratch from the caller.
+ *
+ * Who needs it: code that runs as a plugin hook of an inference runtime or as
+ * a custom-op slot of a framework receives only its input and output buffers.
+ * The host's allocator owns all device memory there; a cudaMalloc from inside
+ * the hook would stall the whole device on the serving path and bypass the
+ * host's memory accounting, so such code must not allocate and has no
+ * workspace to give to b4_fused_moe.
+ *
+ * What it does: the same kernels and results as b4_fused_moe, with the
+ * scratch taken from one array of B4_NOALLOC_SCRATCH_BYTES (64 MiB) that the
+ * library declares in device memory.  The CUDA runtime places that array on
+ * every GPU where it loads this library's device code, and it stays there
+ * until the process exits.  This call never calls cudaMalloc, cudaFree or any
+ * allocating library routine.
+ *
+ * Arguments: as b4_fused_moe, without workspace and workspace_bytes, plus
+ * device_status: NULL, or 2 uint32 of device memory (4-byte aligned) that
+ * receive this call's device status word in stream order -- status
+ * (B4_OK or B4_ERR_TIMEOUT) and the wait site -- which b4_check_status would
+ * otherwise read from a workspace.
+ *
+ * Limit: a shape whose b4_workspace_bytes exceeds B4_NOALLOC_SCRATCH_BYTES is
+ * refused with B4_ERR_WORKSPACE_TOO_SMALL before anything is launched, and
+ * b4_last_error gives both sizes; use b4_fused_moe for it.  With H = 4096,
+ * I = 1536 and top_k = 8, 64 MiB holds the decode path (m <= 64) and the
+ * grouped path up to m = 256.
+ *
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress, which may load the
+ * library's device code onto that device).  Make that first call before any
+ * stream capture begins on the device.
+ *
+ * Sharing: all calls on a device use the same array, and each call leaves its
+ * contents behind.  Every part of it that a call reads is written earlier in
+ * the same call (the status word by the first kernel, the fp32 top-k
+ * accumulator by FC1 before FC2 adds into it), so calls ordered on one stream
+ * do not see each other's data.  Calls that can run at the same time on the
+ * GPU -- on two streams with no event between them, or from two host threads
+ * -- race on the array and produce wrong results: keep them on one stream or
+ * order them. */
+#define B4_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+b4_status b4_fused_moe_noalloc(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
+                               const float* gs13, const uint8_t* w2, const uint8_t* s2, const float* gs2,
+                               const int32_t* topk_ids, const float* topk_weights, int32_t activation,
+                               uint16_t* out, uint32_t* device_status, b4_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* b4_status_string(int32_t status);
 

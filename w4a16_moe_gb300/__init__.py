@@ -36,6 +36,7 @@ PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_GROUPED = 2
 DECODE_MAX_M = 64
+NOALLOC_SCRATCH_BYTES = 64 << 20
 FORMATS = {"nvfp4_e4m3_k16": NVFP4, "mxfp4_e8m0_k32": MXFP4}
 ACTIVATIONS = {"silu": SILU, "relu2": RELU2}
 
@@ -78,6 +79,7 @@ def _load():
         "b4_prepare_weights": (I32, [CP, I32, I32, P, P, P, P, P]),
         "b4_route_pack": (I32, [CP, P, P, P, P, P]),
         "b4_fused_moe": (I32, [CP, P, P, P, P, P, P, P, P, P, I32, P, P, S, P]),
+        "b4_fused_moe_noalloc": (I32, [CP, P, P, P, P, P, P, P, P, P, I32, P, P, P]),
         "b4_check_status": (I32, [P, P]),
         "b4_set_timing_events": (I32, [ctypes.POINTER(P), I32]),
         "b4_set_trace": (I32, [P, S]),
@@ -99,6 +101,7 @@ EXPORTED = (
     "b4_prepare_weights",
     "b4_route_pack",
     "b4_fused_moe",
+    "b4_fused_moe_noalloc",
     "b4_check_status",
     "b4_set_timing_events",
     "b4_set_trace",
@@ -224,6 +227,31 @@ def fused_moe(cfg: MoEConfig, x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_wei
     _check(_lib.b4_fused_moe(ctypes.byref(c), _ptr(x), _ptr(w13), _ptr(s13), _ptr(gs13), _ptr(w2), _ptr(s2),
                              _ptr(gs2), _ptr(topk_ids), _ptr(topk_weights), int(activation), _ptr(out),
                              _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def fused_moe_noalloc(cfg: MoEConfig, x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, activation, out,
+                      device_status=None, stream=None):
+    """``fused_moe`` for callers that cannot allocate: the scratch is the library's
+    static device array of ``NOALLOC_SCRATCH_BYTES``; larger shapes are refused.
+    ``device_status`` (optional int32 CUDA tensor of 2) receives the call's
+    device status word.  Calls that overlap on the GPU race on the shared array."""
+    _need(x, torch.bfloat16, "x")
+    _need(out, torch.bfloat16, "out")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    for t, n in ((w13, "w13"), (s13, "s13"), (w2, "w2"), (s2, "s2")):
+        _need(t, torch.uint8, n)
+    for t, n in ((gs13, "gs13"), (gs2, "gs2")):
+        if t is not None:
+            _need(t, torch.float32, n)
+    if device_status is not None:
+        _need(device_status, torch.int32, "device_status")
+        if device_status.numel() < 2:
+            raise ValueError("device_status needs 2 elements")
+    c = cfg._c()
+    _check(_lib.b4_fused_moe_noalloc(ctypes.byref(c), _ptr(x), _ptr(w13), _ptr(s13), _ptr(gs13), _ptr(w2), _ptr(s2),
+                                     _ptr(gs2), _ptr(topk_ids), _ptr(topk_weights), int(activation), _ptr(out),
+                                     _ptr(device_status), _stream(stream)))
 
 
 def fused_moe_raw(cfg: MoEConfig, ptrs: dict, activation: int, workspace_ptr: int, workspace_bytes_: int,

@@ -208,6 +208,19 @@ cudaError_t launch_mode(int fmt, const GemmParams& p, int grid, bool pdl, cudaSt
 
 }  // namespace
 
+namespace b4 {
+// Sets the message b4_last_error returns on this thread (for entry points
+// defined in other translation units).
+void set_last_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+}
+}  // namespace b4
+
 // device-side counter of invalid scale codes found by b4_prepare_weights
 static __device__ int g_prepare_bad;
 
