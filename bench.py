@@ -195,7 +195,7 @@ class Bench:
         self.flush_sink = torch.empty(1, dtype=torch.int32, device="cuda")
         self.stream = torch.cuda.Stream()
         self.decode = m <= 4
-        self.n_kernels = 3 if self.decode else 4  # decode: FC1, FC2, finalize; grouped: pack, FC1, FC2, finalize
+        self.n_kernels = 1 if self.decode else 4  # decode: one fused kernel; grouped: pack, FC1, FC2, finalize
 
     def flush_l2(self):
         """Evict L2: write a 512 MiB buffer (evicts everything) and read it back,
@@ -327,10 +327,10 @@ def summarize(b: Bench, res, peaks):
     acct_bytes = statistics.mean(a["bytes"] for a in res["accts"])
     acct_flops = statistics.mean(a["flops"] for a in res["accts"])
     wbytes = statistics.mean(a["weight_bytes"] for a in res["accts"])
-    # GEMM kernels: decode kernels 0 (FC1) and 1 (FC2); grouped kernels 1 and 2
-    gi = (0, 1) if b.decode else (1, 2)
+    # GEMM kernels: the fused decode kernel (0); grouped FC1 (1) and FC2 (2)
+    gi = (0,) if b.decode else (1, 2)
     kern = res["kern"]
-    gemm_ms = [k[gi[0]] + k[gi[1]] for k in kern]
+    gemm_ms = [sum(k[j] for j in gi) for k in kern]
     gemm_s = 1e-3 * statistics.mean(gemm_ms)
     g_bytes = statistics.mean(a["fc1_bytes"] + a["fc2_bytes"] for a in res["accts"])
     out = {

@@ -163,7 +163,8 @@ b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32
  * FC1 accumulates gs13 * (x . w13) in fp32, applies the activation in fp32 and
  * rounds h to bf16; FC2 accumulates in fp32, multiplies by gs2 and the router
  * weight and sums the routes of a token in fp32 before one bf16 rounding.
- * Enqueues 3 (decode) or 4 (grouped) launches on `stream`; no allocation,
+ * Enqueues 1 (decode: one cooperative launch, grid no larger than the
+ * resident CTA count) or 4 (grouped) launches on `stream`; no allocation,
  * no synchronisation. */
 b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
                        const float* gs13, const uint8_t* w2, const uint8_t* s2, const float* gs2,
@@ -173,21 +174,24 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
 /* Optional per-kernel timing.  events: host array of n cudaEvent_t handles
  * (created by the caller), or NULL to turn timing off.  While set, each
  * b4_fused_moe call on this thread records events[0] on its stream before its
- * first kernel and events[i+1] after kernel i, so n must be at least the
- * number of kernels plus one: the decode path launches 3 kernels (FC1,
- * FC2, finalize), the grouped path 4 (route pack, FC1, FC2, finalize).  An event
- * recorded between two kernels removes their programmatic overlap, so timed
- * calls can be slightly slower than untimed ones; use this for measurement.
- * Returns B4_ERR_INVALID_ARGUMENT when 0 < n < 4 or events is NULL with n > 0. */
+ * first kernel and events[i+1] after kernel i, as far as n reaches: the
+ * decode path launches 1 kernel (FC1, FC2 and the top-k combine fused), the
+ * grouped path 4 (route pack, FC1, FC2, finalize), so 2 and 5 events cover
+ * them.  An event recorded between two kernels removes their programmatic
+ * overlap, so timed calls can be slightly slower than untimed ones; use this
+ * for measurement.
+ * Returns B4_ERR_INVALID_ARGUMENT when n == 1 or events is NULL with n > 0. */
 b4_status b4_set_timing_events(void* const* events, int32_t n);
 
 /* Optional kernel timeline for profiling: while `device_buffer` is set
- * (>= 163840 bytes, or NULL to turn it off), the FC1 and FC2 kernels of each
+ * (>= 163840 bytes, or NULL to turn it off), the GEMM kernels of each
  * b4_fused_moe call on this thread write clock64() timestamps of CTA 0 into
- * it: FC1 at offset 0, FC2 at offset 81920, each [5][2048] int64 -- weight
- * stage issued, A stage written to tensor memory, MMA stage issued, B
- * stage/row ready, unit epilogue done, indexed by the CTA's running counters.
- * Entries not reached are left untouched. */
+ * it as [5][2048] int64 indexed by the CTA's running counters.  Grouped path:
+ * FC1 at offset 0, FC2 at offset 81920; kinds: weight stage issued, A stage
+ * written to tensor memory, MMA stage issued, B stage ready, unit epilogue
+ * done.  Decode path (one kernel, offset 0): weight slot issued, weight slot
+ * consumed, kernel start (0) and grid barrier passed (1), activation row
+ * ready, unit done.  Entries not reached are left untouched. */
 b4_status b4_set_trace(void* device_buffer, size_t bytes);
 
 /* Synchronises `stream`, then reads the device status word of `workspace`

@@ -67,11 +67,11 @@ def test_timing_events_capture():
     """The timing hook records one event per kernel boundary, also inside a graph."""
     import w4a16_moe_gb300 as b4
 
-    wl = CASES[0][1]
-    hl = host_layer(wl, 2, seed=22)
-    dl = DeviceLayer(hl, path=1)
+    wl = CASES[1][1]
+    hl = host_layer(wl, 40, seed=22)
+    dl = DeviceLayer(hl, path=2)  # grouped: route pack, FC1, FC2, finalize
     s = torch.cuda.Stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for e in ev:
         e.record(s)
     with torch.cuda.stream(s):
@@ -86,8 +86,26 @@ def test_timing_events_capture():
         b4.set_timing_events(None)
     g.replay()
     torch.cuda.synchronize()
-    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
     assert all(t > 0 for t in ms) and sum(ms) < 1000.0, ms
     assert_parity(bf16_to_np(dl.out), oracle_out(hl), "timed replay")
     with pytest.raises(b4.B4Error):
-        b4.set_timing_events(ev[:2])
+        b4.set_timing_events(ev[:1])
+
+
+def test_timing_events_decode():
+    """The decode path is one launch: events[0] before it, events[1] after."""
+    import w4a16_moe_gb300 as b4
+
+    hl = host_layer(CASES[0][1], 2, seed=23)
+    dl = DeviceLayer(hl, path=1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    b4.set_timing_events(ev)
+    try:
+        dl.run()
+    finally:
+        b4.set_timing_events(None)
+    torch.cuda.synchronize()
+    t = ev[0].elapsed_time(ev[1])
+    assert 0 < t < 1000.0, t
+    assert_parity(bf16_to_np(dl.out), oracle_out(hl), "timed decode")

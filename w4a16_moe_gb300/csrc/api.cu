@@ -19,9 +19,9 @@
 namespace b4 {
 template <int MODE, int FMT>
 cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
-cudaError_t launch_finalize(const FinalizeParams& p, bool grouped, int num_sms, cudaStream_t stream);
-template <int MODE, int FMT>
-cudaError_t launch_decode_gemv(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_finalize(const FinalizeParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream);
+cudaError_t decode_occupancy(int fmt, int* blocks_per_sm);
 cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_route_pack(const RoutePackParams& p, cudaStream_t stream);
 size_t route_pack_smem_bytes(int num_local_experts);
@@ -145,7 +145,10 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.h = take(sizeof(uint16_t) * (size_t)L.r_cap * L.inter_pad);
   L.acc = take(sizeof(float) * (size_t)L.t_cap * cfg->hidden);
   L.xp = take(sizeof(uint16_t) * (size_t)L.r_cap * cfg->hidden);
-  L.p = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * L.wnat);
+  // FC1 partials keep their splits innermost, padded to a power of two
+  int p_splits = 1;
+  while (p_splits < L.dec_splits) p_splits <<= 1;
+  L.p = take(sizeof(float) * (size_t)p_splits * dec_rcap * L.wnat);
   L.q = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * cfg->hidden);
   L.total = off;
   return L;
@@ -183,19 +186,47 @@ b4_status device_info(DevInfo& info) {
   return B4_OK;
 }
 
-int pick_splits(int64_t base_units, int k_stages, int grid, int cap) {
-  // a decode unit holds its B slice in shared memory: at most 128 stages
-  const int min_s = (k_stages + 127) / 128;
-  int best = min_s;
-  double best_eff = -1;
-  for (int s = min_s; s <= cap; ++s) {
-    if (k_stages / s < 4 && s > min_s) break;
-    const int64_t units = base_units * s;
-    const int64_t waves = (units + grid - 1) / grid;
-    const double eff = (double)units / (double)(waves * grid);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = s;
+// Decode schedule: K splits of FC1 and FC2 and the grid.  CTA b takes units
+// b, b + G, ... (FC1 units first).  FC2 units wait for their route's FC1
+// units, so the plan is scored as two phases: the largest per-CTA FC1 load
+// plus the largest per-CTA FC2 load, in K stages plus a fixed per-unit cost.
+// A unit holds at most 128 K stages; the FC1 partials are stored with a
+// power-of-two split stride of at most max_splits rounded up.
+struct DecodePlan {
+  int s1, s2, grid;
+};
+
+DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, int grid_cap, int max_splits) {
+  constexpr double kUnitCost = 2.0;  // in K stages
+  int stride_cap = 1;
+  while (stride_cap < max_splits) stride_cap <<= 1;
+  DecodePlan best{1, 1, 1};
+  double best_load = 1e300;
+  long long best_units = 0;
+  const int min1 = (g1.k_stages + 127) / 128, min2 = (g2.k_stages + 127) / 128;
+  for (int s1 = min1; s1 <= stride_cap && s1 <= g1.k_stages; ++s1) {
+    for (int s2 = min2; s2 <= max_splits && s2 <= g2.k_stages; ++s2) {
+      const long long u1 = (long long)routes * g1.n_tiles * s1, u2 = (long long)routes * g2.n_tiles * s2;
+      const long long U = u1 + u2;
+      const int G = (int)(U < grid_cap ? U : grid_cap);
+      const double len1 = (g1.k_stages + s1 - 1) / s1 + kUnitCost, len2 = (g2.k_stages + s2 - 1) / s2 + kUnitCost;
+      // a CTA's unit counts change only at b = u1 mod G and b = U mod G, so a
+      // few representative CTAs give the largest loads
+      long long n1max = 0, n2max = 0;
+      const long long cand[6] = {0, u1 % G - 1, u1 % G, U % G - 1, U % G, (long long)G - 1};
+      for (long long b : cand) {
+        if (b < 0 || b >= G) continue;
+        const long long n_all = (U - 1 - b) / G + 1;
+        const long long n1 = b < u1 ? (u1 - 1 - b) / G + 1 : 0;
+        if (n1 > n1max) n1max = n1;
+        if (n_all - n1 > n2max) n2max = n_all - n1;
+      }
+      const double load = n1max * len1 + n2max * len2;
+      if (load < best_load - 1e-9 || (load < best_load + 1e-9 && U < best_units)) {
+        best_load = load;
+        best_units = U;
+        best = {s1, s2, G};
+      }
     }
   }
   return best;
@@ -376,44 +407,57 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
 
   FinalizeParams fp{};
   fp.m = cfg->m;
-  fp.top_k = cfg->top_k;
   fp.hidden = cfg->hidden;
-  fp.num_global_experts = cfg->num_global_experts;
-  fp.num_local_experts = cfg->num_local_experts;
-  fp.topk_ids = topk_ids;
-  fp.expert_map = cfg->expert_map;
   fp.out = out;
 
   cudaError_t e;
   if (decode) {
     const int R = cfg->m * cfg->top_k;
-    const int grid_cap = 2 * dev.sms;
-    const int s1 = pick_splits((int64_t)R * g1.n_tiles, g1.k_stages, grid_cap, L.dec_splits);
-    const int s2v = pick_splits((int64_t)R * g2.n_tiles, g2.k_stages, grid_cap, L.dec_splits);
-    float* pbuf = reinterpret_cast<float*>(ws + L.p);
-    float* qbuf = reinterpret_cast<float*>(ws + L.q);
-    p1.splits = s1;
-    p1.part_out = pbuf;
-    p2.splits = s2v;
-    p2.part_out = qbuf;
-    p2.p_in = pbuf;
-    p2.splits_in = s1;
-    const int64_t u1 = (int64_t)R * g1.n_tiles * s1, u2 = (int64_t)R * g2.n_tiles * s2v;
-    const int grid1 = (int)(u1 < grid_cap ? u1 : grid_cap), grid2 = (int)(u2 < grid_cap ? u2 : grid_cap);
-    p1.clear_status = 1;
+    int occ = 0;
+    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
+    const DecodePlan plan = plan_decode(R, g1, g2, occ * dev.sms, L.dec_splits);
+    DecodeParams dp{};
+    dp.w1_codes = w13;
+    dp.w1_scales = s13;
+    dp.gs1 = gs13;
+    dp.w2_codes = w2;
+    dp.w2_scales = s2;
+    dp.gs2 = gs2;
+    dp.n_tiles1 = g1.n_tiles;
+    dp.k_stages1 = g1.k_stages;
+    dp.n_tiles2 = g2.n_tiles;
+    dp.k_stages2 = g2.k_stages;
+    dp.m = cfg->m;
+    dp.top_k = cfg->top_k;
+    dp.num_global_experts = cfg->num_global_experts;
+    dp.num_local_experts = cfg->num_local_experts;
+    dp.hidden = cfg->hidden;
+    dp.inter_pad = L.inter_pad;
+    dp.act = act;
+    dp.topk_ids = topk_ids;
+    dp.topk_weights = topk_weights;
+    dp.expert_map = cfg->expert_map;
+    dp.x = x;
+    dp.out = out;
+    dp.s1 = plan.s1;
+    dp.s2 = plan.s2;
+    dp.s1_stride = 1;
+    while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
+    dp.units1 = R * g1.n_tiles * plan.s1;
+    dp.units2 = R * g2.n_tiles * plan.s2;
+    dp.p = reinterpret_cast<float*>(ws + L.p);
+    dp.q = reinterpret_cast<float*>(ws + L.q);
+    dp.p_floats = (size_t)R * fc1_natural_width(act, L.inter_pad) * dp.s1_stride;
+    dp.q_floats = (size_t)plan.s2 * R * cfg->hidden;
+    dp.status = status;
+    dp.trace = g_trace;
+    dp.mul_shr2 = 1u << 30;
+    dp.mul_shr16 = 1u << 16;
+    dp.mul_shr18 = 1u << 14;
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    if ((e = fmt == 0 ? launch_decode_gemv<kFc1Decode, 0>(p1, grid1, false, s)
-                      : launch_decode_gemv<kFc1Decode, 1>(p1, grid1, false, s)) != cudaSuccess)
-      return cuda_fail(e, "fc1 decode");
+    if ((e = launch_decode(dp, fmt, plan.grid, s)) != cudaSuccess) return cuda_fail(e, "decode");
     if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    if ((e = fmt == 0 ? launch_decode_gemv<kFc2Decode, 0>(p2, grid2, true, s)
-                      : launch_decode_gemv<kFc2Decode, 1>(p2, grid2, true, s)) != cudaSuccess)
-      return cuda_fail(e, "fc2 decode");
-    if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    fp.q = qbuf;
-    fp.splits = s2v;
-    if ((e = launch_finalize(fp, false, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize decode");
-    if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     return B4_OK;
   }
 
@@ -463,7 +507,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   if ((e = launch_mode<kFc2Grouped>(fmt, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");
   if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   fp.acc = acc;
-  if ((e = launch_finalize(fp, true, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize grouped");
+  if ((e = launch_finalize(fp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize grouped");
   if ((e = mark(4, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   return B4_OK;
 }
@@ -476,7 +520,7 @@ b4_status b4_set_trace(void* device_buffer, size_t bytes) {
 }
 
 b4_status b4_set_timing_events(void* const* events, int32_t n) {
-  if (n > 0 && (!events || n < 4)) return fail(B4_ERR_INVALID_ARGUMENT, "need NULL or at least 4 events");
+  if (n > 0 && (!events || n < 2)) return fail(B4_ERR_INVALID_ARGUMENT, "need NULL or at least 2 events");
   g_events = n > 0 ? events : nullptr;
   g_num_events = n > 0 ? n : 0;
   return B4_OK;

@@ -46,7 +46,7 @@ __host__ __device__ inline TensorGeom tensor_geom(int which, int act, int hidden
   return g;
 }
 
-enum GemmMode : int { kFc1Grouped = 0, kFc2Grouped = 1, kFc1Decode = 2, kFc2Decode = 3 };
+enum GemmMode : int { kFc1Grouped = 0, kFc2Grouped = 1 };
 
 struct GemmParams {
   // TMA map of the grouped B operand: packed x rows (FC1) or h rows (FC2),
@@ -74,17 +74,12 @@ struct GemmParams {
   uint16_t* xp;         // [R_cap, H] bf16: x rows in packed-route order (grouped FC1)
   const int32_t* valid_count;  // number of valid routes (offsets[E_l] of the route pack)
   const uint16_t* h;    // [R_cap, I_pad] bf16 (FC2 grouped)
-  const float* p_in;    // decode FC1 partials (FC2 decode)
-  int splits_in;        // number of FC1 partial splits (FC2 decode)
   // outputs
   uint16_t* h_out;      // FC1 grouped
   float* acc_out;       // FC2 grouped: [T_cap, H] fp32, zeroed by FC1 grouped
   size_t acc_zero_floats;  // FC1 grouped: floats of acc_out to clear
-  float* part_out;      // decode partials: FC1 -> p [S][R][N1nat], FC2 -> q [S][R][H]
-  int splits;           // split count of this decode GEMM
   uint32_t* status;     // device status word(s)
   int pdl_wait_first;   // all threads wait on the previous grid before starting
-  int clear_status;     // block 0 resets the status word (first kernel of a call)
   // Optional timeline of CTA 0 (clock64 cycles), or null: [kind][index] with
   // kinds 0 weight stage issued, 1 A stage stored to tensor memory, 2 MMA
   // stage issued, 3 B stage (grouped) or row (decode) ready, 4 epilogue of a
@@ -93,6 +88,35 @@ struct GemmParams {
 };
 
 constexpr int kTraceLen = 2048;
+
+// The small-m decode path: a preparation kernel and one fused kernel.
+struct DecodeParams {
+  const uint8_t* w1_codes;   // prepared W13 / W1
+  const uint8_t* w1_scales;
+  const float* gs1;          // [E_l] or null (MXFP4)
+  const uint8_t* w2_codes;   // prepared W2
+  const uint8_t* w2_scales;
+  const float* gs2;
+  int n_tiles1, k_stages1, n_tiles2, k_stages2;
+  int m, top_k, num_global_experts, num_local_experts, hidden, inter_pad;
+  int act;                   // 0 SwiGLU, 1 ReLU^2
+  const int32_t* topk_ids;
+  const float* topk_weights;
+  const int32_t* expert_map;  // or null
+  const uint16_t* x;         // [m, H] bf16
+  uint16_t* out;             // [m, H] bf16
+  int s1, s2;                // K splits of FC1 and FC2
+  int s1_stride;             // split stride of the FC1 partials: s1 rounded up to 1, 2, 4 or 8
+  int units1, units2;        // R * n_tiles1 * s1 and R * n_tiles2 * s2
+  float* p;                  // FC1 split partials [R][N1 natural][s1_stride]
+  float* q;                  // FC2 split partials [s2][R][H]
+  size_t p_floats, q_floats; // sizes of p and q (filled with the not-yet-written marker)
+  uint32_t* status;
+  long long* trace;          // optional timeline (see b4_set_trace)
+  // multipliers 2^30, 2^16, 2^14: right shifts by 2, 16, 18 done as
+  // multiply-high on the FMA pipe instead of the busier integer ALU pipe
+  uint32_t mul_shr2, mul_shr16, mul_shr18;
+};
 
 struct RoutePackParams {
   const int32_t* topk_ids;
@@ -110,12 +134,8 @@ struct RoutePackParams {
 };
 
 struct FinalizeParams {
-  int m, top_k, hidden, num_global_experts, num_local_experts;
-  const int32_t* topk_ids;
-  const int32_t* expert_map;
-  const float* acc;     // grouped: [m, H]
-  const float* q;       // decode: [S][R][H]
-  int splits;
+  int m, hidden;
+  const float* acc;     // [m, H] fp32 top-k sums of the grouped path
   uint16_t* out;
 };
 
@@ -128,7 +148,7 @@ struct PrepareParams {
   int* bad;             // device counter of invalid scale codes
 };
 
-// decode-split partial layout (FC1): natural index of a prepared row
+// width of the FC1 partial rows of the decode path (gate then up for SwiGLU)
 __host__ __device__ inline int fc1_natural_width(int act, int inter_pad) {
   return act == 0 ? 2 * inter_pad : inter_pad;
 }
