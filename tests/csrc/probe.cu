@@ -6,6 +6,7 @@
 
 #include <cstdint>
 
+#include "decode_stage.cuh"
 #include "dequant.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -387,6 +388,120 @@ __global__ void probe_bf16_mul_kernel(const uint32_t* a, const uint32_t* b, uint
   if (i < n) d[i] = bf16x2_mul(a[i], b[i]);
 }
 
+// Steady-state cost of the decode path's stage arithmetic, without producers:
+// every CTA (8 warps, 16 weight rows each) runs `stages` stages over
+// shared-memory data that does not change.  Dynamic shared memory pads the
+// CTA to set how many are resident per SM.  Variants: 0 as the decode kernel
+// (two stages per step, four accumulators); 1 one stage per step; 2 the
+// dequantisation alone (its results folded by bf16x2 adds); 3 the MMAs alone.
+template <int V>
+__global__ void __launch_bounds__(256) probe_decode_stage_kernel(int stages, float* out, long long* cyc) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  uint8_t* codes = sm;                  // 4 slots x 2 stages x 4096
+  uint8_t* scales = sm + 32768;         // 8 stages x 512
+  uint8_t* xrow = sm + 32768 + 4096;    // 128 stages x 128 B
+  for (int i = threadIdx.x; i < 32768 / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(codes)[i] = 0x9E3779B9u * (uint32_t)(i + 1);
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) scales[i] = (uint8_t)(0x68 + (i % 23));
+  for (int i = threadIdx.x; i < 128 * 128 / 2; i += blockDim.x)
+    reinterpret_cast<uint16_t*>(xrow)[i] = (uint16_t)(0x3F80u + (i & 0x3F));
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int r0 = 16 * warp + g;
+  const uint32_t code_off = (t >> 1) * 2048 + r0 * 16 + (t & 1) * 8;
+  const uint32_t sc_off = r0 * 4 + t;
+  float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+  float f[4] = {0.f, 0.f, 0.f, 0.f}, h4[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t fold = 0;
+  const long long t0 = clock64();
+  for (int s = 0; s < stages; s += 2) {
+    const int slot = (s >> 1) & 3;
+    const uint8_t* cs = codes + slot * 8192 + code_off;
+    const uint8_t* ss = scales + (s & 7) * 512 + sc_off;
+    const uint8_t* xr = xrow + t * 32 + (s & 126) * 128;
+    if constexpr (V == 0) {
+      StageIn a, b;
+      load_stage<4>(a, cs, ss, xr);
+      load_stage<4>(b, cs + 4096, ss + 512, xr + 128);
+      compute_stage<0>(a, d, e);
+      compute_stage<0>(b, f, h4);
+    } else if constexpr (V == 1) {
+#pragma unroll 1
+      for (int st = 0; st < 2; ++st) {
+        StageIn a;
+        load_stage<4>(a, cs + st * 4096, ss + st * 512, xr + st * 128);
+        compute_stage<0>(a, d, e);
+      }
+    } else if constexpr (V == 2) {
+      for (int st = 0; st < 2; ++st) {
+        StageIn a;
+        load_stage<4>(a, cs + st * 4096, ss + st * 512, xr + st * 128);
+        const uint32_t sa = d_scale<0>(a.b0), sb = d_scale<0>(a.b1);
+        const uint32_t w[4] = {a.c0.x, a.c0.y, a.c1.x, a.c1.y};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t sq = q < 2 ? sa : sb;
+          uint32_t v0 = bf16x2_mul(fp4x2_lookup(w[q]), sq);
+          uint32_t v1 = bf16x2_mul(fp4x2_lookup((w[q] >> 2)), sq);
+          uint32_t v2 = bf16x2_mul(fp4x2_lookup((w[q] >> 16)), sq);
+          uint32_t v3 = bf16x2_mul(fp4x2_lookup((w[q] >> 18)), sq);
+          asm("add.rn.bf16x2 %0, %0, %1;" : "+r"(fold) : "r"(v0));
+          asm("add.rn.bf16x2 %0, %0, %1;" : "+r"(fold) : "r"(v1));
+          asm("add.rn.bf16x2 %0, %0, %1;" : "+r"(fold) : "r"(v2));
+          asm("add.rn.bf16x2 %0, %0, %1;" : "+r"(fold) : "r"(v3));
+        }
+      }
+    } else {
+      for (int st = 0; st < 2; ++st) {
+        StageIn a;
+        load_stage<4>(a, cs + st * 4096, ss + st * 512, xr + st * 128);
+        mma_16816(st ? f : d, a.xa.x, a.xb.x, a.xa.y, a.xb.y, a.xa.z, a.xa.w);
+        mma_16816(st ? h4 : e, a.xa.z, a.xb.z, a.xa.w, a.xb.w, a.xb.x, a.xb.y);
+        mma_16816(st ? f : d, a.xb.x, a.xa.x, a.xb.y, a.xa.y, a.xa.x, a.xa.y);
+        mma_16816(st ? h4 : e, a.xb.z, a.xa.z, a.xb.w, a.xa.w, a.xb.z, a.xb.w);
+      }
+    }
+  }
+  const long long t1 = clock64();
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+  out[blockIdx.x * blockDim.x + threadIdx.x] = d[0] + e[0] + f[2] + h4[2] + __uint_as_float(fold & 0x3FFFFFFFu);
+}
+
+// Issue rate of single instructions: 8 warps per CTA, one CTA per SM, eight
+// independent dependency chains per thread.  op: 0 prmt, 1 lop3, 2 mul.hi.u32,
+// 3 mul.rn.bf16x2, 4 shr.b32, 5 fma.rn.f32, 6 mul.rn.f16x2, 7 fma.rn.bf16x2,
+// 8 mad.lo.u32, 9 iadd3 (add.u32).
+template <int OP>
+__global__ void __launch_bounds__(256) probe_op_tput_kernel(int iters, uint32_t k, uint32_t* out, long long* cyc) {
+  uint32_t a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = threadIdx.x * 2654435761u + i * 40503u + k;
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if constexpr (OP == 0) asm volatile("prmt.b32 %0, %0, %1, %2;" : "+r"(a[i]) : "r"(k), "r"(0x3210u ^ k));
+      if constexpr (OP == 1) asm volatile("lop3.b32 %0, %0, %1, %2, 0x96;" : "+r"(a[i]) : "r"(k), "r"(a[(i + 1) & 7]));
+      if constexpr (OP == 2) asm volatile("mul.hi.u32 %0, %0, %1;" : "+r"(a[i]) : "r"(k | 0x40000000u));
+      if constexpr (OP == 3) asm volatile("mul.rn.bf16x2 %0, %0, %1;" : "+r"(a[i]) : "r"(0x3F803F80u ^ (k & 1)));
+      if constexpr (OP == 4) asm volatile("shr.b32 %0, %0, %1;" : "+r"(a[i]) : "r"(k & 1));
+      if constexpr (OP == 5) asm volatile("fma.rn.f32 %0, %0, %1, %2;" : "+r"(a[i]) : "r"(0x3F800000u), "r"(k));
+      if constexpr (OP == 6) asm volatile("mul.rn.f16x2 %0, %0, %1;" : "+r"(a[i]) : "r"(0x3C003C00u ^ (k & 1)));
+      if constexpr (OP == 7)
+        asm volatile("fma.rn.bf16x2 %0, %0, %1, %2;" : "+r"(a[i]) : "r"(0x3F803F80u ^ (k & 1)), "r"(0u));
+      if constexpr (OP == 8) asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(a[i]) : "r"(k | 1u), "r"(k));
+      if constexpr (OP == 9) asm volatile("add.u32 %0, %0, %1;" : "+r"(a[i]) : "r"(k));
+    }
+  }
+  const long long t1 = clock64();
+  uint32_t x = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x ^= a[i];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = x;
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
 extern "C" {
 
 int probe_mma_ts(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t* status) {
@@ -438,6 +553,40 @@ int probe_dequant(const uint8_t* codes, const uint8_t* scales, int fmt, int nblo
 int probe_bf16_mul(const uint32_t* a, const uint32_t* b, uint32_t* d, int n) {
   if (n <= 0) return -1;
   probe_bf16_mul_kernel<<<(n + 127) / 128, 128>>>(a, b, d, n);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_decode_stage(int variant, int stages, int grid, int smem_bytes, float* out, long long* cyc) {
+  if (stages < 2 || stages % 2 || smem_bytes < 32768 + 4096 + 16384 || grid < 1) return -1;
+  cudaError_t e = cudaSuccess;
+#define B4_PROBE_STAGE(V)                                                                             \
+  e = cudaFuncSetAttribute(probe_decode_stage_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           smem_bytes);                                                               \
+  if (e == cudaSuccess) probe_decode_stage_kernel<V><<<grid, 256, smem_bytes>>>(stages, out, cyc);
+  switch (variant) {
+    case 0: B4_PROBE_STAGE(0); break;
+    case 1: B4_PROBE_STAGE(1); break;
+    case 2: B4_PROBE_STAGE(2); break;
+    default: B4_PROBE_STAGE(3); break;
+  }
+#undef B4_PROBE_STAGE
+  if (e != cudaSuccess) return (int)e;
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_op_tput(int op, int iters, int grid, uint32_t k, uint32_t* out, long long* cyc) {
+  switch (op) {
+    case 0: probe_op_tput_kernel<0><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 1: probe_op_tput_kernel<1><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 2: probe_op_tput_kernel<2><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 3: probe_op_tput_kernel<3><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 4: probe_op_tput_kernel<4><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 5: probe_op_tput_kernel<5><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 6: probe_op_tput_kernel<6><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 7: probe_op_tput_kernel<7><<<grid, 256>>>(iters, k, out, cyc); break;
+    case 8: probe_op_tput_kernel<8><<<grid, 256>>>(iters, k, out, cyc); break;
+    default: probe_op_tput_kernel<9><<<grid, 256>>>(iters, k, out, cyc); break;
+  }
   return (int)cudaDeviceSynchronize();
 }
 

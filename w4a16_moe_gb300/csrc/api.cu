@@ -452,9 +452,6 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     dp.q_floats = (size_t)plan.s2 * R * cfg->hidden;
     dp.status = status;
     dp.trace = g_trace;
-    dp.mul_shr2 = 1u << 30;
-    dp.mul_shr16 = 1u << 16;
-    dp.mul_shr18 = 1u << 14;
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     if ((e = launch_decode(dp, fmt, plan.grid, s)) != cudaSuccess) return cuda_fail(e, "decode");
     if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");

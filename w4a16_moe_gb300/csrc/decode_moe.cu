@@ -43,9 +43,10 @@
 // Why warp-level MMAs and not tcgen05 here: one tcgen05.mma covers 128 x 16
 // weights and costs ~165 cycles to issue whatever its N, which caps a GEMV
 // near 2 TB/s; m16n8k16 issues in a few cycles, leaving the dequantiser's
-// integer work as the limit.  That work is two ALU-pipe instructions per
-// weight pair (LOP3 + PRMT); shifts run as multiply-high on the FMA pipe and
-// the scale expansion is one IMAD.
+// integer work as the limit: per weight pair a LOP3, a PRMT and a bf16x2
+// multiply, plus three shifts per code word, all on the SM's half-rate
+// integer/bf16 pipe (measured: 2 warp-instructions per clock per SM for each
+// of them, 1 for a multiply-high), which caps the dequantiser near 5 TB/s.
 //
 // K order inside an MMA: thread t of a quad owns physical 16-element block t
 // of the 64-wide stage (one NVFP4 scale block); MMA j takes its pairs 2j and
@@ -57,6 +58,7 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
+#include "decode_stage.cuh"
 #include "dequant.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -131,23 +133,6 @@ __device__ __forceinline__ bool d_unit(const DecodeParams& p, int u, DUnit& U) {
   return U.expert >= 0 && U.kend > U.kbeg;
 }
 
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// bf16x2 block-scale multiplier of a serving scale byte, in one IMAD:
-// NVFP4 bits (b << 4) + 0x5800 (= E4M3 value * 2^63), MXFP4 bits (b + 63) << 7
-// (= 2^(e-127) * 2^63), in both halves.
-template <int FMT>
-__device__ __forceinline__ uint32_t d_scale(uint32_t b) {
-  return FMT == 0 ? b * 0x00100010u + 0x58005800u : b * 0x00800080u + 0x1F801F80u;
-}
-
 __device__ __forceinline__ void d_trace(const DecodeParams& p, int kind, uint32_t idx) {
   if (p.trace && blockIdx.x == 0 && idx < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + idx] = clock64();
 }
@@ -156,53 +141,6 @@ __device__ __forceinline__ void d_trace(const DecodeParams& p, int kind, uint32_
 // barrier passed.
 __device__ __forceinline__ void d_trace_cta(const DecodeParams& p, int kind) {
   if (p.trace && blockIdx.x < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + blockIdx.x] = (long long)globaltimer();
-}
-
-// One thread's operands of one 64-wide stage: 8 code bytes (block t) of rows
-// r0 and r1, their two scale bytes, and the 16 activations of block t.
-struct StageIn {
-  uint2 c0, c1;
-  uint32_t b0, b1;
-  uint4 xa, xb;
-};
-
-template <int SB>
-__device__ __forceinline__ void load_stage(StageIn& in, const uint8_t* cs, const uint8_t* ss, const uint8_t* xr) {
-  in.c0 = *reinterpret_cast<const uint2*>(cs);
-  in.c1 = *reinterpret_cast<const uint2*>(cs + 8 * 16);
-  in.b0 = ss[0];
-  in.b1 = ss[8 * SB];
-  in.xa = *reinterpret_cast<const uint4*>(xr);
-  in.xb = *reinterpret_cast<const uint4*>(xr + 16);
-}
-
-// Dequantise the stage's 2 x 16 weights and run its four m16n8k16 MMAs
-// (pairs 2j, 2j+1 of block t feed MMA j) into two accumulators.
-template <int FMT>
-__device__ __forceinline__ void compute_stage(const StageIn& in, float (&d)[4], float (&e)[4], uint32_t m2,
-                                              uint32_t m16, uint32_t m18) {
-  const uint32_t sa = d_scale<FMT>(in.b0), sb = d_scale<FMT>(in.b1);
-  uint32_t a0[8], a1[8];
-  a0[0] = bf16x2_mul(fp4x2_lookup(in.c0.x), sa);
-  a0[1] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c0.x, m2)), sa);
-  a0[2] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c0.x, m16)), sa);
-  a0[3] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c0.x, m18)), sa);
-  a0[4] = bf16x2_mul(fp4x2_lookup(in.c0.y), sa);
-  a0[5] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c0.y, m2)), sa);
-  a0[6] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c0.y, m16)), sa);
-  a0[7] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c0.y, m18)), sa);
-  a1[0] = bf16x2_mul(fp4x2_lookup(in.c1.x), sb);
-  a1[1] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c1.x, m2)), sb);
-  a1[2] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c1.x, m16)), sb);
-  a1[3] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c1.x, m18)), sb);
-  a1[4] = bf16x2_mul(fp4x2_lookup(in.c1.y), sb);
-  a1[5] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c1.y, m2)), sb);
-  a1[6] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c1.y, m16)), sb);
-  a1[7] = bf16x2_mul(fp4x2_lookup(__umulhi(in.c1.y, m18)), sb);
-  mma_16816(d, a0[0], a1[0], a0[1], a1[1], in.xa.x, in.xa.y);
-  mma_16816(e, a0[2], a1[2], a0[3], a1[3], in.xa.z, in.xa.w);
-  mma_16816(d, a0[4], a1[4], a0[5], a1[5], in.xb.x, in.xb.y);
-  mma_16816(e, a0[6], a1[6], a0[7], a1[7], in.xb.z, in.xb.w);
 }
 
 // The split partials of one element, stored contiguously with stride S
@@ -331,16 +269,46 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   }
   __syncthreads();
 
+  // The producers resolve the CTA's first unit and start its weight stream
+  // and (FC1) x slice before the grid barrier: neither touches the partial
+  // buffers.
+  DUnit U0;
+  const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
+  uint32_t pre_slots = 0;
+  bool pre_row = false;
+  if (warp == 0 && lane == 0 && u0_ok) {
+    const size_t tile_id = (size_t)U0.expert * (U0.fc2 ? p.n_tiles2 : p.n_tiles1) + U0.tile;
+    const int ks = U0.fc2 ? p.k_stages2 : p.k_stages1;
+    const uint8_t* gc = (U0.fc2 ? p.w2_codes : p.w1_codes) + tile_id * ks * kCodeBytesPerStage;
+    const uint8_t* gsc = (U0.fc2 ? p.w2_scales : p.w1_scales) + tile_id * ks * kSS;
+    for (int s = U0.kbeg; s < U0.kend && pre_slots < (uint32_t)kDSlots; s += kDSlotStages, ++pre_slots) {
+      const int n = min(kDSlotStages, U0.kend - s);
+      mbar_arrive_expect_tx(&full_w[pre_slots], n * (kCodeBytesPerStage + kSS));
+      bulk_g2s(s_codes + pre_slots * kDSlotStages * kCodeBytesPerStage, gc + (size_t)s * kCodeBytesPerStage,
+               n * kCodeBytesPerStage, &full_w[pre_slots]);
+      bulk_g2s(s_scales + pre_slots * kDSlotStages * kSS, gsc + (size_t)s * kSS, n * kSS, &full_w[pre_slots]);
+      d_trace(p, 0, pre_slots);
+    }
+  }
+  if (warp == 1 && lane == 0 && u0_ok && !U0.fc2) {
+    uint8_t* row = s_rows;
+    const int k0 = U0.kbeg * kBK, nk = (U0.kend - U0.kbeg) * kBK;
+    const int kv = min(nk, p.hidden - k0);
+    mbar_expect_tx(&full_b[0], (uint32_t)kv * 2);
+    bulk_g2s(row, p.x + (size_t)(U0.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, &full_b[0]);
+    for (int i = kv * 2; i < nk * 2; i += 16) *reinterpret_cast<uint4*>(row + i) = make_uint4(0, 0, 0, 0);
+    s_desc[0].u = blockIdx.x;
+    s_desc[0].expert = U0.expert;
+    s_desc[0].scale = (p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f) * kDTwo63;
+    mbar_arrive(&full_b[0]);
+    pre_row = true;
+  }
+  pre_row = __shfl_sync(0xffffffffu, pre_row, 0);
+
   // Before the grid barrier: fill both partial buffers with the not-written
   // marker, clear the status word, and zero the output rows of tokens without
-  // a valid route (no unit writes them).  The first unit's routing entry is
-  // prefetched into L2 so that resolving it after the barrier is short.
+  // a valid route (no unit writes them).
   {
-    if (threadIdx.x == 0 && (int)blockIdx.x < n_units) {
-      DUnit S0;
-      d_unit_shape(p, blockIdx.x, S0);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.topk_ids + S0.route));
-    }
     const size_t gt = (size_t)blockIdx.x * kDThreads + threadIdx.x, gstride = (size_t)gridDim.x * kDThreads;
     const uint4 mark = make_uint4(kNotWritten, kNotWritten, kNotWritten, kNotWritten);
     for (size_t i = gt; i < p.p_floats / 4; i += gstride) reinterpret_cast<uint4*>(p.p)[i] = mark;
@@ -367,10 +335,6 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   grid.sync();
   if (threadIdx.x == 0) d_trace_cta(p, 9);
 
-  // the producers resolve the CTA's first unit now
-  DUnit U0;
-  const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
-
   if (warp == 0) {
     // ------------------------------------------------------ weight stream
     if (lane == 0) {
@@ -383,6 +347,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         const uint8_t* gc = (U.fc2 ? p.w2_codes : p.w1_codes) + tile_id * ks * kCodeBytesPerStage;
         const uint8_t* gsc = (U.fc2 ? p.w2_scales : p.w1_scales) + tile_id * ks * kSS;
         for (int s = U.kbeg; s < U.kend; s += kDSlotStages, ++ws) {
+          if (ws < pre_slots) continue;  // issued before the grid barrier
           const uint32_t slot = ws % kDSlots;
           if (!mbar_wait(&empty_w[slot], ((ws / kDSlots) & 1) ^ 1, ab, 32)) break;
           const int n = min(kDSlotStages, U.kend - s);
@@ -420,6 +385,11 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
           have = true;
           break;
         }
+      }
+      if (bs == 0 && pre_row && have) {  // issued before the grid barrier
+        ++bs;
+        u += gridDim.x;
+        continue;
       }
       const uint32_t rb = bs & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&empty_b[rb], ((bs >> 1) & 1) ^ 1, ab, 33))) break;
@@ -536,7 +506,6 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   // this thread's 8 code bytes of row r0 (block t of the stage) and of row r1
   const uint32_t code_off = (t >> 1) * (kCodeBytesPerStage / 2) + r0 * 16 + (t & 1) * 8;
   const uint32_t sc_off = FMT == 0 ? r0 * SB + t : r0 * SB + (t >> 1);
-  const uint32_t m2 = p.mul_shr2, m16 = p.mul_shr16, m18 = p.mul_shr18;
   const int wnat = fc1_natural_width(p.act, p.inter_pad);
   uint32_t ws = 0, bs = 0, es = 0;
   while (true) {
@@ -579,10 +548,10 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         // both stages' shared-memory loads are in flight before any math
         StageIn b;
         load_stage<SB>(b, cs + kCodeBytesPerStage, ss + kSS, xr + kBK * 2);
-        compute_stage<FMT>(a, d, e, m2, m16, m18);
-        compute_stage<FMT>(b, f, h4, m2, m16, m18);
+        compute_stage<FMT>(a, d, e);
+        compute_stage<FMT>(b, f, h4);
       } else {
-        compute_stage<FMT>(a, d, e, m2, m16, m18);
+        compute_stage<FMT>(a, d, e);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_w[slot]);

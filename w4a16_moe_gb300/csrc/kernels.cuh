@@ -113,9 +113,6 @@ struct DecodeParams {
   size_t p_floats, q_floats; // sizes of p and q (filled with the not-yet-written marker)
   uint32_t* status;
   long long* trace;          // optional timeline (see b4_set_trace)
-  // multipliers 2^30, 2^16, 2^14: right shifts by 2, 16, 18 done as
-  // multiply-high on the FMA pipe instead of the busier integer ALU pipe
-  uint32_t mul_shr2, mul_shr16, mul_shr18;
 };
 
 struct RoutePackParams {
