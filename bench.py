@@ -320,6 +320,38 @@ class Bench:
         return {"seconds": total, "h2d": h2d, "d2h": d2h}
 
 
+# DRAM traffic of the dominant kernel(s) per call, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum; the summaries under profiles/
+# give the commands).  A figure is reported only while the kernel sources still
+# hash to the profiled ones; after any change it is null until re-measured.
+KERNEL_SOURCES = {
+    "decode": ["decode_moe.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
+    "grouped": ["moe_gemm.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
+}
+NCU_TRAFFIC = {  # (path, workload, m): (source hash, bytes per call of the GEMM kernel(s))
+    ("decode", "decode:relu2", 1): ("92873967035bbfb0", 56_736_512 + 380_928),
+    ("grouped", "prefill:silu", 2048): ("c8dc2932b10dd80f", 1_040_686_000 + 81_905_664 + 599_862_000 + 85_172_736),
+}
+
+
+def kernel_source_hash(path):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[path]:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "w4a16_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(b):
+    path = "decode" if b.decode else "grouped"
+    rec = NCU_TRAFFIC.get((path, f"{b.wl.name}:{b.wl.act}", b.m))
+    if rec is None or rec[0] != kernel_source_hash(path):
+        return None
+    return rec[1]
+
+
 def summarize(b: Bench, res, peaks):
     wl, m = b.wl, b.m
     ms = res["ms"]
@@ -348,12 +380,12 @@ def summarize(b: Bench, res, peaks):
     if b.decode or m <= 64:
         ach = g_bytes / gemm_s / 1e9
         out["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                           "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(b),
                            "peak_src": peaks["src"]}
     else:
         ach = acct_flops / gemm_s / 1e12
         out["roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
-                           "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
+                           "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": measured_traffic(b),
                            "peak_src": peaks["src"]}
     return out
 
@@ -472,8 +504,10 @@ def main():
                    "tokens_per_s": round(head["tokens_per_s"] * world, 1),
                    "weight_stream_TBps": head["weight_stream_TBps"], "bf16_TFLOPs": head["bf16_TFLOPs"]},
         "roofline": {k: v for k, v in head["roofline"].items() if k != "peak_src"},
-        "roofline_note": f"dominant kernel: W4A16 GEMM (FC1 + FC2 launches), peak of {head['roofline']['peak_src']} "
-                         f"MEASURED_PEAKS.json",
+        "roofline_note": (("dominant kernel: the fused decode kernel (FC1, FC2 and combine in one launch)"
+                           if b.decode else "dominant kernels: the grouped FC1 and FC2 GEMM launches")
+                          + f"; peak of {head['roofline']['peak_src']} MEASURED_PEAKS.json; traffic = ncu DRAM "
+                          "bytes per call of those launches (null if their sources changed since the capture)"),
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": b.n_kernels * args.steps,

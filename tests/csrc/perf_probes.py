@@ -1,0 +1,77 @@
+"""Drivers for the timing probes in probe.cu (not run by pytest).
+
+    python tests/csrc/perf_probes.py ops     issue rate of single instructions per SM
+    python tests/csrc/perf_probes.py stage   throughput of the decode stage arithmetic
+    python tests/csrc/perf_probes.py mma     tcgen05.mma cycles per instruction
+
+Needs a GPU and tests/csrc/libb4probe.so (built by __graft_entry__.build()).
+"""
+
+import ctypes
+import os
+import sys
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB = ctypes.CDLL(os.path.join(HERE, "libb4probe.so"))
+
+
+def ops():
+    f = LIB.probe_op_tput
+    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    names = ["prmt", "lop3", "mul.hi.u32", "mul.rn.bf16x2", "shr.b32", "fma.rn.f32", "mul.rn.f16x2",
+             "fma.rn.bf16x2", "mad.lo.u32", "add.u32"]
+    iters = 4096
+    out = torch.zeros(sms * 256, dtype=torch.int32, device="cuda")
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    for op, nm in enumerate(names):
+        assert f(op, 64, sms, 3, out.data_ptr(), cyc.data_ptr()) == 0
+        assert f(op, iters, sms, 3, out.data_ptr(), cyc.data_ptr()) == 0
+        rate = 8 * 8 * iters / cyc.double().mean().item()
+        print(f"{nm:14s} {rate:.2f} warp-instructions / clock / SM")
+
+
+def stage():
+    f = LIB.probe_decode_stage
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    stages = 4096
+    names = ["as the decode kernel", "one stage per step", "dequantisation only", "MMAs only"]
+    for per_sm, smem in ((1, 200 * 1024), (2, 104 * 1024), (3, 70 * 1024), (4, 53 * 1024)):
+        grid = sms * per_sm
+        out = torch.zeros(grid * 256, device="cuda")
+        cyc = torch.zeros(grid, dtype=torch.int64, device="cuda")
+        for v in range(4):
+            assert f(v, 256, grid, smem, out.data_ptr(), cyc.data_ptr()) == 0
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            assert f(v, stages, grid, smem, out.data_ptr(), cyc.data_ptr()) == 0
+            e.record()
+            torch.cuda.synchronize()
+            ms = s.elapsed_time(e)
+            gbs = grid * stages * 4608 / (ms * 1e-3) / 1e9
+            print(f"CTAs/SM {per_sm}, {names[v]:22s}: {gbs:6.0f} GB/s of 4-bit weights, "
+                  f"{cyc.double().mean().item() / stages:5.0f} cycles / stage / CTA")
+
+
+def mma():
+    f = LIB.probe_mma_tput
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for name, v in (("N=160, A tmem, 1 acc", 1), ("N=160, A smem, 1 acc", 2 | 1), ("N=160, A smem, 2 acc", 2 | 1 | 16),
+                    ("N=256, A smem, 1 acc", 2 | 8), ("N=256, A smem, 2 acc", 2 | 8 | 16),
+                    ("N=16,  A smem, 2 acc", 2 | 16)):
+        for per, pc in ((4, 4), (4, 0)):
+            assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0
+            assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0
+            t1, t2 = out.tolist()
+            n = 64 * per
+            commit = "one commit per 4" if pc else "no commits"
+            print(f"{name}, {commit:16s}: {t1 / n:6.1f} cycles / MMA issued, {t2 / n:6.1f} to completion")
+
+
+if __name__ == "__main__":
+    {"ops": ops, "stage": stage, "mma": mma}[sys.argv[1]]()

@@ -337,11 +337,13 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
       for (int kk = 0; kk < per; ++kk) {
         const uint64_t bdesc = smem_desc_noswizzle(smem_u32(sB) + (kk & 3) * 256, 128, 1024);
         if (variant & 2) {
+          // variant bit 16: MMAs alternate between two accumulators (columns 0 and 256)
+          const uint32_t dcol = (variant & 16) ? ((kk & 1) ? 256u : 0u) : 192u;
           const uint64_t adesc = smem_desc_noswizzle(smem_u32(sA) + (kk & 3) * 256, 128, 1024);
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(base + 192),
-              "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)(s > 0 || kk > 0))
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(base + dcol),
+              "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)(s > 0 || kk > 1))
               : "memory");
         } else {
           mma_bf16_ts(base + 192, base + (kk & 3) * 8, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
