@@ -3,6 +3,7 @@
     python tests/csrc/perf_probes.py ops     issue rate of single instructions per SM
     python tests/csrc/perf_probes.py stage   throughput of the decode stage arithmetic
     python tests/csrc/perf_probes.py mma     tcgen05.mma cycles per instruction
+    python tests/csrc/perf_probes.py launch  launch latency of an empty kernel inside a CUDA graph
 
 Needs a GPU and tests/csrc/libb4probe.so (built by __graft_entry__.build()).
 """
@@ -73,5 +74,37 @@ def mma():
             print(f"{name}, {commit:16s}: {t1 / n:6.1f} cycles / MMA issued, {t2 / n:6.1f} to completion")
 
 
+def launch():
+    f = LIB.probe_launch
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for name, grid, block, smem, coop in (("1 x 32, no smem", 1, 32, 0, 0),
+                                          (f"{2 * sms} x 352, 70 KB", 2 * sms, 352, 70 * 1024, 0),
+                                          (f"{2 * sms} x 352, 70 KB, cooperative", 2 * sms, 352, 70 * 1024, 1),
+                                          (f"{sms} x 512, 172 KB", sms, 512, 172 * 1024, 0)):
+        with torch.cuda.stream(s):
+            assert f(grid, block, smem, coop, out.data_ptr(), s.cuda_stream) == 0
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            assert f(grid, block, smem, coop, out.data_ptr(), s.cuda_stream) == 0
+        times = []
+        for i in range(30):
+            with torch.cuda.stream(s):
+                flush.zero_()  # keeps the GPU busy while the host queues the replay
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                g.replay()
+                b.record(s)
+            s.synchronize()
+            if i >= 5:
+                times.append(a.elapsed_time(b) * 1e3)
+        times.sort()
+        print(f"{name:40s}: median {times[len(times) // 2]:.2f} us per graph replay (event to event)")
+
+
 if __name__ == "__main__":
-    {"ops": ops, "stage": stage, "mma": mma}[sys.argv[1]]()
+    {"ops": ops, "stage": stage, "mma": mma, "launch": launch}[sys.argv[1]]()

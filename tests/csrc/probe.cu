@@ -504,6 +504,13 @@ __global__ void __launch_bounds__(256) probe_op_tput_kernel(int iters, uint32_t 
   if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
 }
 
+// Empty kernel for launch-latency measurements (grid, block, dynamic shared
+// memory and the cooperative attribute chosen by the caller).
+__global__ void probe_launch_kernel(int* out) {
+  extern __shared__ int sm_launch[];
+  if (threadIdx.x == 0 && blockIdx.x == 0 && out) out[0] = sm_launch[0] * 0 + 1;
+}
+
 extern "C" {
 
 int probe_mma_ts(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t* status) {
@@ -590,6 +597,26 @@ int probe_op_tput(int op, int iters, int grid, uint32_t k, uint32_t* out, long l
     default: probe_op_tput_kernel<9><<<grid, 256>>>(iters, k, out, cyc); break;
   }
   return (int)cudaDeviceSynchronize();
+}
+
+int probe_launch(int grid, int block, int smem_bytes, int cooperative, int* out, void* stream) {
+  static int configured = 0;
+  if (smem_bytes > configured) {
+    cudaError_t e = cudaFuncSetAttribute(probe_launch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return (int)e;
+    configured = smem_bytes;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 1 : 0;
+  return (int)cudaLaunchKernelEx(&cfg, probe_launch_kernel, out);
 }
 
 }  // extern "C"

@@ -186,50 +186,41 @@ b4_status device_info(DevInfo& info) {
   return B4_OK;
 }
 
-// Decode schedule: K splits of FC1 and FC2 and the grid.  CTA b takes units
-// b, b + G, ... (FC1 units first).  FC2 units wait for their route's FC1
-// units, so the plan is scored as two phases: the largest per-CTA FC1 load
-// plus the largest per-CTA FC2 load, in K stages plus a fixed per-unit cost.
-// A unit holds at most 128 K stages; the FC1 partials are stored with a
-// power-of-two split stride of at most max_splits rounded up.
+// Decode schedule: K splits of FC1 and FC2 and the grid.  CTAs take their
+// first unit statically and claim the rest in unit order, so load balance is
+// dynamic; the splits aim at about two units per CTA of each GEMM with at
+// least 12 (or 20, below) K stages per unit (a unit holds at most 128; FC1
+// needs at most 4 splits below 512 K stages).  The FC1 partials
+// are stored with a power-of-two split stride of at most max_splits rounded
+// up.
 struct DecodePlan {
   int s1, s2, grid;
 };
 
 DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, int grid_cap, int max_splits) {
-  constexpr double kUnitCost = 2.0;  // in K stages
   int stride_cap = 1;
   while (stride_cap < max_splits) stride_cap <<= 1;
-  DecodePlan best{1, 1, 1};
-  double best_load = 1e300;
-  long long best_units = 0;
-  const int min1 = (g1.k_stages + 127) / 128, min2 = (g2.k_stages + 127) / 128;
-  for (int s1 = min1; s1 <= stride_cap && s1 <= g1.k_stages; ++s1) {
-    for (int s2 = min2; s2 <= max_splits && s2 <= g2.k_stages; ++s2) {
-      const long long u1 = (long long)routes * g1.n_tiles * s1, u2 = (long long)routes * g2.n_tiles * s2;
-      const long long U = u1 + u2;
-      const int G = (int)(U < grid_cap ? U : grid_cap);
-      const double len1 = (g1.k_stages + s1 - 1) / s1 + kUnitCost, len2 = (g2.k_stages + s2 - 1) / s2 + kUnitCost;
-      // a CTA's unit counts change only at b = u1 mod G and b = U mod G, so a
-      // few representative CTAs give the largest loads
-      long long n1max = 0, n2max = 0;
-      const long long cand[6] = {0, u1 % G - 1, u1 % G, U % G - 1, U % G, (long long)G - 1};
-      for (long long b : cand) {
-        if (b < 0 || b >= G) continue;
-        const long long n_all = (U - 1 - b) / G + 1;
-        const long long n1 = b < u1 ? (u1 - 1 - b) / G + 1 : 0;
-        if (n1 > n1max) n1max = n1;
-        if (n_all - n1 > n2max) n2max = n_all - n1;
-      }
-      const double load = n1max * len1 + n2max * len2;
-      if (load < best_load - 1e-9 || (load < best_load + 1e-9 && U < best_units)) {
-        best_load = load;
-        best_units = U;
-        best = {s1, s2, G};
-      }
-    }
-  }
-  return best;
+  // When FC1 has at most half as many (route, tile) pairs as CTAs (m = 1 on
+  // the decode workload), units of >= 20 stages measured faster than >= 12:
+  // every unit adds about a microsecond of hand-over.
+  const int min_stages = 2LL * routes * g1.n_tiles <= grid_cap ? 20 : 12;
+  auto pick = [&](const TensorGeom& g, int cap) {
+    const long long base = (long long)routes * g.n_tiles;
+    int s = (int)((2LL * grid_cap + base - 1) / base);
+    const int most = g.k_stages / min_stages > 1 ? g.k_stages / min_stages : 1;
+    if (s > most) s = most;
+    if (s > cap) s = cap;
+    const int least = (g.k_stages + 127) / 128;
+    return s < least ? least : s;
+  };
+  DecodePlan plan;
+  // at most 4 FC1 splits: an FC2 unit sums that many partials per h element,
+  // and with a stride of 8 its loads take more round trips
+  plan.s1 = pick(g1, stride_cap < 4 ? stride_cap : 4);
+  plan.s2 = pick(g2, max_splits);
+  const long long U = (long long)routes * (g1.n_tiles * plan.s1 + g2.n_tiles * plan.s2);
+  plan.grid = (int)(U < grid_cap ? U : grid_cap);
+  return plan;
 }
 
 template <int MODE>
@@ -449,6 +440,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     dp.p = reinterpret_cast<float*>(ws + L.p);
     dp.q = reinterpret_cast<float*>(ws + L.q);
     dp.p_floats = (size_t)R * fc1_natural_width(act, L.inter_pad) * dp.s1_stride;
+    dp.ticket = reinterpret_cast<int*>(ws + L.status + 64);
     dp.q_floats = (size_t)plan.s2 * R * cfg->hidden;
     dp.status = status;
     dp.trace = g_trace;

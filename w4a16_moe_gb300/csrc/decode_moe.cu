@@ -83,7 +83,7 @@ struct DSmem {
   static constexpr size_t scales = (size_t)kDSlots * kDSlotStages * kCodeBytesPerStage;
   static constexpr size_t rows = scales + (size_t)kDSlots * kDSlotStages * kScaleStage;
   static constexpr size_t bars = rows + 2 * (size_t)kDRowBytes;
-  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 8);
+  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 10);
   static constexpr size_t desc = misc + 16;
   static constexpr size_t total = desc + 4 * 16;  // four 16-byte unit descriptors
 };
@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   uint64_t* empty_b = full_b + 2;
   uint64_t* epi_full = empty_b + 2;
   uint64_t* epi_empty = epi_full + 2;
+  uint64_t* desc_full = epi_empty + 2;  // a unit descriptor is ready (for the weight stream)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::misc);
   DDesc* s_desc = reinterpret_cast<DDesc*>(smem + L::desc);  // [2] with the rows
   DDesc* s_edesc = s_desc + 2;                                  // [2] for the output warp
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
       mbar_init(&empty_b[i], kDComputeWarps);
       mbar_init(&epi_full[i], kDComputeWarps);
       mbar_init(&epi_empty[i], 1);
+      mbar_init(&desc_full[i], 1);
     }
     fence_mbar_init();
   }
@@ -301,6 +303,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
     s_desc[0].expert = U0.expert;
     s_desc[0].scale = (p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f) * kDTwo63;
     mbar_arrive(&full_b[0]);
+    mbar_arrive(&desc_full[0]);
     pre_row = true;
   }
   pre_row = __shfl_sync(0xffffffffu, pre_row, 0);
@@ -313,9 +316,12 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
     const uint4 mark = make_uint4(kNotWritten, kNotWritten, kNotWritten, kNotWritten);
     for (size_t i = gt; i < p.p_floats / 4; i += gstride) reinterpret_cast<uint4*>(p.p)[i] = mark;
     for (size_t i = gt; i < p.q_floats / 4; i += gstride) reinterpret_cast<uint4*>(p.q)[i] = mark;
-    if (gt == 0 && p.status) {
-      p.status[0] = 0;
-      p.status[1] = 0;
+    if (gt == 0) {
+      *p.ticket = 0;
+      if (p.status) {
+        p.status[0] = 0;
+        p.status[1] = 0;
+      }
     }
     const int gw = (int)(gt >> 5), nw = (int)(gstride >> 5);
     for (int tk = gw; tk < p.m; tk += nw) {
@@ -337,11 +343,17 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
 
   if (warp == 0) {
     // ------------------------------------------------------ weight stream
+    // follows the unit sequence that warp 1 publishes in the descriptors
     if (lane == 0) {
       uint32_t ws = 0;
-      for (int u = blockIdx.x; u < n_units && !ab.raised(); u += gridDim.x) {
-        DUnit U = U0;
-        if (u == (int)blockIdx.x ? !u0_ok : !d_unit(p, u, U)) continue;
+      for (uint32_t ds = 0; !ab.raised(); ++ds) {
+        const uint32_t rb = ds & 1;
+        if (!mbar_wait(&desc_full[rb], (ds >> 1) & 1, ab, 31)) break;
+        const int u = s_desc[rb].u;
+        if (u < 0) break;
+        DUnit U;
+        d_unit_shape(p, u, U);
+        U.expert = s_desc[rb].expert;
         const size_t tile_id = (size_t)U.expert * (U.fc2 ? p.n_tiles2 : p.n_tiles1) + U.tile;
         const int ks = U.fc2 ? p.k_stages2 : p.k_stages1;
         const uint8_t* gc = (U.fc2 ? p.w2_codes : p.w1_codes) + tile_id * ks * kCodeBytesPerStage;
@@ -373,23 +385,26 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
 
   if (warp == 1) {
     // ------------------------------------- unit schedule and activation rows
-    // Resolves each unit once and passes it to the compute warps with the FC1
-    // x slice; a unit index of -1 ends the sequence.
+    // The CTA's first unit is unit blockIdx.x; later ones are claimed from a
+    // counter in unit order (a CTA that runs faster takes more).  Each unit is
+    // resolved once and published with the FC1 x slice in one of two
+    // descriptor/row slots; a unit index of -1 ends the sequence.
     uint32_t bs = 0;
+    DUnit U = U0;
     int u = blockIdx.x;
+    bool have = u0_ok;
+    if (pre_row) {  // the first unit went out before the grid barrier
+      bs = 1;
+      have = false;
+    }
     while (!ab.raised()) {
-      DUnit U = U0;
-      bool have = false;
-      for (; u < n_units; u += gridDim.x) {
-        if (u == (int)blockIdx.x ? u0_ok : d_unit(p, u, U)) {
-          have = true;
-          break;
-        }
-      }
-      if (bs == 0 && pre_row && have) {  // issued before the grid barrier
-        ++bs;
-        u += gridDim.x;
-        continue;
+      // next valid unit: claims are issued one unit ahead of their use
+      while (!have) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(p.ticket, 1);
+        u = (int)gridDim.x + __shfl_sync(0xffffffffu, t, 0);
+        if (u >= n_units) break;
+        have = d_unit(p, u, U);
       }
       const uint32_t rb = bs & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&empty_b[rb], ((bs >> 1) & 1) ^ 1, ab, 33))) break;
@@ -398,6 +413,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         if (lane == 0) {
           dsc->u = -1;
           mbar_arrive(&full_b[rb]);
+          mbar_arrive(&desc_full[rb]);
         }
         break;
       }
@@ -413,23 +429,27 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
           for (int i = kv * 2; i < nk * 2; i += 16) *reinterpret_cast<uint4*>(row + i) = make_uint4(0, 0, 0, 0);
           dsc->u = u;
           dsc->expert = U.expert;
+          mbar_arrive(&desc_full[rb]);  // the weight stream needs only the unit
           dsc->scale = (p.gs1 ? __ldg(p.gs1 + U.expert) : 1.0f) * kDTwo63;
           mbar_arrive(&full_b[rb]);
         }
       } else {
+        if (lane == 0) {
+          dsc->u = u;
+          dsc->expert = U.expert;
+          mbar_arrive(&desc_full[rb]);
+        }
         const int token = U.route / p.top_k;
         const bool v = lane < p.top_k && d_local_expert(p, token * p.top_k + lane) >= 0;
         const uint32_t mask = __ballot_sync(0xffffffffu, v);
         if (lane == 0) {
-          dsc->u = u;
-          dsc->expert = U.expert;
           dsc->scale = (p.gs2 ? __ldg(p.gs2 + U.expert) : 1.0f) * kDTwo63 * __ldg(p.topk_weights + U.route);
           dsc->mask = mask;
           mbar_arrive(&full_b[rb]);
         }
       }
       ++bs;
-      u += gridDim.x;
+      have = false;
     }
     if (ab.raised() && lane == 0) {
       for (uint32_t i = bs > 2 ? bs - 2 : 0; i < bs; ++i) {

@@ -111,6 +111,7 @@ struct DecodeParams {
   float* p;                  // FC1 split partials [R][N1 natural][s1_stride]
   float* q;                  // FC2 split partials [s2][R][H]
   size_t p_floats, q_floats; // sizes of p and q (filled with the not-yet-written marker)
+  int* ticket;               // units [grid, units1 + units2) are claimed from this counter
   uint32_t* status;
   long long* trace;          // optional timeline (see b4_set_trace)
 };

@@ -9,8 +9,9 @@
 // atomics and no allocation, so the result is bit-exact and the launch is
 // capture-safe:
 //   pass 1  each warp walks its contiguous segment of routes 32 at a time;
-//           __match_any_sync groups lanes with the same local expert and the
-//           group leader adds the group size to the warp's histogram row;
+//           lanes with the same local expert are grouped (one ballot per key
+//           bit) and the group leader adds the group size to the warp's
+//           histogram row;
 //   pass 2  per expert, an exclusive scan over the 32 warp rows gives each
 //           warp its base, and a warp-shuffle scan over experts gives offsets;
 //   pass 3  the segments are walked again; a route lands at
@@ -33,6 +34,20 @@ __device__ __forceinline__ int pack_local_expert(const RoutePackParams& p, int r
   if (id < 0 || id >= p.num_global_experts) return -1;
   const int l = p.expert_map ? p.expert_map[id] : id;
   return (l >= 0 && l < p.num_local_experts) ? l : -1;
+}
+
+// Lanes of the warp holding the same key as this lane (keys in [-1, 2^nbits)),
+// from one ballot per key bit plus one for validity: the result equals
+// __match_any_sync, which issues far slower on this GPU.
+__device__ __forceinline__ unsigned key_peers(int key, int nbits) {
+  const unsigned valid = __ballot_sync(0xffffffffu, key >= 0);
+  unsigned m = key >= 0 ? valid : ~valid;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = key >= 0 && ((key >> b) & 1);
+    const unsigned bb = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
 }
 
 // Exclusive block-wide scan of one value per thread (1024 threads).
@@ -76,6 +91,8 @@ __global__ void __launch_bounds__(kPackThreads, 1) route_pack_kernel(const __gri
   const int beg = warp * seg;
   const int end = min(R, beg + seg);
   const unsigned lt_mask = (1u << lane) - 1u;
+  int nbits = 0;
+  while ((1 << nbits) < E) ++nbits;
 
   if (threadIdx.x == 0 && p.status) {
     p.status[0] = 0;
@@ -98,7 +115,7 @@ __global__ void __launch_bounds__(kPackThreads, 1) route_pack_kernel(const __gri
     for (int i = 0; i < kKeys; ++i) {
       if (b0 + 32 * i >= end) break;
       const int key = keys[i];
-      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      const unsigned peers = key_peers(key, nbits);
       if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
       __syncwarp();
     }
@@ -154,7 +171,7 @@ __global__ void __launch_bounds__(kPackThreads, 1) route_pack_kernel(const __gri
       if (b0 + 32 * i >= end) break;
       const int r = b0 + 32 * i + lane;
       const int key = keys[i];
-      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      const unsigned peers = key_peers(key, nbits);
       if (key >= 0) {
         const int pos = s_off[key] + my_hist[key] + __popc(peers & lt_mask);
         p.sorted_routes[pos] = r;
