@@ -23,7 +23,7 @@ cudaError_t launch_finalize(const FinalizeParams& p, int num_sms, cudaStream_t s
 cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream);
 cudaError_t decode_occupancy(int fmt, int* blocks_per_sm);
 cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream);
-cudaError_t launch_route_pack(const RoutePackParams& p, cudaStream_t stream);
+cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream);
 size_t route_pack_smem_bytes(int num_local_experts);
 cudaError_t launch_prepare(const PrepareParams& p, int num_sms, cudaStream_t stream);
 }  // namespace b4
@@ -328,7 +328,7 @@ b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32
   p.counts = counts;
   p.offsets = offsets;
   p.sorted_routes = sorted_routes;
-  cudaError_t e = launch_route_pack(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_route_pack(p, dev.sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? B4_OK : cuda_fail(e, "route_pack");
 }
 
@@ -466,7 +466,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   rp.chunk_rows = kChunkRows;
   rp.status = status;
   if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-  if ((e = launch_route_pack(rp, s)) != cudaSuccess) return cuda_fail(e, "route pack");
+  if ((e = launch_route_pack(rp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "route pack");
   if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
 
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.h);

@@ -5,55 +5,43 @@
 // ("covering expert_map, invalid expert ids, preallocated buffers, and the
 // workspace capacity contract").
 //
-// One CTA of 1024 threads performs a stable counting sort with no global
-// atomics and no allocation, so the result is bit-exact and the launch is
-// capture-safe:
-//   pass 1  each warp walks its contiguous segment of routes 32 at a time;
-//           lanes with the same local expert are grouped (one ballot per key
-//           bit) and the group leader adds the group size to the warp's
-//           histogram row;
-//   pass 2  per expert, an exclusive scan over the 32 warp rows gives each
-//           warp its base, and a warp-shuffle scan over experts gives offsets;
-//   pass 3  the segments are walked again; a route lands at
-//           offsets[l] + warp base + running count + rank among equal lanes.
-// Routes of one expert therefore keep ascending flat index r = t*top_k + j.
-// The same kernel also emits the grouped-GEMM schedule: each expert's routes
-// cut into chunks of at most `chunk_rows`.
+// A stable counting sort without global atomics, so the result is bit-exact
+// and the launch is capture-safe.  Every CTA (512 threads) builds the full
+// histogram of local experts in shared memory, one row per warp over the
+// warp's contiguous segment of routes (the ids of eight 32-route groups are
+// loaded before any is used), and scans it into expert offsets and, per
+// expert, each warp's base (the same numbers in every CTA).  CTA b then owns
+// experts b, b + G, ...: each warp walks its segment again and a route of the
+// expert lands at offsets[l] + warp base + running count + its rank in the
+// group's ballot, so routes keep ascending flat index r = t*top_k + j.
+// CTA 0 also writes counts, offsets, the grouped-GEMM chunk schedule (each
+// expert's routes cut into chunks of at most `chunk_rows`), the -1 tail of
+// the capacity and the cleared status word.  The ids are read a few times per
+// CTA; they stay in L2.
 
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace b4 {
 
-constexpr int kPackThreads = 1024;
+constexpr int kPackThreads = 512;
 constexpr int kPackWarps = kPackThreads / 32;
-constexpr int kKeys = 16;  // 32-route batches whose keys a warp loads together
+constexpr int kBatch = 8;  // 32-route groups whose keys a warp loads before using any
 
 __device__ __forceinline__ int pack_local_expert(const RoutePackParams& p, int r) {
-  const int id = p.topk_ids[r];
+  const int id = __ldg(p.topk_ids + r);
   if (id < 0 || id >= p.num_global_experts) return -1;
-  const int l = p.expert_map ? p.expert_map[id] : id;
+  const int l = p.expert_map ? __ldg(p.expert_map + id) : id;
   return (l >= 0 && l < p.num_local_experts) ? l : -1;
 }
 
-// Lanes of the warp holding the same key as this lane (keys in [-1, 2^nbits)),
-// from one ballot per key bit plus one for validity: the result equals
-// __match_any_sync, which issues far slower on this GPU.
-__device__ __forceinline__ unsigned key_peers(int key, int nbits) {
-  const unsigned valid = __ballot_sync(0xffffffffu, key >= 0);
-  unsigned m = key >= 0 ? valid : ~valid;
-  for (int b = 0; b < nbits; ++b) {
-    const bool bit = key >= 0 && ((key >> b) & 1);
-    const unsigned bb = __ballot_sync(0xffffffffu, bit);
-    m &= bit ? bb : ~bb;
-  }
-  return m;
-}
-
-// Exclusive block-wide scan of one value per thread (1024 threads).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+// In-place exclusive scan of s[0..n) (n <= 2 * kPackThreads) by the block;
+// returns the total.
+__device__ __forceinline__ int block_scan(int* s, int n, int* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  const int i0 = 2 * threadIdx.x;
+  const int a = i0 < n ? s[i0] : 0, b = i0 + 1 < n ? s[i0 + 1] : 0;
+  int incl = a + b;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, d);
@@ -62,135 +50,126 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& tot
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = s_warp[lane];
+    const int w = lane < kPackWarps ? s_warp[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, wi, d);
       if (lane >= d) wi += y;
     }
-    s_warp[lane] = wi - w;  // exclusive prefix of warp totals
-    if (lane == 31) s_warp[32] = wi;
+    if (lane < kPackWarps) s_warp[lane] = wi - w;
+    if (lane == 31) s_warp[kPackWarps] = wi;
   }
   __syncthreads();
-  total = s_warp[32];
-  const int out = incl - v + s_warp[warp];
+  const int base = incl - (a + b) + s_warp[warp];
+  if (i0 < n) s[i0] = base;
+  if (i0 + 1 < n) s[i0 + 1] = base + a;
+  const int total = s_warp[kPackWarps];
   __syncthreads();
-  return out;
+  return total;
 }
 
-__global__ void __launch_bounds__(kPackThreads, 1) route_pack_kernel(const __grid_constant__ RoutePackParams p) {
-  extern __shared__ int s_hist[];  // [32][E_l], then [E_l] offsets
-  __shared__ int s_warp[33];
-  __shared__ int s_valid;
+__global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_constant__ RoutePackParams p) {
+  extern __shared__ int s_mem[];
   const int E = p.num_local_experts;
-  int* s_off = s_hist + kPackWarps * E;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int* s_whist = s_mem;                   // [warps][E]: counts, then each warp's base within the expert
+  int* s_cnt = s_mem + kPackWarps * E;    // [E]: counts, then offsets; CTA 0 also [E] chunk starts, [E] scratch
+  __shared__ int s_warp[kPackWarps + 1];
   const int R = p.m * p.top_k;
-  const int seg = round_up(cdiv(R, kPackWarps), 32);
-  const int beg = warp * seg;
-  const int end = min(R, beg + seg);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  int nbits = 0;
-  while ((1 << nbits) < E) ++nbits;
+  // each warp owns a contiguous segment of routes (the same in every pass)
+  const int seg = round_up(cdiv(R, kPackWarps), 32);
+  const int beg = warp * seg, end = min(R, beg + seg);
 
-  if (threadIdx.x == 0 && p.status) {
-    p.status[0] = 0;
-    p.status[1] = 0;
-  }
-  for (int i = threadIdx.x; i < kPackWarps * E; i += kPackThreads) s_hist[i] = 0;
+  // per-warp histograms of local experts
+  for (int i = threadIdx.x; i < kPackWarps * E; i += kPackThreads) s_whist[i] = 0;
   __syncthreads();
-
-  // pass 1: per-warp histograms.  Keys of kKeys batches are loaded before
-  // any is used, so the id and expert_map loads of a warp overlap.
-  int* my_hist = s_hist + warp * E;
-  for (int b0 = beg; b0 < end; b0 += 32 * kKeys) {
-    int keys[kKeys];
+  int* my_hist = s_whist + warp * E;
+  for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
+    int keys[kBatch];
 #pragma unroll
-    for (int i = 0; i < kKeys; ++i) {
+    for (int i = 0; i < kBatch; ++i) {
       const int r = b0 + 32 * i + lane;
       keys[i] = r < end ? pack_local_expert(p, r) : -1;
     }
 #pragma unroll
-    for (int i = 0; i < kKeys; ++i) {
-      if (b0 + 32 * i >= end) break;
-      const int key = keys[i];
-      const unsigned peers = key_peers(key, nbits);
-      if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
-      __syncwarp();
+    for (int i = 0; i < kBatch; ++i)
+      if (keys[i] >= 0) atomicAdd(&my_hist[keys[i]], 1);
+  }
+  __syncthreads();
+  // expert counts, and each warp's base among the expert's routes
+  for (int e = threadIdx.x; e < E; e += kPackThreads) {
+    int c = 0;
+    for (int w = 0; w < kPackWarps; ++w) {
+      const int h = s_whist[w * E + e];
+      s_whist[w * E + e] = c;
+      c += h;
     }
+    s_cnt[e] = c;
   }
   __syncthreads();
 
-  // pass 2: warp bases per expert, expert counts, offsets, chunk schedule
-  for (int e0 = 0; e0 < E; e0 += kPackThreads) {
-    // E <= 1024 is enforced by the host, so one iteration
-    const int e = e0 + threadIdx.x;
-    int cnt = 0;
-    if (e < E) {
-      for (int w = 0; w < kPackWarps; ++w) {
-        const int c = s_hist[w * E + e];
-        s_hist[w * E + e] = cnt;
-        cnt += c;
-      }
-    }
-    int total = 0;
-    const int off = block_exclusive_scan(cnt, s_warp, total);
-    if (e < E) {
-      s_off[e] = off;
-      p.counts[e] = cnt;
-      p.offsets[e] = off;
-    }
-    if (threadIdx.x == 0) {
-      p.offsets[E] = total;
-      s_valid = total;
-    }
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += kPackThreads) p.counts[e] = s_cnt[e];
     if (p.chunks) {
-      const int nch = e < E ? cdiv(cnt, p.chunk_rows) : 0;
-      int tot_ch = 0;
-      const int ch0 = block_exclusive_scan(nch, s_warp, tot_ch);
-      for (int c = 0; c < nch; ++c) {
-        const int rows = min(p.chunk_rows, cnt - c * p.chunk_rows);
-        p.chunks[ch0 + c] = make_int4(e, off + c * p.chunk_rows, rows, 0);
+      // chunk schedule: each expert's routes in chunks of <= chunk_rows, in
+      // expert order (computed from the counts before they become offsets)
+      int* s_nch = s_cnt + E;
+      int* s_off = s_nch + E;
+      for (int e = threadIdx.x; e < E; e += kPackThreads) {
+        s_nch[e] = cdiv(s_cnt[e], p.chunk_rows);
+        s_off[e] = s_cnt[e];
+      }
+      __syncthreads();
+      const int tot_ch = block_scan(s_nch, E, s_warp);
+      block_scan(s_off, E, s_warp);
+      for (int e = threadIdx.x; e < E; e += kPackThreads) {
+        const int cnt = s_cnt[e], off = s_off[e], ch0 = s_nch[e];
+        for (int c = 0; c * p.chunk_rows < cnt; ++c)
+          p.chunks[ch0 + c] = make_int4(e, off + c * p.chunk_rows, min(p.chunk_rows, cnt - c * p.chunk_rows), 0);
       }
       if (threadIdx.x == 0) *p.chunk_count = tot_ch;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0 && p.status) {
+      p.status[0] = 0;
+      p.status[1] = 0;
     }
   }
-  __syncthreads();
+  const int valid = block_scan(s_cnt, E, s_warp);  // s_cnt now holds the offsets
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += kPackThreads) p.offsets[e] = s_cnt[e];
+    if (threadIdx.x == 0) p.offsets[E] = valid;
+    for (int i = valid + threadIdx.x; i < p.route_cap; i += kPackThreads) p.sorted_routes[i] = -1;
+  }
 
-  // pass 3: scatter
-  for (int b0 = beg; b0 < end; b0 += 32 * kKeys) {
-    int keys[kKeys];
+  // the routes of this CTA's experts, in ascending flat index
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    int pos = s_cnt[e] + my_hist[e];
+    for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
+      int keys[kBatch];
 #pragma unroll
-    for (int i = 0; i < kKeys; ++i) {
-      const int r = b0 + 32 * i + lane;
-      keys[i] = r < end ? pack_local_expert(p, r) : -1;
-    }
-#pragma unroll
-    for (int i = 0; i < kKeys; ++i) {
-      if (b0 + 32 * i >= end) break;
-      const int r = b0 + 32 * i + lane;
-      const int key = keys[i];
-      const unsigned peers = key_peers(key, nbits);
-      if (key >= 0) {
-        const int pos = s_off[key] + my_hist[key] + __popc(peers & lt_mask);
-        p.sorted_routes[pos] = r;
+      for (int i = 0; i < kBatch; ++i) {
+        const int r = b0 + 32 * i + lane;
+        keys[i] = r < end ? pack_local_expert(p, r) : -1;
       }
-      __syncwarp();
-      if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
-      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const bool hit = keys[i] == e;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (hit) p.sorted_routes[pos + __popc(m & lt_mask)] = b0 + 32 * i + lane;
+        pos += __popc(m);
+      }
     }
   }
-  // tail of the capacity: -1
-  const int valid = s_valid;
-  for (int i = valid + threadIdx.x; i < p.route_cap; i += kPackThreads) p.sorted_routes[i] = -1;
 }
 
 size_t route_pack_smem_bytes(int num_local_experts) {
-  return (size_t)(kPackWarps + 1) * num_local_experts * sizeof(int);
+  return (size_t)(kPackWarps + 3) * num_local_experts * sizeof(int);
 }
 
-cudaError_t launch_route_pack(const RoutePackParams& p, cudaStream_t stream) {
+cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream) {
   const size_t smem = route_pack_smem_bytes(p.num_local_experts);
   static size_t configured = 0;
   if (smem > 48 * 1024 && smem > configured) {
@@ -198,7 +177,9 @@ cudaError_t launch_route_pack(const RoutePackParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  route_pack_kernel<<<1, kPackThreads, smem, stream>>>(p);
+  int grid = p.num_local_experts < 2 * num_sms ? p.num_local_experts : 2 * num_sms;
+  if (grid < 1) grid = 1;
+  route_pack_kernel<<<grid, kPackThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
