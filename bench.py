@@ -17,9 +17,11 @@ the other workloads (decode m=2, 4; small-batch m=16, 64; prefill m=2048 with
 SwiGLU and ReLU^2; MXFP4 m=512), each with its weight-stream TB/s and bf16
 TFLOP/s, "roofline" for the dominant kernel (the W4A16 GEMM, timed per launch
 with the library's timing events), "cpu_baseline" (the float64 CPU oracle on a
-bounded sample), "e2e" (the same call through the Python API with inputs
-copied from pinned host memory and the result read back every step) and the
-SM clocks sampled during the timed region.
+bounded sample), "e2e" (the same call through the Python API with host
+buffers: every step replays a CUDA graph of one host->device copy of the
+step's inputs from pinned memory, the call and the device->host copy of the
+result; wall clock around replay and synchronize) and the SM clocks sampled
+during the timed region.
 
 Replicas only: under torchrun every rank runs the same workload on its own GPU
 with no collective on the data path; rank 0 prints the max over ranks.
@@ -282,42 +284,59 @@ class Bench:
         return res
 
     def e2e_timed(self, steps, warmup):
+        """End to end through the public call with host buffers: every step
+        replays a CUDA graph of one host->device copy of the step's inputs
+        (x, ids and router weights packed in one pinned buffer), the fused
+        call, and one device->host copy of out; wall clock around replay and
+        synchronize."""
         torch = self.torch
-        pins = []
-        for d in self.draws:
-            pins.append({"x": torch.from_numpy(d["x_bits"].view(np.int16).copy()).pin_memory(),
-                         "ids": torch.from_numpy(d["ids"].copy()).pin_memory(),
-                         "wts": torch.from_numpy(d["wts"].copy()).pin_memory()})
-        out_h = torch.empty(self.m, self.wl.hidden, dtype=torch.int16).pin_memory()
-        xd = torch.empty(self.m, self.wl.hidden, dtype=torch.int16, device="cuda")
-        idsd = torch.empty(self.m, self.wl.top_k, dtype=torch.int32, device="cuda")
-        wtsd = torch.empty(self.m, self.wl.top_k, dtype=torch.float32, device="cuda")
+        m, H, k = self.m, self.wl.hidden, self.wl.top_k
+        xb, ib, wb = m * H * 2, m * k * 4, m * k * 4
+        x_off, i_off, w_off = 0, (xb + 255) // 256 * 256, 0
+        w_off = i_off + (ib + 255) // 256 * 256
+        nbytes = w_off + (wb + 255) // 256 * 256
+        dstage = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        xd = dstage[x_off:x_off + xb].view(torch.bfloat16).view(m, H)
+        idsd = dstage[i_off:i_off + ib].view(torch.int32).view(m, k)
+        wtsd = dstage[w_off:w_off + wb].view(torch.float32).view(m, k)
+        out_h = torch.empty(m, H, dtype=torch.int16).pin_memory()
         dv, s = self.dev, self.stream
+        graphs, stages = [], []
+        for d in self.draws:
+            h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+            h[x_off:x_off + xb].view(torch.int16).copy_(torch.from_numpy(d["x_bits"].view(np.int16).reshape(-1)))
+            h[i_off:i_off + ib].view(torch.int32).copy_(torch.from_numpy(d["ids"].reshape(-1)))
+            h[w_off:w_off + wb].view(torch.float32).copy_(torch.from_numpy(d["wts"].reshape(-1)))
+            stages.append(h)
 
-        def one(i):
-            p = pins[i % len(pins)]
-            with torch.cuda.stream(s):
-                xd.copy_(p["x"], non_blocking=True)
-                idsd.copy_(p["ids"], non_blocking=True)
-                wtsd.copy_(p["wts"], non_blocking=True)
-                self.b4.fused_moe(self.cfg, xd.view(torch.bfloat16), dv["w13"], dv["s13"], dv["g13"], dv["w2"],
-                                  dv["s2"], dv["g2"], idsd, wtsd, self.act, self.out, self.ws, stream=s)
+            def step(h=h):
+                dstage.copy_(h, non_blocking=True)
+                self.b4.fused_moe(self.cfg, xd, dv["w13"], dv["s13"], dv["g13"], dv["w2"], dv["s2"], dv["g2"],
+                                  idsd, wtsd, self.act, self.out, self.ws, stream=s)
                 out_h.copy_(self.out.view(torch.int16), non_blocking=True)
-            s.synchronize()
 
+            with torch.cuda.stream(s):
+                step()  # eager first: kernel attributes are set outside capture
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                step()
+            graphs.append(g)
         for i in range(warmup):
-            one(i)
+            with torch.cuda.stream(s):
+                graphs[i % len(graphs)].replay()
+            s.synchronize()
         total = 0.0
         for i in range(steps):
             with torch.cuda.stream(s):
                 self.flush_l2()
-            s.synchronize()
+            torch.cuda.synchronize()
             ta = time.perf_counter()
-            one(i)
+            with torch.cuda.stream(s):  # a graph replays on the current stream
+                graphs[i % len(graphs)].replay()
+            s.synchronize()
             total += time.perf_counter() - ta
-        h2d = self.m * self.wl.hidden * 2 + self.m * self.wl.top_k * 8
-        d2h = self.m * self.wl.hidden * 2
-        return {"seconds": total, "h2d": h2d, "d2h": d2h}
+        return {"seconds": total, "h2d": xb + ib + wb, "d2h": m * H * 2}
 
 
 # DRAM traffic of the dominant kernel(s) per call, from one ncu capture
