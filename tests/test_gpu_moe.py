@@ -37,6 +37,8 @@ CASES = [
     ("small_s", "silu", 16), ("small_s", "silu", 64),
     ("prefill_s", "silu", 200), ("prefill_s", "relu2", 200), ("prefill_s", "silu", 37),
     ("mxfp4_s", "silu", 100), ("mxfp4_s", "relu2", 9),
+    # many routes per expert: the weights-on-M grouped kernel (m * top_k >= 96 * E_l)
+    ("mxfp4_s", "silu", 300), ("tiny", "relu2", 512),
 ]
 
 

@@ -19,6 +19,8 @@
 namespace b4 {
 template <int MODE, int FMT>
 cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
+template <int MODE, int FMT>
+cudaError_t launch_gemm_wn(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream);
 cudaError_t decode_occupancy(int fmt, int* blocks_per_sm);
@@ -117,7 +119,7 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   WsLayout L{};
   L.t_cap = next_pow2(cfg->m > 0 ? cfg->m : 1);
   L.r_cap = L.t_cap * cfg->top_k;
-  L.max_chunks = L.r_cap / kChunkRows + cfg->num_local_experts + 1;
+  L.max_chunks = L.r_cap / kChunkRowsN + cfg->num_local_experts + 1;  // the smaller chunk size
   L.inter_pad = round_up(cfg->inter, kBK);
   L.wnat = fc1_natural_width(act == B4_ACT_SILU_SWIGLU ? 0 : 1, L.inter_pad);
   L.decode_ok = L.t_cap <= B4_DECODE_MAX_M;
@@ -224,7 +226,9 @@ DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, i
 }
 
 template <int MODE>
-cudaError_t launch_mode(int fmt, const GemmParams& p, int grid, bool pdl, cudaStream_t st) {
+cudaError_t launch_mode(int fmt, bool weights_on_n, const GemmParams& p, int grid, bool pdl, cudaStream_t st) {
+  if (weights_on_n)
+    return fmt == 0 ? launch_gemm_wn<MODE, 0>(p, grid, pdl, st) : launch_gemm_wn<MODE, 1>(p, grid, pdl, st);
   return fmt == 0 ? launch_gemm<MODE, 0>(p, grid, pdl, st) : launch_gemm<MODE, 1>(p, grid, pdl, st);
 }
 
@@ -463,7 +467,12 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   rp.sorted_routes = reinterpret_cast<int32_t*>(ws + L.sorted);
   rp.chunks = reinterpret_cast<int4*>(ws + L.chunks);
   rp.chunk_count = reinterpret_cast<int32_t*>(ws + L.chunk_count);
-  rp.chunk_rows = kChunkRows;
+  // Weights on the MMA's N side (256 rows per instruction, chunks of <= 128
+  // routes on M) issue half the MMAs when experts receive few routes; with
+  // ~128 routes per expert (prefill) both issue about as many, and the weights-
+  // on-M kernel keeps the weights in tensor memory and measured faster.
+  const bool weights_on_n = (long long)cfg->m * cfg->top_k < 96LL * cfg->num_local_experts;
+  rp.chunk_rows = weights_on_n ? kChunkRowsN : kChunkRowsM;
   rp.status = status;
   if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   if ((e = launch_route_pack(rp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "route pack");
@@ -491,9 +500,9 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   pp.xp = xp;
   pp.valid_count = rp.offsets + cfg->num_local_experts;
   if ((e = launch_permute_x(pp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "permute x");
-  if ((e = launch_mode<kFc1Grouped>(fmt, p1, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc1 grouped");
+  if ((e = launch_mode<kFc1Grouped>(fmt, weights_on_n, p1, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc1 grouped");
   if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-  if ((e = launch_mode<kFc2Grouped>(fmt, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");
+  if ((e = launch_mode<kFc2Grouped>(fmt, weights_on_n, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");
   if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   fp.acc = acc;
   if ((e = launch_finalize(fp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "finalize grouped");

@@ -56,4 +56,28 @@ __device__ __forceinline__ void dequant_stage(const uint4& c0, const uint4& c1, 
   }
 }
 
+// Half a stage of one row: the 16-byte chunk `half` (32 elements) -> 16
+// registers of packed bf16 pairs, scaled by the row's block scales `sc` (as
+// in dequant_stage).
+template <int FMT>
+__device__ __forceinline__ void dequant_half(const uint4& c, uint32_t sc, int half, uint32_t (&r)[16]) {
+  uint32_t s0, s1;
+  if constexpr (FMT == 0) {
+    s0 = ((((sc >> (16 * half)) & 0xFFu) << 4) + 0x5800u) * 0x10001u;
+    s1 = ((((sc >> (16 * half + 8)) & 0xFFu) << 4) + 0x5800u) * 0x10001u;
+  } else {
+    s0 = s1 = ((((sc >> (8 * half)) & 0xFFu) + 63u) << 7) * 0x10001u;
+  }
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t sq = q < 2 ? s0 : s1;
+    const uint32_t v = w[q];
+    r[4 * q + 0] = bf16x2_mul(fp4x2_lookup(v), sq);
+    r[4 * q + 1] = bf16x2_mul(fp4x2_lookup(v >> 2), sq);
+    r[4 * q + 2] = bf16x2_mul(fp4x2_lookup(v >> 16), sq);
+    r[4 * q + 3] = bf16x2_mul(fp4x2_lookup(v >> 18), sq);
+  }
+}
+
 }  // namespace b4

@@ -13,7 +13,10 @@ namespace b4 {
 constexpr int kTileRows = 128;   // weight rows per tile (tcgen05 M)
 constexpr int kBK = 64;          // K elements per pipeline stage
 constexpr int kCodeBytesPerStage = kTileRows * kBK / 2;  // 4096: [2 chunks][128 rows][16 B]
-constexpr int kChunkRows = 160;  // max routes of one expert per grouped work unit (tcgen05 N)
+// max routes of one expert per grouped work unit: tcgen05 N when the weights
+// are on M (many routes per expert), tcgen05 M when the weights are on N
+constexpr int kChunkRowsM = 160;
+constexpr int kChunkRowsN = 128;
 
 __host__ __device__ constexpr int scale_bytes_per_row(int fmt) { return fmt == 0 ? kBK / 16 : kBK / 32; }
 __host__ __device__ constexpr int scale_bytes_per_stage(int fmt) { return kTileRows * scale_bytes_per_row(fmt); }
@@ -49,8 +52,8 @@ __host__ __device__ inline TensorGeom tensor_geom(int which, int act, int hidden
 enum GemmMode : int { kFc1Grouped = 0, kFc2Grouped = 1 };
 
 struct GemmParams {
-  // TMA map of the grouped B operand: packed x rows (FC1) or h rows (FC2),
-  // box 64 columns x 32 rows, 128-byte swizzle
+  // TMA map of the grouped activation operand: packed x rows (FC1) or h rows
+  // (FC2), box 64 columns x 32 rows, 128-byte swizzle
   CUtensorMap tmap_b;
   // prepared weights of this GEMM
   const uint8_t* wcodes;

@@ -14,7 +14,9 @@
 //
 // A work unit is (expert chunk of <= 160 routes, 128-row weight tile).  The
 // tensor-core operation is swapped: the 128 weight rows are the M operand, the
-// chunk's routes are N (rounded up to 16).  Weights are dequantised from E2M1
+// chunk's routes are N (rounded up to 16).  Used when experts receive many
+// routes (prefill); moe_gemm_wn.cu puts 256 weight rows on N instead, which
+// issues half the MMAs when experts receive few routes.  Weights are dequantised from E2M1
 // codes and E4M3 / E8M0 block scales to bf16 by eight dequant warps (one
 // thread per weight row) and written straight into tensor memory with
 // tcgen05.st, where tcgen05.mma reads them as its A operand; B sits in shared
@@ -48,7 +50,7 @@ constexpr int kThreads = 512;
 constexpr int kAColsPerSlot = kBK / 2;   // 32 columns of packed bf16 pairs
 constexpr int kNW = 10;                  // weight stages in flight
 constexpr int kNB = 6;                   // B stages in flight
-constexpr int kBN = kChunkRows;          // max tcgen05 N
+constexpr int kBN = kChunkRowsM;         // max tcgen05 N
 constexpr int kBStage = kBN * kBK * 2;   // 160 rows x 128 bytes, swizzled
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = kNumA * kAColsPerSlot;  // 192: two accumulators of kBN columns follow
