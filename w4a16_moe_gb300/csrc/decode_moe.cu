@@ -34,7 +34,9 @@
 // at launch, the CTAs fill both partial buffers with a signalling-NaN bit
 // pattern that no arithmetic produces; a reader polls the values it needs
 // until none of them holds the marker (a 4-byte store is seen whole or not at
-// all).  A reader only ever waits for units earlier in unit order, each CTA
+// all).  The barrier is split: a CTA arrives as soon as its share of the fill
+// is done, and only its first partial store or read waits for the other
+// CTAs, so the first unit's weight stream and arithmetic run meanwhile.  A reader only ever waits for units earlier in unit order, each CTA
 // runs its units in order, and a cooperative launch keeps every CTA resident,
 // so every wait ends; every wait is bounded as well.  Before the barrier the
 // CTAs also clear the status word and zero the output rows of tokens without
@@ -83,7 +85,7 @@ struct DSmem {
   static constexpr size_t scales = (size_t)kDSlots * kDSlotStages * kCodeBytesPerStage;
   static constexpr size_t rows = scales + (size_t)kDSlots * kDSlotStages * kScaleStage;
   static constexpr size_t bars = rows + 2 * (size_t)kDRowBytes;
-  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 10);
+  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 12);  // 11 barrier pairs used, one spare
   static constexpr size_t desc = misc + 16;
   static constexpr size_t total = desc + 4 * 16;  // four 16-byte unit descriptors
 };
@@ -136,11 +138,36 @@ __device__ __forceinline__ bool d_unit(const DecodeParams& p, int u, DUnit& U) {
 __device__ __forceinline__ void d_trace(const DecodeParams& p, int kind, uint32_t idx) {
   if (p.trace && blockIdx.x == 0 && idx < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + idx] = clock64();
 }
-// Per-CTA global timestamps (ns), indexed by CTA: kinds 5 start, 6 first
-// weight slot consumed, 7 last FC1 partial stored, 8 compute done, 9 grid
-// barrier passed.
+// Per-CTA global timestamps (ns), indexed by CTA: kinds 5 start, 6 last FC2
+// partial stored, 7 last FC1 partial stored, 8 compute warps done, 9 output
+// warp done.
 __device__ __forceinline__ void d_trace_cta(const DecodeParams& p, int kind) {
   if (p.trace && blockIdx.x < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + blockIdx.x] = (long long)globaltimer();
+}
+
+// Split grid barrier on the word a cooperative launch provides for
+// grid.sync(), with grid.sync()'s arithmetic: every CTA adds 1 once, except
+// CTA 0, which adds 2^31 - (G - 1), so the top bit flips exactly when all G
+// CTAs have arrived and the low bits end where they started.  The add
+// releases the CTA's earlier writes; the polling load acquires every CTA's.
+__device__ __forceinline__ uint32_t grid_arrive(uint32_t* word) {
+  const uint32_t add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(word), "r"(add) : "memory");
+  return old;
+}
+__device__ __forceinline__ bool grid_wait(const uint32_t* word, uint32_t old, const Abort& ab) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    uint32_t cur;
+    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(word) : "memory");
+    if ((cur ^ old) & 0x80000000u) return true;
+    if (ab.raised()) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      ab.raise(30);
+      return false;
+    }
+  }
 }
 
 // The split partials of one element, stored contiguously with stride S
@@ -244,6 +271,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   uint64_t* epi_full = empty_b + 2;
   uint64_t* epi_empty = epi_full + 2;
   uint64_t* desc_full = epi_empty + 2;  // a unit descriptor is ready (for the weight stream)
+  uint64_t* grid_bar = desc_full + 2;   // completes once every CTA has arrived at the grid barrier
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::misc);
   DDesc* s_desc = reinterpret_cast<DDesc*>(smem + L::desc);  // [2] with the rows
   DDesc* s_edesc = s_desc + 2;                                  // [2] for the output warp
@@ -267,6 +295,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
       mbar_init(&epi_empty[i], 1);
       mbar_init(&desc_full[i], 1);
     }
+    mbar_init(grid_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -331,15 +360,24 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         for (int i = lane; i < p.hidden / 8; i += 32) o[i] = make_uint4(0, 0, 0, 0);
       }
     }
-    __threadfence();
   }
   cg::grid_group grid = cg::this_grid();
   if (!grid.is_valid()) {  // not a cooperative launch: there is no grid barrier to wait on
     if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0u, 4u);  // B4_ERR_CUDA
     return;
   }
-  grid.sync();
-  if (threadIdx.x == 0) d_trace_cta(p, 9);
+  // Every thread's fill precedes the CTA's arrival (a release at GPU scope);
+  // warp 1 then waits for the other CTAs and completes grid_bar, which the
+  // first partial store or read of each warp waits on (acquire).
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      uint32_t* word = &cg::details::get_grid_workspace()->barrier;
+      const uint32_t old = grid_arrive(word);
+      if (grid_wait(word, old, ab)) mbar_arrive(grid_bar);
+    }
+    __syncwarp();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------ weight stream
@@ -464,6 +502,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
 
   if (warp == 2 + kDComputeWarps) {
     // ------------------------------------------------------ output tiles
+    if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 42))) return;
     for (uint32_t es = 0;; ++es) {
       const uint32_t eb = es & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&epi_full[eb], (es >> 1) & 1, ab, 37))) break;
@@ -515,6 +554,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&epi_empty[eb]);
     }
+    if (lane == 0) d_trace_cta(p, 9);
     return;
   }
 
@@ -528,6 +568,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   const uint32_t sc_off = FMT == 0 ? r0 * SB + t : r0 * SB + (t >> 1);
   const int wnat = fc1_natural_width(p.act, p.inter_pad);
   uint32_t ws = 0, bs = 0, es = 0;
+  bool synced = false;  // grid_bar seen complete
   while (true) {
     const uint32_t rb = bs & 1;
     if (!__all_sync(0xffffffffu, mbar_wait(&full_b[rb], (bs >> 1) & 1, ab, 35))) break;
@@ -537,6 +578,10 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
     d_unit_shape(p, dsc.u, U);
     const uint8_t* row = s_rows + rb * kDRowBytes + t * 32;  // block t of each stage
     if (U.fc2) {
+      if (!synced) {
+        if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 43))) break;
+        synced = true;
+      }
       // h = act(sum over FC1 splits) in bf16 for this unit's K range
       uint8_t* hrow = s_rows + rb * kDRowBytes;
       switch (p.s1_stride) {
@@ -557,7 +602,6 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         ok = false;
         break;
       }
-      if (ws == 0 && tid == 0) d_trace_cta(p, 6);
       const int n = min(kDSlotStages, U.kend - s);
       const uint8_t* cs = s_codes + slot * kDSlotStages * kCodeBytesPerStage + code_off;
       const uint8_t* ss = s_scales + slot * kDSlotStages * kSS + sc_off;
@@ -581,6 +625,10 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
     if (lane == 0) mbar_arrive(&empty_b[rb]);
     ++bs;
     if (!ok) break;
+    if (!synced) {
+      if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 44))) break;
+      synced = true;
+    }
     // every column of D holds the same dot products: d[0] row r0, d[2] row r1
     const float v0 = (d[0] + e[0]) + (f[0] + h4[0]), v1 = (d[2] + e[2]) + (f[2] + h4[2]);
     if (t < 2) {
@@ -603,8 +651,8 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         if (n < p.hidden) p.q[((size_t)U.split * R + U.route) * p.hidden + n] = v;
       }
     }
+    if (tid == 0) d_trace_cta(p, U.fc2 ? 6 : 7);
     if (!U.fc2) {
-      if (tid == 0) d_trace_cta(p, 7);
     } else if (U.split == p.s2 - 1 && (U.route % p.top_k) == 31 - __clz(dsc.mask)) {
       // the token tile's last unit in unit order: the output warp sums it
       const uint32_t eb = es & 1;
