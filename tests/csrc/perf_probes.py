@@ -64,7 +64,10 @@ def mma():
     st = torch.zeros(2, dtype=torch.int32, device="cuda")
     for name, v in (("N=160, A tmem, 1 acc", 1), ("N=160, A smem, 1 acc", 2 | 1), ("N=160, A smem, 2 acc", 2 | 1 | 16),
                     ("N=256, A smem, 1 acc", 2 | 8), ("N=256, A smem, 2 acc", 2 | 8 | 16),
-                    ("N=16,  A smem, 2 acc", 2 | 16)):
+                    ("N=16,  A smem, 2 acc", 2 | 16),
+                    ("SW128 N=64,  A smem, 2 acc", 32 | 2 | 16 | 128), ("SW128 N=128, A smem, 2 acc", 32 | 2 | 16 | 64),
+                    ("SW128 N=256, A smem, 2 acc", 32 | 2 | 16 | 8), ("SW128 N=128, A tmem, 1 acc", 32 | 64),
+                    ("SW128 N=256, A tmem, 1 acc", 32 | 8)):
         for per, pc in ((4, 4), (4, 0)):
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0

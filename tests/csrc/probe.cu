@@ -326,7 +326,8 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
   const uint32_t base = tmem;
   if (tid == 0) {
     mbar_arrive(&bar_ready);  // phase 0 complete: waits on it return at once
-    const uint32_t n = (variant & 8) ? 256u : (variant & 1) ? 160u : 16u;
+    const uint32_t n = (variant & 8) ? 256u : (variant & 1) ? 160u : (variant & 64) ? 128u : (variant & 128) ? 64u : 16u;
+    const bool sw = (variant & 32) != 0;  // 128-byte-swizzled K-major operands (as in the GEMM kernels)
     const uint32_t idesc = idesc_bf16_m128(n);
     const long long t0 = clock64();
     for (int s = 0; s < 64; ++s) {
@@ -335,11 +336,13 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
         tc_fence_after();
       }
       for (int kk = 0; kk < per; ++kk) {
-        const uint64_t bdesc = smem_desc_noswizzle(smem_u32(sB) + (kk & 3) * 256, 128, 1024);
+        const uint64_t bdesc = sw ? smem_desc_sw128(smem_u32(sB) + (kk & 3) * 32)
+                                  : smem_desc_noswizzle(smem_u32(sB) + (kk & 3) * 256, 128, 1024);
         if (variant & 2) {
           // variant bit 16: MMAs alternate between two accumulators (columns 0 and 256)
           const uint32_t dcol = (variant & 16) ? ((kk & 1) ? 256u : 0u) : 192u;
-          const uint64_t adesc = smem_desc_noswizzle(smem_u32(sA) + (kk & 3) * 256, 128, 1024);
+          const uint64_t adesc = sw ? smem_desc_sw128(smem_u32(sA) + (kk & 3) * 32)
+                                    : smem_desc_noswizzle(smem_u32(sA) + (kk & 3) * 256, 128, 1024);
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(base + dcol),
