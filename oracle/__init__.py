@@ -29,6 +29,7 @@ quant     NVFP4 (e4m3_k16 + fp32 global scale) and MXFP4 (e8m0_k32)
 routing   route validity, expert_map remap, power-of-two capacity, stable
           route packing.
 moe       the fused MoE layer itself.
+linear    the dense W4A16 linear layer (one weight matrix, no routing).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_*.py`` against something other than itself (torch casts,
@@ -36,4 +37,4 @@ bit-field definitions, brute force, closed forms, a dense-MLP special case,
 exact integer arithmetic and invariances).  No function is "parity unpinned".
 """
 
-from . import formats, quant, routing, moe  # noqa: F401
+from . import formats, quant, routing, moe, linear  # noqa: F401

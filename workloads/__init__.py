@@ -16,6 +16,8 @@ decode    NVFP4, E=128, top_k=8, H=4096, I=1536, ReLU^2                1, 2, 4
 small     NVFP4, E=64, top_k=6, H=2048, I=1408, SwiGLU, 8 hot experts  16, 64
 prefill   NVFP4, E=128, top_k=8, H=4096, I=1536, SwiGLU and ReLU^2     2048
 mxfp4     MXFP4, E_g=32 -> E_l=28, top_k=4, H=2880, I=1440, SwiGLU      512
+linear    NVFP4 dense linear layer, N = K = 4096 (one weight matrix,    1, 16, 2048
+          top-1, no activation: "hidden" is K, "inter" is N)
 ========  ==========================================================  ============
 
 Recipe: x ~ N(0, 1) rounded to bf16; weights ~ N(0, 0.02) in float32 (the
@@ -96,6 +98,7 @@ WORKLOADS = {
     "decode": Workload("decode", NV, 128, 128, 8, 4096, 1536, "relu2", (1, 2, 4)),
     "small": Workload("small", NV, 64, 64, 6, 2048, 1408, "silu", (16, 64), hot_experts=8),
     "prefill": Workload("prefill", NV, 128, 128, 8, 4096, 1536, "silu", (2048,)),
+    "linear": Workload("linear", NV, 1, 1, 1, 4096, 4096, "relu2", (1, 16, 2048)),
     "mxfp4": Workload(
         "mxfp4", MX, 32, 28, 4, 2880, 1440, "silu", (512,),
         drop_globals=(3, 11, 19, 27), invalid_frac=0.01,
