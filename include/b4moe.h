@@ -247,6 +247,34 @@ b4_status b4_fused_moe_noalloc(const b4_moe_config* cfg, const uint16_t* x, cons
                                const int32_t* topk_ids, const float* topk_weights, int32_t activation,
                                uint16_t* out, uint32_t* device_status, b4_stream_t stream);
 
+/* Dense W4A16 linear layer: one FP4 weight matrix W [N, K], bf16 x, no
+ * routing and no activation -- the dense W4A16 GEMM with a capture-safe
+ * small-M dispatch and caller-owned buffers of b12x PR #136, "fix(gemm):
+ * restore capture-safe K6 small-M dispatch" (Summary), here on this
+ * library's FP4 weights: the E = 1, top-1 case of the FC1 GEMM with the
+ * activation left out.
+ *   out[t][n] = bf16( gs * sum_k x[t][k] * W[n][k] ),  t < m, n < N,
+ * W[n][k] = e2m1(code) * block scale (E4M3 per 16 or E8M0 per 32 along K),
+ * accumulated in fp32 and rounded to bf16 once.
+ *
+ * cfg           m = tokens, hidden = K, inter = N, top_k = 1,
+ *               num_global_experts = num_local_experts = 1, expert_map NULL,
+ *               format, path (AUTO: the fused small-m kernel for
+ *               m <= B4_DECODE_MAX_M, the grouped tcgen05 GEMM above that).
+ * w, s          W prepared by b4_prepare_weights(cfg, which = 0,
+ *               B4_ACT_RELU2, ...) -- the non-gated FC1 layout of one expert.
+ * gs            [1] fp32 global scale (NVFP4); NULL for MXFP4.
+ * x             [m, K] bf16; out [m, N] bf16, written in full.
+ * workspace     >= b4_linear_workspace_bytes(cfg) bytes, 256-byte aligned;
+ *               contents on entry do not matter; holds the status word.
+ * Enqueues 1 (small m: one cooperative launch) or 2-3 (route pack of the
+ * trivial routing, the GEMM, and a strided device copy when N is not a
+ * multiple of 64) operations on `stream`; no allocation, no synchronisation
+ * (capture-safe).  Shape errors: B4_ERR_INVALID_ARGUMENT before any launch. */
+size_t b4_linear_workspace_bytes(const b4_moe_config* cfg);
+b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w, const uint8_t* s,
+                    const float* gs, uint16_t* out, void* workspace, size_t workspace_bytes, b4_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* b4_status_string(int32_t status);
 

@@ -128,3 +128,31 @@ def test_status_strings(b4):
         "B4_OK", "B4_ERR_INVALID_ARGUMENT", "B4_ERR_UNSUPPORTED_DEVICE", "B4_ERR_WORKSPACE_TOO_SMALL",
         "B4_ERR_CUDA", "B4_ERR_TIMEOUT"]
     assert b4.status_string(99) == "B4_UNKNOWN_STATUS"
+
+
+def test_linear_entry_points_validate_on_the_host(b4):
+    """b4_linear takes one expert, top-1, no expert_map; sizes need no device."""
+    cfg = b4.linear_config(16, 4096, 4096)
+    assert b4.linear_workspace_bytes(cfg) > 0
+    for kw, fragment in ((dict(top_k=2), "top_k = 1"), (dict(num_local_experts=2, num_global_experts=2), "one expert"),
+                         (dict(inter=40), "inter")):
+        bad = b4.linear_config(16, 4096, 4096)
+        for k_, v in kw.items():
+            setattr(bad, k_, v)
+        with pytest.raises(b4.B4Error) as ei:
+            b4.linear_workspace_bytes(bad)
+        assert fragment in str(ei.value)
+    lib = b4.raw_lib()
+    c = cfg._c()
+    assert lib.b4_linear(ctypes.byref(c), None, None, None, None, None, None, 0, None) == b4.B4_ERR_INVALID_ARGUMENT
+    assert "null" in b4.last_error()
+    c0 = b4.linear_config(0, 4096, 4096)._c()  # m = 0: a no-op
+    assert lib.b4_linear(ctypes.byref(c0), None, None, None, None, None, None, 0, None) == b4.B4_OK
+    # MXFP4 takes no global scale, NVFP4 needs one (checked before any pointer is used)
+    one = ctypes.c_float(1.0)
+    cmx = b4.linear_config(2, 256, 256, format=b4.MXFP4)._c()
+    buf = ctypes.create_string_buffer(1 << 12)
+    p = ctypes.addressof(buf)
+    assert lib.b4_linear(ctypes.byref(cmx), p, p, p, ctypes.addressof(one), p, p, 1 << 12,
+                         None) == b4.B4_ERR_INVALID_ARGUMENT
+    assert "global scale" in b4.last_error()

@@ -80,6 +80,8 @@ def _load():
         "b4_route_pack": (I32, [CP, P, P, P, P, P]),
         "b4_fused_moe": (I32, [CP, P, P, P, P, P, P, P, P, P, I32, P, P, S, P]),
         "b4_fused_moe_noalloc": (I32, [CP, P, P, P, P, P, P, P, P, P, I32, P, P, P]),
+        "b4_linear_workspace_bytes": (S, [CP]),
+        "b4_linear": (I32, [CP, P, P, P, P, P, P, S, P]),
         "b4_check_status": (I32, [P, P]),
         "b4_set_timing_events": (I32, [ctypes.POINTER(P), I32]),
         "b4_set_trace": (I32, [P, S]),
@@ -102,6 +104,8 @@ EXPORTED = (
     "b4_route_pack",
     "b4_fused_moe",
     "b4_fused_moe_noalloc",
+    "b4_linear_workspace_bytes",
+    "b4_linear",
     "b4_check_status",
     "b4_set_timing_events",
     "b4_set_trace",
@@ -252,6 +256,41 @@ def fused_moe_noalloc(cfg: MoEConfig, x, w13, s13, gs13, w2, s2, gs2, topk_ids, 
     _check(_lib.b4_fused_moe_noalloc(ctypes.byref(c), _ptr(x), _ptr(w13), _ptr(s13), _ptr(gs13), _ptr(w2), _ptr(s2),
                                      _ptr(gs2), _ptr(topk_ids), _ptr(topk_weights), int(activation), _ptr(out),
                                      _ptr(device_status), _stream(stream)))
+
+
+def linear_config(m: int, n: int, k: int, format: int = NVFP4, path: int = PATH_AUTO) -> MoEConfig:
+    """Shape of a dense W4A16 linear call: out [m, n] = x [m, k] . W[n, k]^T
+    (one expert, top-1, inter = n, hidden = k; ``b4_linear`` in b4moe.h)."""
+    return MoEConfig(m=m, top_k=1, num_global_experts=1, num_local_experts=1, hidden=k, inter=n, format=format,
+                     path=path)
+
+
+def linear_workspace_bytes(cfg: MoEConfig) -> int:
+    c = cfg._c()
+    n = _lib.b4_linear_workspace_bytes(ctypes.byref(c))
+    if n == 0:
+        raise B4Error(B4_ERR_INVALID_ARGUMENT, last_error())
+    return int(n)
+
+
+def prepare_linear_weights(cfg: MoEConfig, src_codes, src_scales, stream=None):
+    """W [n, k] (codes [n, k/2], scales [n, k/g]; a leading expert axis of 1 is
+    optional) -> the serving layout ``linear`` reads (the non-gated FC1 layout)."""
+    return prepare_weights(cfg, 0, RELU2, src_codes, src_scales, stream=stream)
+
+
+def linear(cfg: MoEConfig, x, w, s, gs, out, workspace, stream=None):
+    """Enqueue the dense W4A16 linear layer; ``out`` [m, n] bf16 is written in full."""
+    _need(x, torch.bfloat16, "x")
+    _need(out, torch.bfloat16, "out")
+    _need(workspace, torch.uint8, "workspace")
+    _need(w, torch.uint8, "w")
+    _need(s, torch.uint8, "s")
+    if gs is not None:
+        _need(gs, torch.float32, "gs")
+    c = cfg._c()
+    _check(_lib.b4_linear(ctypes.byref(c), _ptr(x), _ptr(w), _ptr(s), _ptr(gs), _ptr(out), _ptr(workspace),
+                          workspace.numel(), _stream(stream)))
 
 
 def fused_moe_raw(cfg: MoEConfig, ptrs: dict, activation: int, workspace_ptr: int, workspace_bytes_: int,

@@ -510,6 +510,166 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   return B4_OK;
 }
 
+// ------------------------------------------------------------ dense linear
+namespace {
+b4_status check_linear(const b4_moe_config* cfg) {
+  b4_status st = check_config(cfg, B4_ACT_RELU2);
+  if (st != B4_OK) return st;
+  if (cfg->top_k != 1 || cfg->num_local_experts != 1 || cfg->num_global_experts != 1 || cfg->expert_map)
+    return fail(B4_ERR_INVALID_ARGUMENT, "the linear layer takes top_k = 1, one expert and no expert_map");
+  return B4_OK;
+}
+}  // namespace
+
+size_t b4_linear_workspace_bytes(const b4_moe_config* cfg) {
+  if (check_linear(cfg) != B4_OK) return 0;
+  return ws_layout(cfg, B4_ACT_RELU2).total;
+}
+
+b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w, const uint8_t* sc,
+                    const float* gs, uint16_t* out, void* workspace, size_t workspace_bytes, b4_stream_t stream) {
+  b4_status st = check_linear(cfg);
+  if (st != B4_OK) return st;
+  if (cfg->m == 0) return B4_OK;  // nothing to compute, nothing launched
+  if (!x || !w || !sc || !out || !workspace) return fail(B4_ERR_INVALID_ARGUMENT, "null pointer argument");
+  const bool nv = cfg->format == B4_NVFP4_E4M3_K16;
+  if (nv && !gs) return fail(B4_ERR_INVALID_ARGUMENT, "NVFP4 needs gs");
+  if (!nv && gs) return fail(B4_ERR_INVALID_ARGUMENT, "MXFP4 takes no global scale (pass NULL)");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(w, 16) || !aligned(sc, 16))
+    return fail(B4_ERR_INVALID_ARGUMENT, "x, out and the weight buffers must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(B4_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if (gs && !aligned(gs, 4)) return fail(B4_ERR_INVALID_ARGUMENT, "misaligned gs");
+  const WsLayout L = ws_layout(cfg, B4_ACT_RELU2);
+  if (workspace_bytes < L.total)
+    return fail(B4_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, L.total);
+  DevInfo dev;
+  if ((st = device_info(dev)) != B4_OK) return st;
+
+  const int fmt = cfg->format;
+  const int m = cfg->m, N = cfg->inter, K = cfg->hidden;
+  bool small = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && m <= B4_DECODE_MAX_M);
+  if (small && !L.decode_ok) small = false;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const TensorGeom g1 = tensor_geom(0, 1, K, N);
+  cudaError_t e;
+
+  if (small) {
+    // The fused small-m kernel: K-split GEMV units, then one output unit per
+    // (token, 128 columns) that sums the split partials into out.
+    int occ = 0;
+    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
+    // K splits: about two GEMV units per CTA, at least 8 stages each, at
+    // most the partial buffer's split count (summing up to 8 partials per
+    // output is cheap here: no activation row is built from them).
+    const int cap = occ * dev.sms;
+    const long long base = (long long)m * g1.n_tiles;
+    int s1 = (int)((2LL * cap + base - 1) / base);
+    const int most = g1.k_stages / 8 > 1 ? g1.k_stages / 8 : 1;
+    if (s1 > most) s1 = most;
+    if (s1 > L.dec_splits) s1 = L.dec_splits;
+    const int least = (g1.k_stages + 127) / 128;
+    if (s1 < least) s1 = least;
+    const DecodePlan plan{s1, 1, 0};
+    DecodeParams dp{};
+    dp.w1_codes = w;
+    dp.w1_scales = sc;
+    dp.gs1 = gs;
+    dp.n_tiles1 = g1.n_tiles;
+    dp.k_stages1 = g1.k_stages;
+    dp.n_tiles2 = g1.n_tiles;
+    dp.k_stages2 = 1;
+    dp.m = m;
+    dp.top_k = 1;
+    dp.num_global_experts = 1;
+    dp.num_local_experts = 1;
+    dp.hidden = K;
+    dp.inter_pad = L.inter_pad;
+    dp.act = 1;  // the non-gated FC1 partial layout; no activation is applied
+    dp.linear = 1;
+    dp.n_out = N;
+    dp.x = x;
+    dp.out = out;
+    dp.s1 = plan.s1;
+    dp.s2 = 1;
+    dp.s1_stride = 1;
+    while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
+    dp.units1 = m * g1.n_tiles * plan.s1;
+    dp.units2 = m * g1.n_tiles;
+    dp.p = reinterpret_cast<float*>(ws + L.p);
+    dp.p_floats = (size_t)m * L.inter_pad * dp.s1_stride;
+    dp.ticket = reinterpret_cast<int*>(ws + L.status + 64);
+    dp.status = status;
+    dp.trace = g_trace;
+    const long long U = (long long)dp.units1 + dp.units2;
+    const int grid = (int)(U < cap ? U : cap);
+    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    if ((e = launch_decode(dp, fmt, grid, s)) != cudaSuccess) return cuda_fail(e, "linear (fused small-m)");
+    if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    return B4_OK;
+  }
+
+  // The grouped tcgen05 GEMM over one "expert" whose routes are the tokens in
+  // order: the route pack of the trivial routing writes the chunk schedule,
+  // the GEMM reads x rows directly (slot i is token i) and its epilogue stores
+  // the scaled accumulator as bf16.
+  RoutePackParams rp{};
+  rp.topk_ids = nullptr;
+  rp.m = m;
+  rp.top_k = 1;
+  rp.num_global_experts = 1;
+  rp.num_local_experts = 1;
+  rp.route_cap = L.r_cap;
+  rp.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  rp.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  rp.sorted_routes = reinterpret_cast<int32_t*>(ws + L.sorted);
+  rp.chunks = reinterpret_cast<int4*>(ws + L.chunks);
+  rp.chunk_count = reinterpret_cast<int32_t*>(ws + L.chunk_count);
+  const bool weights_on_n = m < 96;  // the fused-MoE rule m * top_k < 96 * E_l with E_l = top_k = 1
+  rp.chunk_rows = weights_on_n ? kChunkRowsN : kChunkRowsM;
+  rp.status = status;
+  GemmParams p1{};
+  p1.m = m;
+  p1.top_k = 1;
+  p1.num_global_experts = 1;
+  p1.num_local_experts = 1;
+  p1.hidden = K;
+  p1.inter = N;
+  p1.inter_pad = L.inter_pad;
+  p1.act = 2;
+  p1.x = x;
+  p1.status = status;
+  p1.max_chunks = L.max_chunks;
+  p1.trace = g_trace;
+  p1.wcodes = w;
+  p1.wscales = sc;
+  p1.gs = gs;
+  p1.n_tiles = g1.n_tiles;
+  p1.k_stages = g1.k_stages;
+  p1.sorted_routes = rp.sorted_routes;
+  p1.chunk_count = rp.chunk_count;
+  p1.chunks = rp.chunks;
+  if (!make_tmap_bf16_2d(&p1.tmap_b, x, (uint64_t)m, (uint64_t)K, 32))
+    return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the x map");
+  const bool direct = N == L.inter_pad;  // rows of h are rows of out
+  uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.h);
+  p1.h_out = direct ? out : hbuf;
+  p1.pdl_wait_first = 1;
+  if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+  if ((e = launch_route_pack(rp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "route pack");
+  if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+  if ((e = launch_mode<kFc1Grouped>(fmt, weights_on_n, p1, dev.sms, true, s)) != cudaSuccess)
+    return cuda_fail(e, "linear (grouped)");
+  if (!direct &&
+      (e = cudaMemcpy2DAsync(out, (size_t)N * 2, hbuf, (size_t)L.inter_pad * 2, (size_t)N * 2, (size_t)m,
+                             cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "linear: copy to out");
+  if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+  return B4_OK;
+}
+
 b4_status b4_set_trace(void* device_buffer, size_t bytes) {
   if (device_buffer && bytes < 10 * kTraceLen * sizeof(long long))
     return fail(B4_ERR_INVALID_ARGUMENT, "trace buffer needs %zu bytes", 10 * kTraceLen * sizeof(long long));

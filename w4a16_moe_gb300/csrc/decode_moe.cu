@@ -42,6 +42,11 @@
 // CTAs also clear the status word and zero the output rows of tokens without
 // a valid route.
 //
+// The dense W4A16 linear layer (one weight matrix, top-1, no activation, no
+// FC2) runs in the same kernel: its FC1 units are the layer's K-split GEMV
+// units, and each "FC2" unit is an output tile (token, 128 columns) that sums
+// the FC1 split partials straight into out; those units stream no weights.
+//
 // Why warp-level MMAs and not tcgen05 here: one tcgen05.mma covers 128 x 16
 // weights and costs ~165 cycles to issue whatever its N, which caps a GEMV
 // near 2 TB/s; m16n8k16 issues in a few cycles, leaving the dequantiser's
@@ -91,6 +96,7 @@ struct DSmem {
 };
 
 __device__ __forceinline__ int d_local_expert(const DecodeParams& p, int route) {
+  if (!p.topk_ids) return 0;  // dense linear layer: one expert, every route valid
   const int id = __ldg(p.topk_ids + route);
   if (id < 0 || id >= p.num_global_experts) return -1;
   const int l = p.expert_map ? __ldg(p.expert_map + id) : id;
@@ -253,6 +259,34 @@ __device__ __forceinline__ bool build_h(const DecodeParams& p, const DUnit& U, u
   return ok;
 }
 
+// Dense linear layer: out[token][n] = bf16(sum of the FC1 split partials of
+// column n, ascending split order) for the unit's 128 columns, one compute
+// thread per column; a partial still holding the not-written marker is read
+// again.  Returns false on timeout (the abort flag is raised).
+template <int S>
+__device__ __forceinline__ bool linear_out(const DecodeParams& p, const DUnit& U, int tid, const Abort& ab) {
+  const int n = U.tile * kTileRows + tid;
+  if (tid >= kTileRows || n >= p.n_out) return true;
+  const float* src = p.p + ((size_t)U.route * p.inter_pad + n) * S;
+  const unsigned long long t0 = globaltimer();
+  float v[S];
+  while (true) {
+    load_splits<S>(v, src);
+    bool ready = true;
+#pragma unroll
+    for (int sp = 0; sp < S; ++sp)
+      if (sp < p.s1 && __float_as_uint(v[sp]) == kNotWritten) ready = false;
+    if (ready) break;
+    if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
+      if (!ab.raised()) ab.raise(45);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  p.out[(size_t)(U.route / p.top_k) * p.n_out + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum_splits<S>(v, p.s1)));
+  return true;
+}
+
 // ------------------------------------------------------------------ fused
 template <int FMT>
 __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_constant__ DecodeParams p) {
@@ -307,7 +341,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
   uint32_t pre_slots = 0;
   bool pre_row = false;
-  if (warp == 0 && lane == 0 && u0_ok) {
+  if (warp == 0 && lane == 0 && u0_ok && !(U0.fc2 && p.linear)) {
     const size_t tile_id = (size_t)U0.expert * (U0.fc2 ? p.n_tiles2 : p.n_tiles1) + U0.tile;
     const int ks = U0.fc2 ? p.k_stages2 : p.k_stages1;
     const uint8_t* gc = (U0.fc2 ? p.w2_codes : p.w1_codes) + tile_id * ks * kCodeBytesPerStage;
@@ -391,6 +425,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         if (u < 0) break;
         DUnit U;
         d_unit_shape(p, u, U);
+        if (U.fc2 && p.linear) continue;  // an output unit of the dense linear layer streams no weights
         U.expert = s_desc[rb].expert;
         const size_t tile_id = (size_t)U.expert * (U.fc2 ? p.n_tiles2 : p.n_tiles1) + U.tile;
         const int ks = U.fc2 ? p.k_stages2 : p.k_stages1;
@@ -469,6 +504,15 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
           dsc->expert = U.expert;
           mbar_arrive(&desc_full[rb]);  // the weight stream needs only the unit
           dsc->scale = (p.gs1 ? __ldg(p.gs1 + U.expert) : 1.0f) * kDTwo63;
+          mbar_arrive(&full_b[rb]);
+        }
+      } else if (p.linear) {
+        if (lane == 0) {
+          dsc->u = u;
+          dsc->expert = U.expert;
+          mbar_arrive(&desc_full[rb]);
+          dsc->scale = 1.0f;
+          dsc->mask = 1u;
           mbar_arrive(&full_b[rb]);
         }
       } else {
@@ -576,6 +620,24 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
     if (dsc.u < 0) break;
     DUnit U;
     d_unit_shape(p, dsc.u, U);
+    if (U.fc2 && p.linear) {
+      // dense linear layer: this unit writes 128 columns of out
+      if (!synced) {
+        if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 46))) break;
+        synced = true;
+      }
+      switch (p.s1_stride) {
+        case 1: linear_out<1>(p, U, tid, ab); break;
+        case 2: linear_out<2>(p, U, tid, ab); break;
+        case 4: linear_out<4>(p, U, tid, ab); break;
+        default: linear_out<8>(p, U, tid, ab); break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_b[rb]);
+      ++bs;
+      if (ab.raised()) break;
+      continue;
+    }
     const uint8_t* row = s_rows + rb * kDRowBytes + t * 32;  // block t of each stage
     if (U.fc2) {
       if (!synced) {

@@ -31,7 +31,8 @@ struct TensorGeom {
   int k_stages;    // 64-element stages
 };
 
-// which: 0 = W13/W1, 1 = W2.  act: 0 = SwiGLU, 1 = ReLU^2.
+// which: 0 = W13/W1, 1 = W2.  act: 0 = SwiGLU (gated W13), otherwise a
+// non-gated W1 (1 = ReLU^2, 2 = none: the dense linear layer).
 __host__ __device__ inline TensorGeom tensor_geom(int which, int act, int hidden, int inter) {
   TensorGeom g;
   const int inter_pad = round_up(inter, kBK);
@@ -62,7 +63,7 @@ struct GemmParams {
   int n_tiles, k_stages;
   // layer shape
   int m, top_k, num_global_experts, num_local_experts, hidden, inter, inter_pad;
-  int act;              // 0 SwiGLU, 1 ReLU^2
+  int act;              // 0 SwiGLU, 1 ReLU^2, 2 none (dense linear: h = the scaled accumulator)
   // routing inputs
   const int32_t* topk_ids;
   const float* topk_weights;
@@ -103,7 +104,12 @@ struct DecodeParams {
   int n_tiles1, k_stages1, n_tiles2, k_stages2;
   int m, top_k, num_global_experts, num_local_experts, hidden, inter_pad;
   int act;                   // 0 SwiGLU, 1 ReLU^2
-  const int32_t* topk_ids;
+  // Dense linear layer (E = 1, top-1, no activation, no FC2): the FC2 units
+  // become output units (route, 128-column tile of N) that sum the FC1 split
+  // partials into out [m, n_out] bf16; topk_ids, topk_weights, w2 and q are
+  // unused.
+  int linear, n_out;
+  const int32_t* topk_ids;   // [m, top_k], or null: every route goes to local expert 0
   const float* topk_weights;
   const int32_t* expert_map;  // or null
   const uint16_t* x;         // [m, H] bf16
@@ -120,7 +126,7 @@ struct DecodeParams {
 };
 
 struct RoutePackParams {
-  const int32_t* topk_ids;
+  const int32_t* topk_ids;   // or null: every route goes to local expert 0 (the dense linear layer)
   const int32_t* expert_map;
   int m, top_k, num_global_experts, num_local_experts;
   int route_cap;

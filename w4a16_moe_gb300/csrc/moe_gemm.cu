@@ -7,7 +7,8 @@
 //
 //   FC1  B = x rows of the routes of one expert chunk, copied into
 //        packed-route order by permute_x_kernel; the epilogue applies
-//        SiLU-SwiGLU or ReLU^2 and stores bf16 h in the same order.
+//        SiLU-SwiGLU or ReLU^2 (none for the dense linear layer, whose
+//        B rows are x itself) and stores bf16 h in the same order.
 //   FC2  B = h rows of the chunk; the epilogue multiplies by gs2 and the
 //        router weight and adds into an fp32 [tokens, H] accumulator (the
 //        top-k sum), which finalize_grouped_kernel rounds to bf16.
@@ -393,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               const int col = c0 + j;
               const float a = __uint_as_float(v[j]) * gsv;
               if (col < U.rows && i < p.inter_pad)
-                p.h_out[(size_t)(U.slot0 + col) * p.inter_pad + i] = float_to_bf16_bits(a > 0.f ? a * a : 0.f);
+                p.h_out[(size_t)(U.slot0 + col) * p.inter_pad + i] =
+                    float_to_bf16_bits(p.act == 2 ? a : (a > 0.f ? a * a : 0.f));
             }
           }
         } else {

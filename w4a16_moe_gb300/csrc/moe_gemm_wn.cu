@@ -9,7 +9,8 @@
 //
 //   FC1  activations = x rows of the routes of one expert chunk, copied into
 //        packed-route order by permute_x_kernel; the epilogue applies
-//        SiLU-SwiGLU or ReLU^2 and stores bf16 h in the same order.
+//        SiLU-SwiGLU or ReLU^2 (none for the dense linear layer) and
+//        stores bf16 h in the same order.
 //   FC2  activations = h rows of the chunk; the epilogue multiplies by gs2 and
 //        the router weight and adds into an fp32 [tokens, H] accumulator (the
 //        top-k sum), which finalize_grouped_kernel rounds to bf16.
@@ -410,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                   const float a0 = __uint_as_float(v[2 * j]) * gsv, a1 = __uint_as_float(v[2 * j + 1]) * gsv;
-                  o[j] = pack_bf16x2(a0 > 0.f ? a0 * a0 : 0.f, a1 > 0.f ? a1 * a1 : 0.f);
+                  o[j] = p.act == 2 ? pack_bf16x2(a0, a1)
+                                    : pack_bf16x2(a0 > 0.f ? a0 * a0 : 0.f, a1 > 0.f ? a1 * a1 : 0.f);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(p.h_out + (size_t)(U.slot0 + er) * p.inter_pad + i0);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -29,6 +29,7 @@ constexpr int kPackWarps = kPackThreads / 32;
 constexpr int kBatch = 8;  // 32-route groups whose keys a warp loads before using any
 
 __device__ __forceinline__ int pack_local_expert(const RoutePackParams& p, int r) {
+  if (!p.topk_ids) return 0;
   const int id = __ldg(p.topk_ids + r);
   if (id < 0 || id >= p.num_global_experts) return -1;
   const int l = p.expert_map ? __ldg(p.expert_map + id) : id;
