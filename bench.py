@@ -14,7 +14,8 @@ resident in HBM.
 
 Besides the headline it reports, in "secondary", the same measurement for
 the other workloads (decode m=2, 4; small-batch m=16, 64; prefill m=2048 with
-SwiGLU and ReLU^2; MXFP4 m=512), each with its weight-stream TB/s and bf16
+SwiGLU and ReLU^2; MXFP4 m=512; the dense W4A16 linear layer b4_linear,
+N = K = 4096, m = 1, 16, 2048), each with its weight-stream TB/s and bf16
 TFLOP/s, "roofline" for the dominant kernel (the W4A16 GEMM, timed per launch
 with the library's timing events), "cpu_baseline" (the float64 CPU oracle on a
 bounded sample), "e2e" (the same call through the Python API with host
@@ -46,7 +47,8 @@ sys.path.insert(0, ROOT)
 METRIC = "fused W4A16 MoE µs/call; weight-stream TB/s (m≤16), bf16 TFLOPS (m=2048)"
 HEADLINE = ("decode", "relu2", 1)
 SECONDARY = [("decode", "relu2", 2), ("decode", "relu2", 4), ("small", "silu", 16), ("small", "silu", 64),
-             ("prefill", "silu", 2048), ("prefill", "relu2", 2048), ("mxfp4", "silu", 512)]
+             ("prefill", "silu", 2048), ("prefill", "relu2", 2048), ("mxfp4", "silu", 512),
+             ("linear", "none", 1), ("linear", "none", 16), ("linear", "none", 2048)]
 L2_FLUSH_BYTES = 512 << 20
 DRAWS = 8  # independent routing / activation draws cycled through the steps
 
@@ -58,6 +60,9 @@ def torch_int32():
 
 
 def describe(wl, m):
+    if wl.name == "linear":
+        return (f"linear {'NVFP4' if wl.fmt.startswith('nvfp4') else 'MXFP4'} dense W4A16 linear layer: "
+                f"N={wl.inter} K={wl.hidden} m={m}")
     return (f"{wl.name} {'NVFP4' if wl.fmt.startswith('nvfp4') else 'MXFP4'} MoE: E_g={wl.num_global_experts} "
             f"E_l={wl.num_local_experts} top_k={wl.top_k} H={wl.hidden} I={wl.inter} "
             f"{'SiLU-SwiGLU' if wl.act == 'silu' else 'ReLU^2'} m={m}")
@@ -353,6 +358,50 @@ NCU_TRAFFIC = {  # (path, workload, m): (source hash, bytes per call of the GEMM
 }
 
 
+class LinearBench(Bench):
+    """The dense W4A16 linear layer (b4_linear) on the same timing harness:
+    a step is one call, out [m, N] = x [m, K] . W^T."""
+
+    def __init__(self, wl, m, seed=7):
+        import torch
+
+        import w4a16_moe_gb300 as b4
+        import workloads as W
+
+        self.torch, self.b4, self.W = torch, b4, W
+        self.wl, self.m = wl, m
+        n, k = wl.inter, wl.hidden
+        self.cfg = b4.linear_config(m, n, k, format=b4.FORMATS[wl.fmt])
+        c, s, g = W.random_codes(wl, seed, 0)
+        wc, ws = b4.prepare_linear_weights(self.cfg, torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda())
+        self.dev = {"w": wc, "s": ws, "g": None if g is None else torch.from_numpy(g).cuda()}
+        wbytes = n * k // 2 + n * k // wl.group + (4 if g is not None else 0)
+        acct = {"bytes": wbytes + m * k * 2 + m * n * 2, "weight_bytes": wbytes, "fc1_bytes": wbytes + m * k * 2,
+                "fc2_bytes": m * n * 2, "flops": 2.0 * m * n * k, "experts_hit": 1, "routes": m}
+        self.draws = []
+        for d in range(DRAWS):
+            xb, x = W.activations(wl, m, seed=100 + d)
+            self.draws.append({"x_bits": xb, "x": x, "acct": acct,
+                               "xd": torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)})
+        self.ws = torch.empty(b4.linear_workspace_bytes(self.cfg), dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.flush_sink = torch.empty(1, dtype=torch.int32, device="cuda")
+        self.stream = torch.cuda.Stream()
+        # the fused small-m kernel (one launch) for m <= 4; above, the grouped
+        # GEMM: with fewer (chunk, tile pair) units than SMs it splits K and adds
+        # fp32 partials (events: memset + route pack, GEMM, rounding pass),
+        # otherwise it stores bf16 (route pack, GEMM)
+        self.decode = m <= 4
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        k_split = m < 96 and -(-m // 128) * ((-(-n // 128) + 1) // 2) < sms
+        self.n_kernels = 1 if self.decode else (3 if k_split else 2)
+
+    def call(self, d, stream=None):
+        dv = self.dev
+        self.b4.linear(self.cfg, d["xd"], dv["w"], dv["s"], dv["g"], self.out, self.ws, stream=stream)
+
+
 def kernel_source_hash(path):
     import hashlib
 
@@ -378,8 +427,9 @@ def summarize(b: Bench, res, peaks):
     acct_bytes = statistics.mean(a["bytes"] for a in res["accts"])
     acct_flops = statistics.mean(a["flops"] for a in res["accts"])
     wbytes = statistics.mean(a["weight_bytes"] for a in res["accts"])
-    # GEMM kernels: the fused decode kernel (0); grouped FC1 (1) and FC2 (2)
-    gi = (0,) if b.decode else (1, 2)
+    # GEMM kernels: the fused decode kernel (0); grouped FC1 (1) and FC2 (2);
+    # the linear layer's grouped GEMM (1)
+    gi = (0,) if b.decode else ((1,) if isinstance(b, LinearBench) else (1, 2))
     kern = res["kern"]
     gemm_ms = [sum(k[j] for j in gi) for k in kern]
     gemm_s = 1e-3 * statistics.mean(gemm_ms)
@@ -483,6 +533,8 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
+    if args.workload.split(":")[0] == "linear":
+        ap.error("the linear layer is reported in the secondary lines, not as the headline")
 
     import torch
 
@@ -538,7 +590,7 @@ def main():
     if not args.no_secondary:
         sec = []
         for nm, ac, mm in SECONDARY:
-            bb = Bench(W.WORKLOADS[nm].with_act(ac), mm)
+            bb = LinearBench(W.WORKLOADS[nm], mm) if nm == "linear" else Bench(W.WORKLOADS[nm].with_act(ac), mm)
             r = bb.run(min(args.steps, 10), 3, barrier)
             sec.append(summarize(bb, r, peaks))
             del bb

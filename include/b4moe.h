@@ -259,18 +259,23 @@ b4_status b4_fused_moe_noalloc(const b4_moe_config* cfg, const uint16_t* x, cons
  *
  * cfg           m = tokens, hidden = K, inter = N, top_k = 1,
  *               num_global_experts = num_local_experts = 1, expert_map NULL,
- *               format, path (AUTO: the fused small-m kernel for
- *               m <= B4_DECODE_MAX_M, the grouped tcgen05 GEMM above that).
+ *               format, path (AUTO: the fused small-m kernel for m <= 4,
+ *               the grouped tcgen05 GEMM above that; DECODE is accepted
+ *               for m <= B4_DECODE_MAX_M).
  * w, s          W prepared by b4_prepare_weights(cfg, which = 0,
  *               B4_ACT_RELU2, ...) -- the non-gated FC1 layout of one expert.
  * gs            [1] fp32 global scale (NVFP4); NULL for MXFP4.
  * x             [m, K] bf16; out [m, N] bf16, written in full.
  * workspace     >= b4_linear_workspace_bytes(cfg) bytes, 256-byte aligned;
  *               contents on entry do not matter; holds the status word.
- * Enqueues 1 (small m: one cooperative launch) or 2-3 (route pack of the
- * trivial routing, the GEMM, and a strided device copy when N is not a
- * multiple of 64) operations on `stream`; no allocation, no synchronisation
- * (capture-safe).  Shape errors: B4_ERR_INVALID_ARGUMENT before any launch. */
+ * Enqueues on `stream`: 1 cooperative launch (small m); or, when the GEMM
+ * has fewer (token chunk, 256-row tile pair) units than SMs, 4 operations
+ * (a memset of an fp32 accumulator, the route pack of the trivial routing,
+ * the GEMM with K split across units adding fp32 partials, and a rounding
+ * pass); otherwise 2-3 (route pack, the GEMM storing bf16, and a strided
+ * device copy when N is not a multiple of 64).  No allocation, no
+ * synchronisation (capture-safe).  Shape errors: B4_ERR_INVALID_ARGUMENT
+ * before any launch. */
 size_t b4_linear_workspace_bytes(const b4_moe_config* cfg);
 b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w, const uint8_t* s,
                     const float* gs, uint16_t* out, void* workspace, size_t workspace_bytes, b4_stream_t stream);

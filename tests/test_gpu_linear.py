@@ -1,10 +1,11 @@
 """GPU parity of the dense W4A16 linear layer (b4_linear) with the oracle.
 
-Both execution paths: the fused small-m kernel (K-split GEMV units, then
-output units that sum the split partials) for m <= 64, and the grouped
-tcgen05 GEMM above that (weights on N below m = 96, weights on M above), the
-latter including N not a multiple of 64 (a strided copy into out).  Also:
-capture in a CUDA graph, and both paths agreeing with each other.
+Every execution path: the fused small-m kernel (K-split GEMV units, then
+output units that sum the split partials) for m <= 4 (or forced up to 64);
+the weights-on-N tcgen05 GEMM with K split across units and fp32 partial sums
+(few units: small m, moderate N); the weights-on-M GEMM storing bf16 (m >=
+96), including N not a multiple of 64 (a strided copy into out).  Also:
+capture in a CUDA graph, and the paths agreeing with each other.
 """
 
 import numpy as np
@@ -24,6 +25,8 @@ CASES = [
     ("nv_m3", NV, 3, 640, 1024, "auto", "quantized"),
     ("nv_m16", NV, 16, 384, 2048, "auto", "quantized"),
     ("nv_m64", NV, 64, 256, 512, "auto", "quantized"),
+    ("nv_m40_decode", NV, 40, 256, 1024, "decode", "quantized"),
+    ("nv_m16_full", NV, 16, 4096, 4096, "auto", "random"),
     ("nv_m65_wn", NV, 65, 512, 256, "auto", "quantized"),
     ("nv_m300_wm", NV, 300, 1024, 512, "auto", "quantized"),
     ("nv_m7_grouped", NV, 7, 256, 512, "grouped", "quantized"),

@@ -519,11 +519,19 @@ b4_status check_linear(const b4_moe_config* cfg) {
     return fail(B4_ERR_INVALID_ARGUMENT, "the linear layer takes top_k = 1, one expert and no expert_map");
   return B4_OK;
 }
+
+// The linear layer's workspace: the fused layer's pieces with the fp32
+// accumulator rows widened to max(K, N) (a K-split GEMM adds into [m, N]).
+WsLayout linear_layout(const b4_moe_config* cfg) {
+  b4_moe_config c = *cfg;
+  if (c.inter > c.hidden) c.hidden = c.inter;
+  return ws_layout(&c, B4_ACT_RELU2);
+}
 }  // namespace
 
 size_t b4_linear_workspace_bytes(const b4_moe_config* cfg) {
   if (check_linear(cfg) != B4_OK) return 0;
-  return ws_layout(cfg, B4_ACT_RELU2).total;
+  return linear_layout(cfg).total;
 }
 
 b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w, const uint8_t* sc,
@@ -539,7 +547,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
     return fail(B4_ERR_INVALID_ARGUMENT, "x, out and the weight buffers must be 16-byte aligned");
   if (!aligned(workspace, 256)) return fail(B4_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
   if (gs && !aligned(gs, 4)) return fail(B4_ERR_INVALID_ARGUMENT, "misaligned gs");
-  const WsLayout L = ws_layout(cfg, B4_ACT_RELU2);
+  const WsLayout L = linear_layout(cfg);
   if (workspace_bytes < L.total)
     return fail(B4_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, L.total);
   DevInfo dev;
@@ -547,7 +555,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
 
   const int fmt = cfg->format;
   const int m = cfg->m, N = cfg->inter, K = cfg->hidden;
-  bool small = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && m <= B4_DECODE_MAX_M);
+  bool small = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && m <= kDecodeAutoMaxM);
   if (small && !L.decode_ok) small = false;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
@@ -612,9 +620,12 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
   }
 
   // The grouped tcgen05 GEMM over one "expert" whose routes are the tokens in
-  // order: the route pack of the trivial routing writes the chunk schedule,
-  // the GEMM reads x rows directly (slot i is token i) and its epilogue stores
-  // the scaled accumulator as bf16.
+  // order: the route pack of the trivial routing writes the chunk schedule
+  // and the GEMM reads x rows directly (slot i is token i).  With enough
+  // (chunk, tile) units for the GPU, its FC1 epilogue stores the scaled
+  // accumulator as bf16; with few (small m: one chunk, N / 256 tile pairs),
+  // the weights-on-N kernel runs in its FC2 mode with K split across units,
+  // adding fp32 partials into [m, N], and the finalize kernel rounds them.
   RoutePackParams rp{};
   rp.topk_ids = nullptr;
   rp.m = m;
@@ -630,6 +641,55 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
   const bool weights_on_n = m < 96;  // the fused-MoE rule m * top_k < 96 * E_l with E_l = top_k = 1
   rp.chunk_rows = weights_on_n ? kChunkRowsN : kChunkRowsM;
   rp.status = status;
+  const int base_units = cdiv(m, kChunkRowsN) * ((g1.n_tiles + 1) / 2);
+  if (weights_on_n && base_units < dev.sms) {
+    int ks = cdiv(dev.sms, base_units);
+    const int most = g1.k_stages / 4 > 1 ? g1.k_stages / 4 : 1;  // >= 4 K stages per split
+    if (ks > most) ks = most;
+    GemmParams p2{};
+    p2.m = m;
+    p2.top_k = 1;
+    p2.num_global_experts = 1;
+    p2.num_local_experts = 1;
+    p2.hidden = N;  // FC2 mode: output columns
+    p2.inter = K;   // ... and its K
+    p2.inter_pad = round_up(K, kBK);
+    p2.act = 1;
+    p2.x = x;
+    p2.status = status;
+    p2.max_chunks = L.max_chunks;
+    p2.trace = g_trace;
+    p2.wcodes = w;
+    p2.wscales = sc;
+    p2.gs = gs;
+    p2.n_tiles = g1.n_tiles;
+    p2.k_stages = g1.k_stages;
+    p2.k_splits = ks;
+    p2.sorted_routes = rp.sorted_routes;
+    p2.chunk_count = rp.chunk_count;
+    p2.chunks = rp.chunks;
+    if (!make_tmap_bf16_2d(&p2.tmap_b, x, (uint64_t)m, (uint64_t)K, 32))
+      return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the x map");
+    float* acc = reinterpret_cast<float*>(ws + L.acc);
+    p2.acc_out = acc;
+    p2.pdl_wait_first = 1;
+    FinalizeParams fp{};
+    fp.m = m;
+    fp.hidden = N;
+    fp.acc = acc;
+    fp.out = out;
+    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    if ((e = cudaMemsetAsync(acc, 0, (size_t)m * N * sizeof(float), s)) != cudaSuccess)
+      return cuda_fail(e, "linear: clear the accumulator");
+    if ((e = launch_route_pack(rp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "route pack");
+    if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    if ((e = launch_mode<kFc2Grouped>(fmt, true, p2, dev.sms, true, s)) != cudaSuccess)
+      return cuda_fail(e, "linear (K-split grouped)");
+    if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    if ((e = launch_finalize(fp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "linear: finalize");
+    if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    return B4_OK;
+  }
   GemmParams p1{};
   p1.m = m;
   p1.top_k = 1;

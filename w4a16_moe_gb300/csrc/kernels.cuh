@@ -66,13 +66,16 @@ struct GemmParams {
   int act;              // 0 SwiGLU, 1 ReLU^2, 2 none (dense linear: h = the scaled accumulator)
   // routing inputs
   const int32_t* topk_ids;
-  const float* topk_weights;
+  const float* topk_weights;  // or null (FC2: router weight 1, the dense linear layer)
   const int32_t* expert_map;  // or null
   // grouped schedule (from the route-pack kernel)
   const int32_t* sorted_routes;
   const int32_t* chunk_count;
   const int4* chunks;   // (expert, first slot, rows, 0)
   int max_chunks;
+  // K splits of each (chunk, tile pair) unit: weights-on-N kernel, FC2 mode
+  // only (its epilogue adds partials); 0 or 1 = none
+  int k_splits;
   // B operand sources
   const uint16_t* x;    // [m, H] bf16 (FC1)
   uint16_t* xp;         // [R_cap, H] bf16: x rows in packed-route order (grouped FC1)

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         for (int i = et; i < U.rows; i += 128) {
           const int route = __ldg(p.sorted_routes + U.slot0 + i);
           s_tok[i] = route / p.top_k;
-          s_wt[i] = __ldg(p.topk_weights + route);
+          s_wt[i] = p.topk_weights ? __ldg(p.topk_weights + route) : 1.0f;
         }
         named_bar_sync(2, 128);
       }

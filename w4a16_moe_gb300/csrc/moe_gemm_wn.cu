@@ -78,18 +78,26 @@ struct SmemLayout {
 
 struct Unit {
   int expert, pair, slot0, rows, ntiles;
+  int kbeg, kend;  // K stages of the unit (a K split of FC2 adds its partial like any other)
 };
 
 __device__ __forceinline__ int num_pairs(const GemmParams& p) { return (p.n_tiles + 1) >> 1; }
 
+__device__ __forceinline__ int num_ksplits(const GemmParams& p) { return p.k_splits > 1 ? p.k_splits : 1; }
+
 __device__ __forceinline__ int num_units(const GemmParams& p) {
   int c = *(volatile const int32_t*)p.chunk_count;
   c = c < 0 ? 0 : (c > p.max_chunks ? p.max_chunks : c);
-  return c * num_pairs(p);
+  return c * num_pairs(p) * num_ksplits(p);
 }
 
+// Unit u = ((chunk * pairs) + pair) * splits + split.
 __device__ __forceinline__ bool get_unit(const GemmParams& p, int u, Unit& U) {
-  const int np = num_pairs(p);
+  const int np = num_pairs(p), ns = num_ksplits(p);
+  const int ks = u % ns;
+  u /= ns;
+  U.kbeg = (int)((long long)ks * p.k_stages / ns);
+  U.kend = (int)((long long)(ks + 1) * p.k_stages / ns);
   const int c = u / np;
   U.pair = u - c * np;
   U.ntiles = min(2, p.n_tiles - 2 * U.pair);
@@ -97,7 +105,7 @@ __device__ __forceinline__ bool get_unit(const GemmParams& p, int u, Unit& U) {
   U.expert = ch.x;
   U.slot0 = ch.y;
   U.rows = ch.z;
-  return U.rows > 0;
+  return U.rows > 0 && U.kend > U.kbeg;
 }
 
 // Timeline hook: CTA 0 records clock64() of event `kind` number `idx`.
@@ -190,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         Unit U;
         if (!get_unit(p, u, U)) continue;
         const size_t tile0 = (size_t)U.expert * p.n_tiles + 2 * U.pair;
-        for (int s = 0; s < p.k_stages; ++s, ++ws) {
+        for (int s = U.kbeg; s < U.kend; ++s, ++ws) {
           const uint32_t slot = ws % NW;
           if (!mbar_wait(&empty_w[slot], ((ws / NW) & 1) ^ 1, ab, 1)) break;
           mbar_arrive_expect_tx(&full_w[slot], U.ntiles * (kCodeBytesPerStage + kScaleStage));
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const uint32_t d_tmem = tmem_base + abuf * kBN;
         const uint32_t idesc = idesc_bf16_m128((uint32_t)(U.ntiles * kTileRows));
         bool ok = true;
-        for (int s = 0; s < p.k_stages; ++s, ++ss) {
+        for (int s = U.kbeg; s < U.kend; ++s, ++ss) {
           const uint32_t slot = ss % NS;
           if (!mbar_wait(&full_a[slot], (ss / NS) & 1, ab, 3) || !mbar_wait(&full_b[slot], (ss / NS) & 1, ab, 4)) {
             ok = false;
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t adesc = smem_desc_sw128(a_base + slot * kAStage + kk * 32);
             const uint64_t bdesc = smem_desc_sw128(b_base + slot * kBStage + kk * 32);
-            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (s > U.kbeg || kk > 0) ? 1u : 0u);
           }
           mma_commit(&stage_free[slot]);
           trace_mark(p, 2, ss);
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int nload = cdiv(U.rows, 32);
       const uint32_t bytes = (uint32_t)nload * 4096u;
       bool ok = true;
-      for (int s = 0; s < p.k_stages; ++s, ++ss) {
+      for (int s = U.kbeg; s < U.kend; ++s, ++ss) {
         const uint32_t slot = ss % NS;
         if (!warp_wait(&stage_free[slot], ((ss / NS) & 1) ^ 1, ab, 5)) {
           ok = false;
@@ -305,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       if (!get_unit(p, u, U)) continue;
       const bool active = tl < U.ntiles;
       bool ok = true;
-      for (int s = 0; s < p.k_stages; ++s, ++ws) {
+      for (int s = U.kbeg; s < U.kend; ++s, ++ws) {
         const uint32_t wslot = ws % NW, slot = ws % NS;
         if (!warp_wait(&full_w[wslot], (ws / NW) & 1, ab, 6)) {
           ok = false;
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       if (MODE == kFc2Grouped && live) {
         const int route = __ldg(p.sorted_routes + U.slot0 + er);
         token = route / p.top_k;
-        gsv *= __ldg(p.topk_weights + route);
+        if (p.topk_weights) gsv *= __ldg(p.topk_weights + route);  // null: weight 1 (the dense linear layer)
       }
       if (!warp_wait(&full_acc[abuf], (acc_i >> 1) & 1, ab, 8)) break;
       tc_fence_after();
