@@ -4,6 +4,7 @@
     python tests/csrc/perf_probes.py stage   throughput of the decode stage arithmetic
     python tests/csrc/perf_probes.py mma     tcgen05.mma cycles per instruction
     python tests/csrc/perf_probes.py launch  launch latency of an empty kernel inside a CUDA graph
+    python tests/csrc/perf_probes.py subnormal  mma.sync bf16 with subnormal A inputs
 
 Needs a GPU and tests/csrc/libb4probe.so (built by __graft_entry__.build()).
 """
@@ -77,6 +78,19 @@ def mma():
             print(f"{name}, {commit:16s}: {t1 / n:6.1f} cycles / MMA issued, {t2 / n:6.1f} to completion")
 
 
+def subnormal():
+    """mma.sync bf16 with subnormal A: 16 products of A x B summed per output."""
+    f = LIB.probe_mma_sync_const
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    out = torch.zeros(128, device="cuda")
+    for a_bits, what in ((0x0040, "2^-127 (subnormal)"), (0x0001, "2^-133 (smallest subnormal)"),
+                         (0x0080, "2^-126 (smallest normal)"), (0x3F80, "1.0")):
+        for b_bits, bwhat in ((0x7180, "2^100"), (0x3F80, "1.0")):
+            assert f(a_bits, b_bits, out.data_ptr()) == 0
+            v = out[0].item()
+            print(f"A = {what:28s} B = {bwhat:6s}: D = {v!r} (all equal: {bool((out == out[0]).all())})")
+
+
 def launch():
     f = LIB.probe_launch
     f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
@@ -110,4 +124,4 @@ def launch():
 
 
 if __name__ == "__main__":
-    {"ops": ops, "stage": stage, "mma": mma, "launch": launch}[sys.argv[1]]()
+    {"ops": ops, "stage": stage, "mma": mma, "launch": launch, "subnormal": subnormal}[sys.argv[1]]()

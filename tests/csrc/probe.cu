@@ -514,6 +514,16 @@ __global__ void probe_launch_kernel(int* out) {
   if (threadIdx.x == 0 && blockIdx.x == 0 && out) out[0] = sm_launch[0] * 0 + 1;
 }
 
+// mma.sync m16n8k16 bf16 with every A element = a_bits and every B element =
+// b_bits (one warp): out[lane * 4 + i] = D fragment element i.  With A a
+// bf16 subnormal this shows whether the tensor core keeps subnormal inputs.
+__global__ void probe_mma_sync_const_kernel(uint16_t a_bits, uint16_t b_bits, float* out) {
+  const uint32_t a = (uint32_t)a_bits | ((uint32_t)a_bits << 16), b = (uint32_t)b_bits | ((uint32_t)b_bits << 16);
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_16816(d, a, a, a, a, b, b);
+  for (int i = 0; i < 4; ++i) out[threadIdx.x * 4 + i] = d[i];
+}
+
 extern "C" {
 
 int probe_mma_ts(const uint16_t* A, const uint16_t* B, int N, float* D, uint32_t* status) {
@@ -620,6 +630,11 @@ int probe_launch(int grid, int block, int smem_bytes, int cooperative, int* out,
   cfg.attrs = attr;
   cfg.numAttrs = cooperative ? 1 : 0;
   return (int)cudaLaunchKernelEx(&cfg, probe_launch_kernel, out);
+}
+
+int probe_mma_sync_const(int a_bits, int b_bits, float* out) {
+  probe_mma_sync_const_kernel<<<1, 32>>>((uint16_t)a_bits, (uint16_t)b_bits, out);
+  return (int)cudaDeviceSynchronize();
 }
 
 }  // extern "C"

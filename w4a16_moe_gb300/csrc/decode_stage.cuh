@@ -52,22 +52,15 @@ template <int FMT>
 __device__ __forceinline__ void compute_stage(const StageIn& in, float (&d)[4], float (&e)[4]) {
   const uint32_t sa = d_scale<FMT>(in.b0), sb = d_scale<FMT>(in.b1);
   uint32_t a0[8], a1[8];
-  a0[0] = bf16x2_mul(fp4x2_lookup(in.c0.x), sa);
-  a0[1] = bf16x2_mul(fp4x2_lookup((in.c0.x >> 2)), sa);
-  a0[2] = bf16x2_mul(fp4x2_lookup((in.c0.x >> 16)), sa);
-  a0[3] = bf16x2_mul(fp4x2_lookup((in.c0.x >> 18)), sa);
-  a0[4] = bf16x2_mul(fp4x2_lookup(in.c0.y), sa);
-  a0[5] = bf16x2_mul(fp4x2_lookup((in.c0.y >> 2)), sa);
-  a0[6] = bf16x2_mul(fp4x2_lookup((in.c0.y >> 16)), sa);
-  a0[7] = bf16x2_mul(fp4x2_lookup((in.c0.y >> 18)), sa);
-  a1[0] = bf16x2_mul(fp4x2_lookup(in.c1.x), sb);
-  a1[1] = bf16x2_mul(fp4x2_lookup((in.c1.x >> 2)), sb);
-  a1[2] = bf16x2_mul(fp4x2_lookup((in.c1.x >> 16)), sb);
-  a1[3] = bf16x2_mul(fp4x2_lookup((in.c1.x >> 18)), sb);
-  a1[4] = bf16x2_mul(fp4x2_lookup(in.c1.y), sb);
-  a1[5] = bf16x2_mul(fp4x2_lookup((in.c1.y >> 2)), sb);
-  a1[6] = bf16x2_mul(fp4x2_lookup((in.c1.y >> 16)), sb);
-  a1[7] = bf16x2_mul(fp4x2_lookup((in.c1.y >> 18)), sb);
+  fp4x8_lookup(in.c0.x, a0[0], a0[1], a0[2], a0[3]);
+  fp4x8_lookup(in.c0.y, a0[4], a0[5], a0[6], a0[7]);
+  fp4x8_lookup(in.c1.x, a1[0], a1[1], a1[2], a1[3]);
+  fp4x8_lookup(in.c1.y, a1[4], a1[5], a1[6], a1[7]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a0[i] = bf16x2_mul(a0[i], sa);
+    a1[i] = bf16x2_mul(a1[i], sb);
+  }
   mma_16816(d, a0[0], a1[0], a0[1], a1[1], in.xa.x, in.xa.y);
   mma_16816(e, a0[2], a1[2], a0[3], a1[3], in.xa.z, in.xa.w);
   mma_16816(d, a0[4], a1[4], a0[5], a1[5], in.xb.x, in.xb.y);

@@ -25,6 +25,21 @@ __device__ __forceinline__ uint32_t fp4x2_lookup(uint32_t sel) {
   return __byte_perm(0xC0804000u, 0x81800100u, (sel & 0x3333u) | 0x4040u);
 }
 
+// The four pairs of one code word, with the selectors formed on all 32 bits
+// at once: (v & 0x33333333) | 0x40404040 holds the selectors of pairs 0 (low
+// half) and 2 (high half), the same of v >> 2 those of pairs 1 and 3, and a
+// PRMT reads only the low 16 bits of its selector -- two LOP3 and three
+// shifts per word instead of four LOP3 and three shifts (the decode path's
+// register dequantiser, which is bound by these instructions).
+__device__ __forceinline__ void fp4x8_lookup(uint32_t v, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  const uint32_t s = (v & 0x33333333u) | 0x40404040u;
+  const uint32_t t = ((v >> 2) & 0x33333333u) | 0x40404040u;
+  p0 = __byte_perm(0xC0804000u, 0x81800100u, s);
+  p1 = __byte_perm(0xC0804000u, 0x81800100u, t);
+  p2 = __byte_perm(0xC0804000u, 0x81800100u, s >> 16);
+  p3 = __byte_perm(0xC0804000u, 0x81800100u, t >> 16);
+}
+
 template <int FMT>
 __device__ __forceinline__ void dequant_stage(const uint4& c0, const uint4& c1, uint32_t sc, uint32_t (&r)[32]) {
   uint32_t s[4];
