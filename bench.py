@@ -351,10 +351,12 @@ class Bench:
 KERNEL_SOURCES = {
     "decode": ["decode_moe.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
     "grouped": ["moe_gemm.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
+    "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
-NCU_TRAFFIC = {  # (path, workload, m): (source hash, bytes per call of the GEMM kernel(s))
-    ("decode", "decode:relu2", 1): ("92873967035bbfb0", 56_736_512 + 380_928),
-    ("grouped", "prefill:silu", 2048): ("c8dc2932b10dd80f", 1_040_686_000 + 81_905_664 + 599_862_000 + 85_172_736),
+NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
+    ("decode", "decode:relu2", 1): ("407121b85be645f0", 56_748_288 + 386_048),
+    ("grouped", "prefill:silu", 2048): ("955279f4e866ec39", 1_040_492_800 + 81_080_576 + 599_979_264 + 81_397_760),
+    ("grouped_wn", "small:silu", 16): ("70e0638bfeda1c70", 114_016_000 + 3_664_128 + 57_218_304 + 115_968),
 }
 
 
@@ -412,8 +414,17 @@ def kernel_source_hash(path):
     return h.hexdigest()[:16]
 
 
+def kernel_family(b):
+    """Which GEMM kernels serve the call: the fused decode kernel, or the
+    grouped weights-on-N / weights-on-M kernels (api.cu's dispatch rule)."""
+    if b.decode:
+        return "decode"
+    wl = b.wl
+    return "grouped_wn" if b.m * wl.top_k < 96 * wl.num_local_experts else "grouped"
+
+
 def measured_traffic(b):
-    path = "decode" if b.decode else "grouped"
+    path = kernel_family(b)
     rec = NCU_TRAFFIC.get((path, f"{b.wl.name}:{b.wl.act}", b.m))
     if rec is None or rec[0] != kernel_source_hash(path):
         return None
