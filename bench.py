@@ -354,9 +354,9 @@ KERNEL_SOURCES = {
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
-    ("decode", "decode:relu2", 1): ("407121b85be645f0", 56_748_288 + 386_048),
+    ("decode", "decode:relu2", 1): ("b77a30c44d61b593", 56_748_288 + 338_688),
     ("grouped", "prefill:silu", 2048): ("955279f4e866ec39", 1_040_492_800 + 81_080_576 + 599_979_264 + 81_397_760),
-    ("grouped_wn", "small:silu", 16): ("70e0638bfeda1c70", 114_016_000 + 3_664_128 + 57_218_304 + 115_968),
+    ("grouped_wn", "small:silu", 16): ("1a8ae9ea77297757", 114_006_272 + 3_308_288 + 57_212_416 + 94_976),
 }
 
 

@@ -130,8 +130,8 @@ __device__ __forceinline__ void d_unit_shape(const DecodeParams& p, int u, DUnit
   const int rem = u - U.route * per_route;
   U.tile = rem / ns;
   U.split = rem - U.tile * ns;
-  U.kbeg = (int)((long long)U.split * ks / ns);
-  U.kend = (int)((long long)(U.split + 1) * ks / ns);
+  U.kbeg = U.split * ks / ns;  // ks <= 1024 stages, ns <= 8 splits: no overflow
+  U.kend = (U.split + 1) * ks / ns;
   U.expert = -1;
 }
 

@@ -93,11 +93,17 @@ __device__ __forceinline__ int num_units(const GemmParams& p) {
 
 // Unit u = ((chunk * pairs) + pair) * splits + split.
 __device__ __forceinline__ bool get_unit(const GemmParams& p, int u, Unit& U) {
-  const int np = num_pairs(p), ns = num_ksplits(p);
-  const int ks = u % ns;
-  u /= ns;
-  U.kbeg = (int)((long long)ks * p.k_stages / ns);
-  U.kend = (int)((long long)(ks + 1) * p.k_stages / ns);
+  const int np = num_pairs(p);
+  if (p.k_splits > 1) {
+    const int ns = p.k_splits;
+    const int ks = u % ns;
+    u /= ns;
+    U.kbeg = ks * p.k_stages / ns;  // k_stages * splits stays far below 2^31
+    U.kend = (ks + 1) * p.k_stages / ns;
+  } else {
+    U.kbeg = 0;
+    U.kend = p.k_stages;
+  }
   const int c = u / np;
   U.pair = u - c * np;
   U.ntiles = min(2, p.n_tiles - 2 * U.pair);
