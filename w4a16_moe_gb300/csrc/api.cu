@@ -496,6 +496,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   p1.pdl_wait_first = 1;
   p2.h = hbuf;
   p2.acc_out = acc;
+  if (weights_on_n) p2.k_splits = -1;  // few units: split FC2's K (its epilogue adds fp32 partials)
   GemmParams pp = p1;  // permute: x rows -> packed-route order
   pp.xp = xp;
   pp.valid_count = rp.offsets + cfg->num_local_experts;

@@ -74,7 +74,8 @@ struct GemmParams {
   const int4* chunks;   // (expert, first slot, rows, 0)
   int max_chunks;
   // K splits of each (chunk, tile pair) unit: weights-on-N kernel, FC2 mode
-  // only (its epilogue adds partials); 0 or 1 = none
+  // only (its epilogue adds partials); 0 or 1 = none, negative = chosen in
+  // the kernel from the chunk count (about two units per CTA)
   int k_splits;
   // B operand sources
   const uint16_t* x;    // [m, H] bf16 (FC1)

@@ -83,19 +83,31 @@ struct Unit {
 
 __device__ __forceinline__ int num_pairs(const GemmParams& p) { return (p.n_tiles + 1) >> 1; }
 
-__device__ __forceinline__ int num_ksplits(const GemmParams& p) { return p.k_splits > 1 ? p.k_splits : 1; }
+__device__ __forceinline__ int num_chunks(const GemmParams& p) {
+  const int c = *(volatile const int32_t*)p.chunk_count;
+  return c < 0 ? 0 : (c > p.max_chunks ? p.max_chunks : c);
+}
 
-__device__ __forceinline__ int num_units(const GemmParams& p) {
-  int c = *(volatile const int32_t*)p.chunk_count;
-  c = c < 0 ? 0 : (c > p.max_chunks ? p.max_chunks : c);
-  return c * num_pairs(p) * num_ksplits(p);
+// K splits of every unit: p.k_splits when above 1; when negative (automatic,
+// FC2 only), enough for about two units per CTA, at most 4 and with at least
+// 4 stages each; otherwise none.  Every thread computes the same value from
+// the chunk count.
+__device__ __forceinline__ int num_ksplits(const GemmParams& p, int chunks) {
+  if (p.k_splits > 1) return p.k_splits;
+  if (p.k_splits < 0 && chunks > 0) {
+    const int base = chunks * num_pairs(p);
+    const int most = p.k_stages / 4 < 4 ? p.k_stages / 4 : 4;
+    int ns = (2 * (int)gridDim.x + base - 1) / base;
+    ns = ns < most ? ns : most;
+    return ns > 1 ? ns : 1;
+  }
+  return 1;
 }
 
 // Unit u = ((chunk * pairs) + pair) * splits + split.
-__device__ __forceinline__ bool get_unit(const GemmParams& p, int u, Unit& U) {
+__device__ __forceinline__ bool get_unit(const GemmParams& p, int u, int ns, Unit& U) {
   const int np = num_pairs(p);
-  if (p.k_splits > 1) {
-    const int ns = p.k_splits;
+  if (ns > 1) {
     const int ks = u % ns;
     u /= ns;
     U.kbeg = ks * p.k_stages / ns;  // k_stages * splits stays far below 2^31
@@ -192,7 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   if (p.pdl_wait_first) pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  const int n_units = num_units(p);
+  const int n_chunks = num_chunks(p);
+  const int n_split = num_ksplits(p, n_chunks);
+  const int n_units = n_chunks * num_pairs(p) * n_split;
   const size_t wtile_codes = (size_t)p.k_stages * kCodeBytesPerStage;
   const size_t wtile_scales = (size_t)p.k_stages * kScaleStage;
 
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (lane == 0) {
       for (int u = blockIdx.x; u < n_units && !ab.raised(); u += gridDim.x) {
         Unit U;
-        if (!get_unit(p, u, U)) continue;
+        if (!get_unit(p, u, n_split, U)) continue;
         const size_t tile0 = (size_t)U.expert * p.n_tiles + 2 * U.pair;
         for (int s = U.kbeg; s < U.kend; ++s, ++ws) {
           const uint32_t slot = ws % NW;
@@ -236,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         Unit U;
-        if (!get_unit(p, u, U)) continue;
+        if (!get_unit(p, u, n_split, U)) continue;
         const uint32_t abuf = acc_i & 1;
         if (!mbar_wait(&empty_acc[abuf], ((acc_i >> 1) & 1) ^ 1, ab, 2)) break;
         tc_fence_after();
@@ -276,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     uint32_t ss = 0;
     for (int u = blockIdx.x; u < n_units && !ab.raised(); u += gridDim.x) {
       Unit U;
-      if (!get_unit(p, u, U)) continue;
+      if (!get_unit(p, u, n_split, U)) continue;
       const int nload = cdiv(U.rows, 32);
       const uint32_t bytes = (uint32_t)nload * 4096u;
       bool ok = true;
@@ -316,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     uint32_t ws = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
-      if (!get_unit(p, u, U)) continue;
+      if (!get_unit(p, u, n_split, U)) continue;
       const bool active = tl < U.ntiles;
       bool ok = true;
       for (int s = U.kbeg; s < U.kend; ++s, ++ws) {
@@ -376,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     uint32_t acc_i = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
-      if (!get_unit(p, u, U)) continue;
+      if (!get_unit(p, u, n_split, U)) continue;
       const uint32_t abuf = acc_i & 1;
       const bool live = er < U.rows;
       // per-route constants, resolved before the wait
