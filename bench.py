@@ -404,21 +404,27 @@ class LinearBench(Bench):
         self.b4.linear(self.cfg, d["xd"], dv["w"], dv["s"], dv["g"], self.out, self.ws, stream=stream)
 
 
-def kernel_source_hash(path):
-    """Hash of the kernel family's sources with comments and blank lines
-    removed: a comment edit does not change the kernels the counters were
-    taken on."""
+def source_hash(texts):
+    """Hash of source texts with comments and blank lines removed: a comment
+    edit does not change the kernels the counters were taken on."""
     import hashlib
     import re
 
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[path]:
-        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "w4a16_moe_gb300", "csrc", f)) as fh:
-            src = fh.read()
+    for src in texts:
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
         h.update("\n".join(line.rstrip() for line in src.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash(path):
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "w4a16_moe_gb300", "csrc")
+    texts = []
+    for f in KERNEL_SOURCES[path]:
+        with open(os.path.join(csrc, f)) as fh:
+            texts.append(fh.read())
+    return source_hash(texts)
 
 
 def kernel_family(b):

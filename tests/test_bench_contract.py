@@ -1,0 +1,73 @@
+"""bench.py's output contract, on CPU: the reference arm's JSON line, the
+argument guards, and the per-call byte / flop accounting the roofline uses."""
+
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def _run(*args):
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                          cwd=ROOT, timeout=600)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["higher_is_better"] is False and d["unit"] == "us/call"
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["config"]["workload"].startswith("decode NVFP4 MoE") and d["config"]["workload"].endswith("m=1")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["value"] > 0 and abs(d["ms_per_step"] - d["value"] / 1e3) < 1e-3
+
+
+def test_argument_guards():
+    r = _run("--warmup", "2")
+    assert r.returncode != 0 and "warmup" in r.stderr
+    r = _run("--workload", "linear:none:1")
+    assert r.returncode != 0 and "secondary" in r.stderr
+
+
+def test_call_accounting_counts_each_hit_expert_once():
+    wl = W.WORKLOADS["decode"]
+    b1 = wl.inter * wl.hidden // 2 + wl.inter * wl.hidden // 16 + 4  # W1 codes + E4M3 scales + fp32 gs
+    b2 = wl.hidden * wl.inter // 2 + wl.hidden * wl.inter // 16 + 4
+    ids = np.array([[0, 1, 2, 3, 4, 5, 6, 7], [7, 6, 5, 4, 3, 2, 1, 0]], np.int32)  # 8 distinct experts, twice
+    a = bench.call_accounting(wl, 2, ids, None)
+    assert a["experts_hit"] == 8 and a["routes"] == 16
+    assert a["weight_bytes"] == 8 * (b1 + b2)
+    assert a["bytes"] == 8 * (b1 + b2) + 2 * wl.hidden * 2 * 2 + 2 * wl.top_k * 8
+    assert a["flops"] == 2.0 * 16 * (wl.inter * wl.hidden + wl.hidden * wl.inter)
+    # invalid ids and experts mapped away carry no bytes
+    wl_mx = W.WORKLOADS["mxfp4"]
+    em = W.expert_map(wl_mx)
+    ids = np.array([[-1, 32, 3, 11]], np.int32)  # invalid, invalid, dropped by the map, dropped by the map
+    a = bench.call_accounting(wl_mx, 1, ids, em)
+    assert a["experts_hit"] == 0 and a["weight_bytes"] == 0 and a["routes"] == 0
+
+
+def test_traffic_hash_ignores_comments():
+    """The measured traffic stays attached to unchanged kernel code."""
+    h1 = bench.source_hash(["int f() { return 1; }  // one\n/* block\n comment */\n", "x"])
+    h2 = bench.source_hash(["// a new comment\n\nint f() { return 1; }\n", "x  "])
+    h3 = bench.source_hash(["int f() { return 2; }\n", "x"])
+    assert h1 == h2 != h3
+    for fam in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_source_hash(fam)) == 16
