@@ -541,6 +541,16 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(value, dist, device):
+    """The slowest rank's value (replicas: the job's time per step is the
+    longest rank's); every rank gets it."""
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -584,9 +594,7 @@ def main():
     head = summarize(b, res, peaks)
     us = head["us_per_call"]
     if dist is not None:
-        t = torch.tensor([us], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us = float(t.item())
+        us = max_over_ranks(us, dist, "cuda")
     e2e = res["e2e_s"]
     e2e_us = e2e["seconds"] / args.steps * 1e6
     line = {
