@@ -48,12 +48,13 @@
 // the FC1 split partials straight into out; those units stream no weights.
 //
 // Why warp-level MMAs and not tcgen05 here: one tcgen05.mma covers 128 x 16
-// weights and costs ~165 cycles to issue whatever its N, which caps a GEMV
+// weights and costs ~200-275 cycles to issue whatever its N, which caps a GEMV
 // near 2 TB/s; m16n8k16 issues in a few cycles, leaving the dequantiser's
-// integer work as the limit: per weight pair a LOP3, a PRMT and a bf16x2
-// multiply, plus three shifts per code word, all on the SM's half-rate
-// integer/bf16 pipe (measured: 2 warp-instructions per clock per SM for each
-// of them, 1 for a multiply-high), which caps the dequantiser near 5 TB/s.
+// integer work as the limit: per code word (8 weights) two LOP3 and three
+// shifts, per weight pair a PRMT and a bf16x2 multiply, all on the SM's
+// half-rate integer/bf16 pipe (measured: 2 warp-instructions per clock per SM
+// for each of them, 1 for a multiply-high), which caps the stage arithmetic
+// near 4.7 TB/s at two CTAs per SM.
 //
 // K order inside an MMA: thread t of a quad owns physical 16-element block t
 // of the 64-wide stage (one NVFP4 scale block); MMA j takes its pairs 2j and

@@ -20,7 +20,7 @@
 // shared memory, loaded by TMA in 32-row 2-D boxes with the 128-byte
 // swizzle), N = 256 weight rows (B, K-major in shared memory, 128-byte
 // swizzle), fp32 accumulators in tensor memory.  One tcgen05.mma issue costs
-// about the same time whatever its N (measured ~197 cycles), and an expert
+// about the same time whatever its N (measured ~200-275 cycles), and an expert
 // here has about as many routes as a tile has rows, so putting the 256 weight
 // rows on N does twice the work per instruction that 128 weight rows on M
 // would.  Weights are dequantised from E2M1 codes and E4M3 / E8M0 block scales
