@@ -68,7 +68,13 @@ def mma():
                     ("N=16,  A smem, 2 acc", 2 | 16),
                     ("SW128 N=64,  A smem, 2 acc", 32 | 2 | 16 | 128), ("SW128 N=128, A smem, 2 acc", 32 | 2 | 16 | 64),
                     ("SW128 N=256, A smem, 2 acc", 32 | 2 | 16 | 8), ("SW128 N=128, A tmem, 1 acc", 32 | 64),
-                    ("SW128 N=256, A tmem, 1 acc", 32 | 8)):
+                    ("SW128 N=256, A tmem, 1 acc", 32 | 8),
+                    ("SW128 M=64 N=128, A smem, 2 acc", 256 | 32 | 2 | 16 | 64),
+                    ("SW128 M=64 N=256, A smem, 2 acc", 256 | 32 | 2 | 16 | 8),
+                    ("hoisted descriptors, N=64", 512 | 128), ("hoisted descriptors, N=128", 512 | 64),
+                    ("hoisted descriptors, N=256", 512 | 8),
+                    ("per-MMA descriptors, runtime slot, N=128", 2048 | 64),
+                    ("per-MMA descriptors, runtime slot, commit per stage, N=128", 2048 | 4096 | 64)):
         for per, pc in ((4, 4), (4, 0)):
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0

@@ -328,7 +328,52 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
     mbar_arrive(&bar_ready);  // phase 0 complete: waits on it return at once
     const uint32_t n = (variant & 8) ? 256u : (variant & 1) ? 160u : (variant & 64) ? 128u : (variant & 128) ? 64u : 16u;
     const bool sw = (variant & 32) != 0;  // 128-byte-swizzled K-major operands (as in the GEMM kernels)
-    const uint32_t idesc = idesc_bf16_m128(n);
+    // variant bit 256: M = 64 instead of 128 (A from shared memory)
+    const uint32_t idesc = (variant & 256) ? ((idesc_bf16_m128(n) & ~(0x1Fu << 24)) | ((64u >> 4) << 24))
+                                           : idesc_bf16_m128(n);
+    if (variant & 2048) {
+      // as the GEMM kernels issue: descriptors rebuilt for every MMA from a
+      // runtime ring slot (three 16 KB A and 32 KB B stages), four MMAs per
+      // stage unrolled, one commit per stage when bit 4096 is set
+      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+      const uint32_t rz = (uint32_t)variant >> 30;  // 0 at run time, unknown to the compiler
+      const long long t0b = clock64();
+      for (int s = 0; s < 64; ++s) {
+        const uint32_t slot = ((uint32_t)s % 3u) * rz;  // every slot maps onto the one probe buffer
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t adesc = smem_desc_sw128(a_base + slot * 16384u + kk * 32);
+          const uint64_t bdesc = smem_desc_sw128(b_base + slot * 32768u + kk * 32);
+          mma_bf16_ss(base + ((kk & 1) ? 256u : 0u), adesc, bdesc, idesc, (s > 0 || kk > 1) ? 1u : 0u);
+        }
+        if (variant & 4096) mma_commit(&bar_stage);
+      }
+      const long long t1b = clock64();
+      mma_commit(&bar_done);
+      mbar_wait(&bar_done, 0, ab, 116);
+      out[0] = t1b - t0b;
+      out[1] = clock64() - t0b;
+    } else if (variant & 512) {
+      // descriptors computed before the loop, four MMAs per iteration
+      // unrolled (A and B in shared memory, 128-byte swizzle, two accumulators)
+      uint64_t ad[4], bd[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        ad[kk] = smem_desc_sw128(smem_u32(sA) + kk * 32);
+        bd[kk] = smem_desc_sw128(smem_u32(sB) + kk * 32);
+      }
+      const long long t0b = clock64();
+      for (int s = 0; s < 64; ++s) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(base + ((kk & 1) ? 256u : 0u), ad[kk], bd[kk], idesc, (s > 0 || kk > 1) ? 1u : 0u);
+      }
+      const long long t1b = clock64();
+      mma_commit(&bar_done);
+      mbar_wait(&bar_done, 0, ab, 115);
+      out[0] = t1b - t0b;
+      out[1] = clock64() - t0b;
+    } else {
     const long long t0 = clock64();
     for (int s = 0; s < 64; ++s) {
       if (variant & 4) {
@@ -360,6 +405,7 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
     const long long t2 = clock64();
     out[0] = t1 - t0;  // issue time of 64 stages
     out[1] = t2 - t0;  // until the last completes
+    }
   }
   tc_fence_before();
   __syncthreads();

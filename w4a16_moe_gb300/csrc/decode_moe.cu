@@ -47,10 +47,11 @@
 // units, and each "FC2" unit is an output tile (token, 128 columns) that sums
 // the FC1 split partials straight into out; those units stream no weights.
 //
-// Why warp-level MMAs and not tcgen05 here: one tcgen05.mma covers 128 x 16
-// weights and costs ~200-275 cycles to issue whatever its N, which caps a GEMV
-// near 2 TB/s; m16n8k16 issues in a few cycles, leaving the dequantiser's
-// integer work as the limit: per code word (8 weights) two LOP3 and three
+// Why warp-level MMAs and not tcgen05 here: the register dequantiser feeds
+// m16n8k16 fragments directly, while a tcgen05.mma reads its weight operand
+// from shared or tensor memory, so every dequantised weight would make a
+// round trip there first; with one token per unit the MMA work is tiny either
+// way, which leaves the dequantiser's integer work as the limit: per code word (8 weights) two LOP3 and three
 // shifts, per weight pair a PRMT and a bf16x2 multiply, all on the SM's
 // half-rate integer/bf16 pipe (measured: 2 warp-instructions per clock per SM
 // for each of them, 1 for a multiply-high), which caps the stage arithmetic

@@ -19,11 +19,10 @@
 // tiles).  The tensor-core operation: M = the chunk's routes (A, K-major in
 // shared memory, loaded by TMA in 32-row 2-D boxes with the 128-byte
 // swizzle), N = 256 weight rows (B, K-major in shared memory, 128-byte
-// swizzle), fp32 accumulators in tensor memory.  One tcgen05.mma issue costs
-// about the same time whatever its N (measured ~200-275 cycles), and an expert
-// here has about as many routes as a tile has rows, so putting the 256 weight
-// rows on N does twice the work per instruction that 128 weight rows on M
-// would.  Weights are dequantised from E2M1 codes and E4M3 / E8M0 block scales
+// swizzle), fp32 accumulators in tensor memory.  With few routes per expert,
+// putting 256 weight rows on N does the work of two weights-on-M
+// instructions (whose N would be the few routes, padded to 16) in one, and
+// the expert's weights are dequantised once per 128 routes.  Weights are dequantised from E2M1 codes and E4M3 / E8M0 block scales
 // to bf16 by sixteen dequant warps and stored in the swizzled B layout.
 // Roles, one CTA of 24 warps:
 //   warp 0       bulk-copy (TMA engine) producer of packed codes and scales
