@@ -73,8 +73,12 @@ def mma():
                     ("SW128 M=64 N=256, A smem, 2 acc", 256 | 32 | 2 | 16 | 8),
                     ("hoisted descriptors, N=64", 512 | 128), ("hoisted descriptors, N=128", 512 | 64),
                     ("hoisted descriptors, N=256", 512 | 8),
-                    ("per-MMA descriptors, runtime slot, N=128", 2048 | 64),
-                    ("per-MMA descriptors, runtime slot, commit per stage, N=128", 2048 | 4096 | 64)):
+                    ("kernel-like loop (per-MMA descriptors, runtime slot, commit per stage), N=128", 2048 | 64),
+                    ("  the same + two barrier waits and a fence per stage", 2048 | 8192 | 64),
+                    ("  the same with A in tensor memory, no waits", 2048 | 16384 | 64),
+                    ("  the same with A in tensor memory + waits", 2048 | 8192 | 16384 | 64),
+                    ("  A in tensor memory, test_wait first + fence", 2048 | 32768 | 16384 | 64),
+                    ("  A in tensor memory, try_wait, no fence", 2048 | 65536 | 16384 | 64)):
         for per, pc in ((4, 4), (4, 0)):
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0

@@ -299,6 +299,61 @@ __global__ void probe_mma_sw128_kernel(const __grid_constant__ CUtensorMap tm, c
 // the completion of the last (cycles).  variant bit 0: N = 160 (else 16);
 // bit 1: A from shared memory (else TMEM); bit 2: per stage, also wait on an
 // already-completed mbarrier and fence; bit 3: N = 256.
+// Non-blocking test of a phase (mbarrier.test_wait): true when complete.
+__device__ __forceinline__ bool probe_mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 64 stages of four MMAs as the GEMM kernels issue them (see probe_mma_tput).
+// rz is 0 at run time but unknown to the compiler, so the slot arithmetic is
+// not folded away.  cyc[0] = issue time, cyc[1] = until the last completes.
+template <int WAITS, bool A_TMEM>
+__device__ __noinline__ void issue_loop(uint32_t base, uint32_t a_base, uint32_t b_base, uint32_t idesc, uint32_t rz,
+                                        uint64_t* bar_stage, uint64_t* bar_ready, uint64_t* bar_done, const Abort& ab,
+                                        long long* cyc) {
+  const long long t0 = clock64();
+  for (int s = 0; s < 64; ++s) {
+    const uint32_t slot = ((uint32_t)s % 3u) * rz;
+    if constexpr (WAITS == 1) {  // two bounded try_wait waits and a fence
+      mbar_wait(bar_ready, 0, ab, 117);
+      mbar_wait(bar_ready, 0, ab, 118);
+      tc_fence_after();
+    } else if constexpr (WAITS == 2) {  // two non-blocking tests first, then the fence
+      if (!probe_mbar_test(bar_ready, 0)) mbar_wait(bar_ready, 0, ab, 119);
+      if (!probe_mbar_test(bar_ready, 0)) mbar_wait(bar_ready, 0, ab, 120);
+      tc_fence_after();
+    } else if constexpr (WAITS == 3) {  // two bounded waits, no fence
+      mbar_wait(bar_ready, 0, ab, 121);
+      mbar_wait(bar_ready, 0, ab, 122);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t bdesc = smem_desc_sw128(b_base + slot * 32768u + kk * 32);
+      if constexpr (A_TMEM) {
+        mma_bf16_ts(base + ((kk & 1) ? 320u : 128u), base + (slot * 32u + kk * 8u), bdesc, idesc,
+                    (s > 0 || kk > 1) ? 1u : 0u);
+      } else {
+        const uint64_t adesc = smem_desc_sw128(a_base + slot * 16384u + kk * 32);
+        mma_bf16_ss(base + ((kk & 1) ? 256u : 0u), adesc, bdesc, idesc, (s > 0 || kk > 1) ? 1u : 0u);
+      }
+    }
+    mma_commit(bar_stage);
+  }
+  const long long t1 = clock64();
+  mma_commit(bar_done);
+  mbar_wait(bar_done, 0, ab, 116);
+  cyc[0] = t1 - t0;
+  cyc[1] = clock64() - t0;
+}
+
 __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long long* out, uint32_t* status) {
   __shared__ __align__(1024) uint8_t sB[256 * 128];  // B rows (N <= 256); A in shared memory reuses rows 0..127
   uint8_t* sA = sB;
@@ -331,28 +386,35 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
     // variant bit 256: M = 64 instead of 128 (A from shared memory)
     const uint32_t idesc = (variant & 256) ? ((idesc_bf16_m128(n) & ~(0x1Fu << 24)) | ((64u >> 4) << 24))
                                            : idesc_bf16_m128(n);
-    if (variant & 2048) {
+    if ((variant & 16384) && n > 128) {
+      out[0] = out[1] = -1;  // the tensor-memory-A variant is laid out for N <= 128 only
+    } else if (variant & 2048) {
       // as the GEMM kernels issue: descriptors rebuilt for every MMA from a
-      // runtime ring slot (three 16 KB A and 32 KB B stages), four MMAs per
-      // stage unrolled, one commit per stage when bit 4096 is set
-      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-      const uint32_t rz = (uint32_t)variant >> 30;  // 0 at run time, unknown to the compiler
-      const long long t0b = clock64();
-      for (int s = 0; s < 64; ++s) {
-        const uint32_t slot = ((uint32_t)s % 3u) * rz;  // every slot maps onto the one probe buffer
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(a_base + slot * 16384u + kk * 32);
-          const uint64_t bdesc = smem_desc_sw128(b_base + slot * 32768u + kk * 32);
-          mma_bf16_ss(base + ((kk & 1) ? 256u : 0u), adesc, bdesc, idesc, (s > 0 || kk > 1) ? 1u : 0u);
+      // runtime ring slot, four MMAs per stage unrolled, one commit per stage;
+      // bit 8192 adds two barrier waits and a fence per stage, bit 16384 takes
+      // A from tensor memory.  Each combination is its own branch-free loop.
+      // bits 8192 / 32768 / 65536: waits as try_wait + fence / test_wait first + fence / try_wait, no fence
+      const int waits = (variant & 8192) ? 1 : (variant & 32768) ? 2 : (variant & 65536) ? 3 : 0;
+      const uint32_t rz = (uint32_t)variant >> 30;
+      long long cyc[2];
+      const uint32_t sa = smem_u32(sA), sb = smem_u32(sB);
+      if (variant & 16384) {
+        switch (waits) {
+          case 0: issue_loop<0, true>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+          case 1: issue_loop<1, true>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+          case 2: issue_loop<2, true>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+          default: issue_loop<3, true>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
         }
-        if (variant & 4096) mma_commit(&bar_stage);
+      } else {
+        switch (waits) {
+          case 0: issue_loop<0, false>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+          case 1: issue_loop<1, false>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+          case 2: issue_loop<2, false>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+          default: issue_loop<3, false>(base, sa, sb, idesc, rz, &bar_stage, &bar_ready, &bar_done, ab, cyc); break;
+        }
       }
-      const long long t1b = clock64();
-      mma_commit(&bar_done);
-      mbar_wait(&bar_done, 0, ab, 116);
-      out[0] = t1b - t0b;
-      out[1] = clock64() - t0b;
+      out[0] = cyc[0];
+      out[1] = cyc[1];
     } else if (variant & 512) {
       // descriptors computed before the loop, four MMAs per iteration
       // unrolled (A and B in shared memory, 128-byte swizzle, two accumulators)

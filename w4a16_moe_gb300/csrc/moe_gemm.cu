@@ -98,6 +98,40 @@ __device__ __forceinline__ void trace_mark(const GemmParams& p, int kind, uint32
   if (p.trace && blockIdx.x == 0 && idx < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + idx] = clock64();
 }
 
+// One stage of four MMAs (A slices in tensor memory, B by descriptor), with
+// two non-blocking tests of the next stage's barriers issued first and read
+// only after the MMAs: a barrier test takes ~130 cycles, which the MMA issue
+// then hides.  *na / *nb: the next stage's A / B barriers were seen complete
+// (false when test is 0).
+__device__ __forceinline__ void mma_stage_test_next(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                                    uint32_t idesc, uint32_t accumulate, uint64_t* bar_a,
+                                                    uint32_t par_a, uint64_t* bar_b, uint32_t par_b, uint32_t test,
+                                                    bool* na, bool* nb) {
+  uint32_t ra, rb;
+  asm volatile(
+      "{\n\t.reg .pred pa, pb, g, q, t;\n\t"
+      "setp.ne.b32 g, %9, 0;\n\t"
+      "setp.ne.b32 pa, %9, %9;\n\t"
+      "setp.ne.b32 pb, %9, %9;\n\t"
+      "@g mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 pa, [%5], %6;\n\t"
+      "@g mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 pb, [%7], %8;\n\t"
+      "setp.ne.b32 q, %4, 0;\n\t"
+      "setp.eq.b32 t, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [%3], %10, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [%12], %13, %11, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [%14], %15, %11, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [%16], %17, %11, t;\n\t"
+      "selp.u32 %0, 1, 0, pa;\n\t"
+      "selp.u32 %1, 1, 0, pb;\n\t}"
+      : "=r"(ra), "=r"(rb)
+      : "r"(d_tmem), "r"(a[0]), "r"(accumulate), "r"(smem_u32(bar_a)), "r"(par_a), "r"(smem_u32(bar_b)),
+        "r"(par_b), "r"(test), "l"(b[0]), "r"(idesc), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]),
+        "l"(b[3])
+      : "memory");
+  *na = ra != 0;
+  *nb = rb != 0;
+}
+
 // Warp-uniform bounded wait.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Abort& ab, uint32_t where) {
   const bool ok = mbar_wait(bar, parity, ab, where);
@@ -219,20 +253,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const uint32_t d_tmem = tmem_base + kAccCol0 + abuf * kBN;
         const uint32_t idesc = idesc_bf16_m128((uint32_t)round_up(U.rows, 16));
         bool ok = true;
+        bool pre_a = false, pre_b = false;  // this stage's operands were seen ready during the previous stage
         for (int s = 0; s < p.k_stages; ++s, ++as, ++bs) {
           const uint32_t aslot = as % kNumA, bslot = bs % NB;
-          if (!mbar_wait(&full_a[aslot], (as / kNumA) & 1, ab, 3) ||
-              !mbar_wait(&full_b[bslot], (bs / NB) & 1, ab, 4)) {
+          if ((!pre_a && !mbar_wait(&full_a[aslot], (as / kNumA) & 1, ab, 3)) ||
+              (!pre_b && !mbar_wait(&full_b[bslot], (bs / NB) & 1, ab, 4))) {
             ok = false;
             break;
           }
           tc_fence_after();
+          uint32_t a_tm[4];
+          uint64_t b_desc[4];
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t a_tmem = tmem_base + aslot * kAColsPerSlot + kk * 8;
-            const uint64_t bdesc = smem_desc_sw128(b_base + bslot * kBStage + kk * 32);
-            mma_bf16_ts(d_tmem, a_tmem, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            a_tm[kk] = tmem_base + aslot * kAColsPerSlot + kk * 8;
+            b_desc[kk] = smem_desc_sw128(b_base + bslot * kBStage + kk * 32);
           }
+          const uint32_t nas = as + 1, nbs = bs + 1;
+          mma_stage_test_next(d_tmem, a_tm, b_desc, idesc, s > 0 ? 1u : 0u, &full_a[nas % kNumA],
+                              (nas / kNumA) & 1, &full_b[nbs % NB], (nbs / NB) & 1, s + 1 < p.k_stages ? 1u : 0u,
+                              &pre_a, &pre_b);
           mma_commit(&stage_free[aslot]);
           trace_mark(p, 2, as);
         }
