@@ -355,7 +355,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
     ("decode", "decode:relu2", 1): ("eea3645ca0961c6e", 56_748_288 + 338_688),
-    ("grouped", "prefill:silu", 2048): ("f802220d7ab98c95", 1_040_492_800 + 81_080_576 + 599_979_264 + 81_397_760),
+    ("grouped", "prefill:silu", 2048): ("104a4a1a5aee0830", 1_041_019_392 + 81_157_376 + 599_991_296 + 81_412_608),
     ("grouped_wn", "small:silu", 16): ("14dde3c0816bca2d", 114_006_016 + 3_177_472 + 57_212_672 + 78_592),
 }
 
