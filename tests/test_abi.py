@@ -156,3 +156,13 @@ def test_linear_entry_points_validate_on_the_host(b4):
     assert lib.b4_linear(ctypes.byref(cmx), p, p, p, ctypes.addressof(one), p, p, 1 << 12,
                          None) == b4.B4_ERR_INVALID_ARGUMENT
     assert "global scale" in b4.last_error()
+
+
+def test_linear_workspace_is_monotone_and_capacity_stable(b4):
+    """One workspace serves every m up to the next power of two, and the
+    size never shrinks as m grows (the same contract as b4_workspace_bytes)."""
+    for fmt, n, k in ((b4.NVFP4, 4096, 4096), (b4.MXFP4, 1440, 2880), (b4.NVFP4, 256, 8192)):
+        sizes = [b4.linear_workspace_bytes(b4.linear_config(m, n, k, format=fmt)) for m in range(0, 300, 5)]
+        assert all(a <= b for a, b in zip(sizes, sizes[1:]))
+        assert (b4.linear_workspace_bytes(b4.linear_config(33, n, k, format=fmt))
+                == b4.linear_workspace_bytes(b4.linear_config(64, n, k, format=fmt)))
