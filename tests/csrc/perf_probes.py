@@ -78,7 +78,11 @@ def mma():
                     ("  the same with A in tensor memory, no waits", 2048 | 16384 | 64),
                     ("  the same with A in tensor memory + waits", 2048 | 8192 | 16384 | 64),
                     ("  A in tensor memory, test_wait first + fence", 2048 | 32768 | 16384 | 64),
-                    ("  A in tensor memory, try_wait, no fence", 2048 | 65536 | 16384 | 64)):
+                    ("  A in tensor memory, try_wait, no fence", 2048 | 65536 | 16384 | 64),
+                    ("kernel-like, A in tensor memory, no waits, three warps storing to TMEM meanwhile",
+                     2048 | 16384 | 64 | 131072),
+                    ("kernel-like, A in shared memory, no waits, three warps storing to TMEM meanwhile",
+                     2048 | 64 | 131072)):
         for per, pc in ((4, 4), (4, 0)):
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0
             assert f(v, per, pc, out.data_ptr(), st.data_ptr()) == 0

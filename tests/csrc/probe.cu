@@ -468,6 +468,18 @@ __global__ void probe_mma_tput_kernel(int variant, int per, int per_commit, long
     out[0] = t1 - t0;  // issue time of 64 stages
     out[1] = t2 - t0;  // until the last completes
     }
+  } else if ((variant & 131072) && warp >= 1) {
+    // warps 1-3 store into tensor memory (columns 448..479 of their lane
+    // quarters, away from the MMA operands and accumulators) while thread 0
+    // issues the MMAs: the dequantiser warps' traffic in the GEMM kernels
+    uint32_t r[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) r[c] = 0x3F803F80u + c;
+    const uint32_t taddr = base + ((uint32_t)(32 * warp) << 16) + 448u;
+    for (int it = 0; it < 400; ++it) {
+      tmem_st32(taddr, r);
+      tmem_st_wait();
+    }
   }
   tc_fence_before();
   __syncthreads();
