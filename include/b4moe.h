@@ -184,14 +184,18 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
 b4_status b4_set_timing_events(void* const* events, int32_t n);
 
 /* Optional kernel timeline for profiling: while `device_buffer` is set
- * (>= 163840 bytes, or NULL to turn it off), the GEMM kernels of each
- * b4_fused_moe call on this thread write clock64() timestamps of CTA 0 into
- * it as [5][2048] int64 indexed by the CTA's running counters.  Grouped path:
- * FC1 at offset 0, FC2 at offset 81920; kinds: weight stage issued, A stage
- * written to tensor memory, MMA stage issued, B stage ready, unit epilogue
- * done.  Decode path (one kernel, offset 0): weight slot issued, weight slot
- * consumed, kernel start (0) and grid barrier passed (1), activation row
- * ready, unit done.  Entries not reached are left untouched. */
+ * (>= 163840 bytes = [10][2048] int64, or NULL to turn it off), the kernels
+ * of each b4_fused_moe / b4_linear call on this thread write timestamps into
+ * it.  Grouped path: clock64() of CTA 0 as [5][2048] per GEMM, indexed by the
+ * CTA's running counters, FC1 at int64 offset 0 and FC2 at 10240; kinds:
+ * weight stage issued, A stage written to tensor memory (weights on M) or B
+ * stage dequantised (weights on N), MMA stage issued, activation stage
+ * ready, unit epilogue done.  Decode path (one kernel): kinds 0-4 are
+ * clock64() of CTA 0 -- weight slot issued, weight slot consumed, kernel
+ * start (index 0), activation row ready, unit done; kinds 5-9 are
+ * %globaltimer nanoseconds indexed by CTA -- CTA start, last FC2 partial
+ * stored, last FC1 partial stored, compute warps done, output warp done.
+ * Entries not reached are left untouched. */
 b4_status b4_set_trace(void* device_buffer, size_t bytes);
 
 /* Synchronises `stream`, then reads the device status word of `workspace`
