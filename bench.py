@@ -202,7 +202,8 @@ class Bench:
         self.flush_sink = torch.empty(1, dtype=torch.int32, device="cuda")
         self.stream = torch.cuda.Stream()
         self.decode = m <= 4
-        self.n_kernels = 1 if self.decode else 4  # decode: one fused kernel; grouped: pack, FC1, FC2, finalize
+        self.n_kernels = 1 if self.decode else 4  # timed intervals: decode kernel; pack, permute + FC1, FC2, finalize
+        self.launches = 1 if self.decode else 5  # this library's kernels per call
 
     def flush_l2(self):
         """Evict L2: write a 512 MiB buffer (evicts everything) and read it back,
@@ -398,6 +399,7 @@ class LinearBench(Bench):
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         k_split = m < 96 and -(-m // 128) * ((-(-n // 128) + 1) // 2) < sms
         self.n_kernels = 1 if self.decode else (3 if k_split else 2)
+        self.launches = 1 if self.decode else (3 if k_split else 2)  # pack, GEMM (, rounding pass)
 
     def call(self, d, stream=None):
         dv = self.dev
@@ -613,7 +615,7 @@ def main():
                           "bytes per call of those launches (null if their sources changed since the capture)"),
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"]},
-        "gpu_launches": b.n_kernels * args.steps,
+        "gpu_launches": b.launches * args.steps,
         "clocks": res["clocks"],
         "kernel_us_mean": head["kernel_us_mean"],
     }
