@@ -350,7 +350,7 @@ class Bench:
 # give the commands).  A figure is reported only while the kernel sources still
 # hash to the profiled ones; after any change it is null until re-measured.
 KERNEL_SOURCES = {
-    "decode": ["decode_moe.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
+    "decode": ["decode_grouped.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
     "grouped": ["moe_gemm.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }

@@ -237,8 +237,12 @@ b4_status b4_check_status(void* workspace, b4_stream_t stream);
  *
  * Set-up: the first call on each device, with that device current, looks up
  * the array's device address (cudaGetSymbolAddress, which may load the
- * library's device code onto that device).  Make that first call before any
- * stream capture begins on the device.
+ * library's device code onto that device) and keeps it with the id of the
+ * context it was found in.  Make that first call before any stream capture
+ * begins on the device.  A call in a different context on that device (after
+ * cudaDeviceReset, or a teardown and re-creation of the primary context,
+ * which may place the array elsewhere) looks the address up again, so a
+ * stale address is never used; make that call, too, outside stream capture.
  *
  * Sharing: all calls on a device use the same array, and each call leaves its
  * contents behind.  Every part of it that a call reads is written earlier in

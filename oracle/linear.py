@@ -10,7 +10,7 @@ layer (flashinfer PR #4255, Description): NVFP4 (E2M1 codes, an E4M3 scale
 per 16 elements along K, an fp32 global scale) or MXFP4 (E2M1 codes, an E8M0
 scale per 32 elements along K).
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 
 * out = x . W^T, W[n, k] the dequantised weight of output n and input k,
   i.e. the FC1 product of a one-expert, top-1 MoE layer with no activation;

@@ -11,7 +11,7 @@ What the pages fix (flashinfer PR #4255, Description and Performance):
 * a separate small-m decode path computes the same thing.
 
 This module is the plain definition of what those kernels compute.  Readings
-taken where the pages are silent (each listed in the design doc):
+taken where the pages are silent:
 
 * W13 rows [0, I) are the gate projection and rows [I, 2I) the up projection;
   ReLU^2 is non-gated with W1 of I rows;

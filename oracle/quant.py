@@ -11,7 +11,7 @@ What the pages fix (flashinfer PR #4255, Description and review comments):
   power-of-two scale per 32 elements along K, "including scale-tail handling
   for TP shards that are not 128-aligned".
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * packing: element 2j of a row sits in the low nibble of byte j, element
   2j+1 in the high nibble (the ModelOpt convention);

@@ -14,7 +14,7 @@ What the pages fix (flashinfer PR #4255):
   not use, and the packed-route and route-block capacities are clamped to at
   least 1.
 
-Readings taken (listed in the design doc):
+Readings taken:
 
 * capacity: T_cap = next_pow2(max(m, 1)) tokens, R_cap = T_cap * top_k routes;
 * a route (t, j) with id = ids[t, j] is valid iff 0 <= id < E_g and

@@ -32,8 +32,7 @@ def probe():
     if not os.path.exists(PROBE):
         pytest.fail("tests/csrc/libb4probe.so missing: run __graft_entry__.build()")
     lib = ctypes.CDLL(PROBE)
-    for name in ("probe_mma_ts", "probe_mma_rowb", "probe_dequant", "probe_bf16_mul", "probe_tma", "probe_mma_sw128",
-                 "probe_mma_tput"):
+    for name in ("probe_mma_ts", "probe_mma_rowb", "probe_dequant", "probe_bf16_mul", "probe_tma", "probe_mma_sw128"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 

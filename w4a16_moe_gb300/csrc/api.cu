@@ -22,8 +22,9 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t st
 template <int MODE, int FMT>
 cudaError_t launch_gemm_wn(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int num_sms, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream);
-cudaError_t decode_occupancy(int fmt, int* blocks_per_sm);
+cudaError_t launch_decode_grouped(const DecodeParams& p, int fmt, int sets, int grid, cudaStream_t stream);
+cudaError_t decode_grouped_occupancy(int fmt, int sets, size_t smem, int* blocks_per_sm);
+size_t decode_grouped_smem(int fmt, int sets, int routes);
 cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream);
 size_t route_pack_smem_bytes(int num_local_experts);
@@ -67,7 +68,8 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int kDecodeAutoMaxM = 4;  // flashinfer PR #4255, Reviewer Notes: decode path up to m = 4
-constexpr int kMaxSplits = 8;
+constexpr int kDecodeW0 = 4;        // small-m partition: a stage costs kDecodeW0 + its route column sets
+constexpr size_t kDecodePrefetch = 48u << 20;  // FC2 weights prefetched into L2 at launch, whole grid
 
 int32_t next_pow2(int64_t n) {
   int64_t p = 1;
@@ -107,9 +109,17 @@ b4_status check_config(const b4_moe_config* cfg, int32_t act) {
 }
 
 // ------------------------------------------------------------- workspace
+// Common pieces (status word, route pack, chunk schedule), then one region
+// that the grouped path and the small-m path each lay out for themselves
+// (a call runs one of them): its size is the larger of the two.  Every size
+// depends on m only through T_cap, and monotonically.
 struct WsLayout {
-  size_t status, counts, offsets, sorted, chunks, chunk_count, h, acc, p, q, xp, total;
-  int t_cap, r_cap, max_chunks, inter_pad, wnat, dec_splits;
+  size_t status, counts, offsets, sorted, chunks, chunk_count;
+  size_t h, acc, xp;                     // grouped path
+  size_t dp, dq, dh, dcnt;               // small-m path
+  size_t total;
+  int t_cap, r_cap, max_chunks, inter_pad, wnat;
+  int dec_tcap, dec_rcap, dec_pmax;      // small-m path sizes (tokens capped at B4_DECODE_MAX_M)
   bool decode_ok;
 };
 
@@ -123,15 +133,11 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.inter_pad = round_up(cfg->inter, kBK);
   L.wnat = fc1_natural_width(act == B4_ACT_SILU_SWIGLU ? 0 : 1, L.inter_pad);
   L.decode_ok = L.t_cap <= B4_DECODE_MAX_M;
-  // decode partial buffers are sized for min(T_cap, B4_DECODE_MAX_M) tokens,
-  // which keeps the total monotone in T_cap
-  const int dec_rcap = (L.t_cap < B4_DECODE_MAX_M ? L.t_cap : B4_DECODE_MAX_M) * cfg->top_k;
-  int s = 256 / dec_rcap;
-  s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
-  // a decode unit covers at most 128 K stages, so long K needs that many splits
-  const int kst = cdiv(cfg->hidden > L.inter_pad ? cfg->hidden : L.inter_pad, kBK);
-  const int need = (kst + 127) / 128;
-  L.dec_splits = s > need ? s : need;
+  L.dec_tcap = L.t_cap < B4_DECODE_MAX_M ? L.t_cap : B4_DECODE_MAX_M;
+  L.dec_rcap = L.dec_tcap * cfg->top_k;
+  // at most this many CTAs share one tile of the small-m partition: fewer at
+  // larger capacity, so the partial buffers stay monotone and bounded
+  L.dec_pmax = L.dec_rcap <= 64 ? 8 : 4;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -144,15 +150,18 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.sorted = take(sizeof(int32_t) * L.r_cap);
   L.chunks = take(sizeof(int4) * L.max_chunks);
   L.chunk_count = take(sizeof(int32_t));
+  const size_t region = off;
   L.h = take(sizeof(uint16_t) * (size_t)L.r_cap * L.inter_pad);
   L.acc = take(sizeof(float) * (size_t)L.t_cap * cfg->hidden);
   L.xp = take(sizeof(uint16_t) * (size_t)L.r_cap * cfg->hidden);
-  // FC1 partials keep their splits innermost, padded to a power of two
-  int p_splits = 1;
-  while (p_splits < L.dec_splits) p_splits <<= 1;
-  L.p = take(sizeof(float) * (size_t)p_splits * dec_rcap * L.wnat);
-  L.q = take(sizeof(float) * (size_t)L.dec_splits * dec_rcap * cfg->hidden);
-  L.total = off;
+  const size_t grouped_end = off;
+  off = region;
+  const int nt1 = cdiv(L.wnat, kTileRows) + 1, nt2 = cdiv(cfg->hidden, kTileRows);
+  L.dp = take(sizeof(float) * (size_t)L.dec_rcap * L.wnat * L.dec_pmax);
+  L.dq = take(sizeof(float) * (size_t)L.dec_pmax * L.dec_rcap * cfg->hidden);
+  L.dh = take(sizeof(uint16_t) * (size_t)L.dec_rcap * L.inter_pad);
+  L.dcnt = take(sizeof(int32_t) * ((size_t)L.dec_rcap * (nt1 + nt2) + (size_t)L.dec_tcap * nt2));
+  L.total = off > grouped_end ? off : grouped_end;
   return L;
 }
 
@@ -188,43 +197,6 @@ b4_status device_info(DevInfo& info) {
   return B4_OK;
 }
 
-// Decode schedule: K splits of FC1 and FC2 and the grid.  CTAs take their
-// first unit statically and claim the rest in unit order, so load balance is
-// dynamic; the splits aim at about two units per CTA of each GEMM with at
-// least 12 (or 20, below) K stages per unit (a unit holds at most 128; FC1
-// needs at most 4 splits below 512 K stages).  The FC1 partials
-// are stored with a power-of-two split stride of at most max_splits rounded
-// up.
-struct DecodePlan {
-  int s1, s2, grid;
-};
-
-DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, int grid_cap, int max_splits) {
-  int stride_cap = 1;
-  while (stride_cap < max_splits) stride_cap <<= 1;
-  // When FC1 has at most half as many (route, tile) pairs as CTAs (m = 1 on
-  // the decode workload), units of >= 20 stages measured faster than >= 12:
-  // every unit adds about a microsecond of hand-over.
-  const int min_stages = 2LL * routes * g1.n_tiles <= grid_cap ? 20 : 12;
-  auto pick = [&](const TensorGeom& g, int cap) {
-    const long long base = (long long)routes * g.n_tiles;
-    int s = (int)((2LL * grid_cap + base - 1) / base);
-    const int most = g.k_stages / min_stages > 1 ? g.k_stages / min_stages : 1;
-    if (s > most) s = most;
-    if (s > cap) s = cap;
-    const int least = (g.k_stages + 127) / 128;
-    return s < least ? least : s;
-  };
-  DecodePlan plan;
-  // at most 4 FC1 splits: an FC2 unit sums that many partials per h element,
-  // and with a stride of 8 its loads take more round trips
-  plan.s1 = pick(g1, stride_cap < 4 ? stride_cap : 4);
-  plan.s2 = pick(g2, max_splits);
-  const long long U = (long long)routes * (g1.n_tiles * plan.s1 + g2.n_tiles * plan.s2);
-  plan.grid = (int)(U < grid_cap ? U : grid_cap);
-  return plan;
-}
-
 template <int MODE>
 cudaError_t launch_mode(int fmt, bool weights_on_n, const GemmParams& p, int grid, bool pdl, cudaStream_t st) {
   if (weights_on_n)
@@ -235,6 +207,35 @@ cudaError_t launch_mode(int fmt, bool weights_on_n, const GemmParams& p, int gri
 }  // namespace
 
 namespace b4 {
+// Raises the dynamic shared-memory limit of kernel `func` to `bytes` on the
+// current device.  The limit is a per-device setting, so it is set once per
+// (device, kernel) and raised again if a larger size is asked for; the table
+// is shared by every host thread under one lock.
+cudaError_t ensure_smem_limit(const void* func, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Entry {
+    int dev;
+    const void* func;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static Entry table[256];
+  static int used = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int i = 0;
+  for (; i < used; ++i)
+    if (table[i].dev == dev && table[i].func == func) break;
+  if (i < used && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  if (i < used) table[i].bytes = bytes;
+  else if (used < 256) table[used++] = Entry{dev, func, bytes};
+  return cudaSuccess;
+}
+
 // Sets the message b4_last_error returns on this thread (for entry points
 // defined in other translation units).
 void set_last_error(const char* fmt, ...) {
@@ -408,10 +409,11 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   cudaError_t e;
   if (decode) {
     const int R = cfg->m * cfg->top_k;
+    const int sets = R <= 8 ? 1 : 4;  // groups of at most 8 or 32 routes
+    const size_t smem = decode_grouped_smem(fmt, sets, R);
     int occ = 0;
-    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
-    if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
-    const DecodePlan plan = plan_decode(R, g1, g2, occ * dev.sms, L.dec_splits);
+    if ((e = decode_grouped_occupancy(fmt, sets, smem, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if (occ < 1) return fail(B4_ERR_CUDA, "the small-m kernel does not fit on an SM");
     DecodeParams dp{};
     dp.w1_codes = w13;
     dp.w1_scales = s13;
@@ -435,21 +437,21 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     dp.expert_map = cfg->expert_map;
     dp.x = x;
     dp.out = out;
-    dp.s1 = plan.s1;
-    dp.s2 = plan.s2;
-    dp.s1_stride = 1;
-    while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
-    dp.units1 = R * g1.n_tiles * plan.s1;
-    dp.units2 = R * g2.n_tiles * plan.s2;
-    dp.p = reinterpret_cast<float*>(ws + L.p);
-    dp.q = reinterpret_cast<float*>(ws + L.q);
-    dp.p_floats = (size_t)R * fc1_natural_width(act, L.inter_pad) * dp.s1_stride;
-    dp.ticket = reinterpret_cast<int*>(ws + L.status + 64);
-    dp.q_floats = (size_t)plan.s2 * R * cfg->hidden;
+    dp.p = reinterpret_cast<float*>(ws + L.dp);
+    dp.p_stride = L.dec_pmax;
+    dp.q = reinterpret_cast<float*>(ws + L.dq);
+    dp.q_pieces = L.dec_pmax;
+    dp.h = reinterpret_cast<uint16_t*>(ws + L.dh);
+    dp.hcount = reinterpret_cast<int*>(ws + L.dcnt);
+    dp.pcount = dp.hcount + (size_t)R * g1.n_tiles;
+    dp.ocount = dp.pcount + (size_t)R * g2.n_tiles;
+    dp.n_counters = (size_t)R * (g1.n_tiles + g2.n_tiles) + (size_t)cfg->m * g2.n_tiles;
+    dp.pmax = L.dec_pmax;
+    dp.w0 = kDecodeW0;
+    dp.l2_prefetch_bytes = (long long)(kDecodePrefetch / (size_t)dev.sms);
     dp.status = status;
-    dp.trace = g_trace;
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    if ((e = launch_decode(dp, fmt, plan.grid, s)) != cudaSuccess) return cuda_fail(e, "decode");
+    if ((e = launch_decode_grouped(dp, fmt, sets, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "decode");
     if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     return B4_OK;
   }
@@ -565,57 +567,43 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
   cudaError_t e;
 
   if (small) {
-    // The fused small-m kernel: K-split GEMV units, then one output unit per
-    // (token, 128 columns) that sums the split partials into out.
+    // The small-m kernel's FC1 phase alone: the routes are the tokens (every
+    // one to the single expert), and the last piece of each 128-column tile
+    // writes out.
+    const int sets = m <= 8 ? 1 : 4;
+    const size_t smem = decode_grouped_smem(fmt, sets, m);
     int occ = 0;
-    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
-    if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
-    // K splits: about two GEMV units per CTA, at least 8 stages each, at
-    // most the partial buffer's split count (summing up to 8 partials per
-    // output is cheap here: no activation row is built from them).
-    const int cap = occ * dev.sms;
-    const long long base = (long long)m * g1.n_tiles;
-    int s1 = (int)((2LL * cap + base - 1) / base);
-    const int most = g1.k_stages / 8 > 1 ? g1.k_stages / 8 : 1;
-    if (s1 > most) s1 = most;
-    if (s1 > L.dec_splits) s1 = L.dec_splits;
-    const int least = (g1.k_stages + 127) / 128;
-    if (s1 < least) s1 = least;
-    const DecodePlan plan{s1, 1, 0};
+    if ((e = decode_grouped_occupancy(fmt, sets, smem, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if (occ < 1) return fail(B4_ERR_CUDA, "the small-m kernel does not fit on an SM");
     DecodeParams dp{};
     dp.w1_codes = w;
     dp.w1_scales = sc;
     dp.gs1 = gs;
     dp.n_tiles1 = g1.n_tiles;
     dp.k_stages1 = g1.k_stages;
-    dp.n_tiles2 = g1.n_tiles;
-    dp.k_stages2 = 1;
     dp.m = m;
     dp.top_k = 1;
     dp.num_global_experts = 1;
     dp.num_local_experts = 1;
     dp.hidden = K;
     dp.inter_pad = L.inter_pad;
-    dp.act = 1;  // the non-gated FC1 partial layout; no activation is applied
-    dp.linear = 1;
+    dp.act = 2;
     dp.n_out = N;
     dp.x = x;
     dp.out = out;
-    dp.s1 = plan.s1;
-    dp.s2 = 1;
-    dp.s1_stride = 1;
-    while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
-    dp.units1 = m * g1.n_tiles * plan.s1;
-    dp.units2 = m * g1.n_tiles;
-    dp.p = reinterpret_cast<float*>(ws + L.p);
-    dp.p_floats = (size_t)m * L.inter_pad * dp.s1_stride;
-    dp.ticket = reinterpret_cast<int*>(ws + L.status + 64);
+    dp.p = reinterpret_cast<float*>(ws + L.dp);
+    dp.p_stride = L.dec_pmax;
+    dp.q_pieces = L.dec_pmax;
+    dp.hcount = reinterpret_cast<int*>(ws + L.dcnt);
+    dp.pcount = dp.hcount + (size_t)m * g1.n_tiles;
+    dp.ocount = dp.pcount;
+    dp.n_counters = (size_t)m * g1.n_tiles;
+    dp.pmax = L.dec_pmax;
+    dp.w0 = kDecodeW0;
     dp.status = status;
-    dp.trace = g_trace;
-    const long long U = (long long)dp.units1 + dp.units2;
-    const int grid = (int)(U < cap ? U : cap);
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-    if ((e = launch_decode(dp, fmt, grid, s)) != cudaSuccess) return cuda_fail(e, "linear (fused small-m)");
+    if ((e = launch_decode_grouped(dp, fmt, sets, dev.sms, s)) != cudaSuccess)
+      return cuda_fail(e, "linear (fused small-m)");
     if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     return B4_OK;
   }

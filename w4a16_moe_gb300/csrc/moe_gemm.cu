@@ -46,6 +46,8 @@
 
 namespace b4 {
 
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
+
 constexpr int kNumA = 6;                 // A slots (K stages) held in tensor memory
 constexpr int kThreads = 512;
 constexpr int kAColsPerSlot = kBK / 2;   // 32 columns of packed bf16 pairs
@@ -503,12 +505,8 @@ template <int MODE, int FMT>
 cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream) {
   auto kern = moe_gemm_kernel<MODE, FMT>;
   const size_t smem = SmemLayout<FMT>::total;
-  static bool configured = false;  // attribute set once per process (idempotent)
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

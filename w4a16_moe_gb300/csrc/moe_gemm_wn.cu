@@ -47,6 +47,8 @@
 #include "tma.cuh"
 
 namespace b4 {
+
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 namespace wn {
 
 constexpr int kThreads = 768;
@@ -487,12 +489,8 @@ cudaError_t launch_gemm_wn(const GemmParams& p, int grid, bool pdl, cudaStream_t
   using namespace wn;
   auto kern = wn::moe_gemm_kernel<MODE, FMT>;
   const size_t smem = wn::SmemLayout<FMT>::total;
-  static bool configured = false;  // attribute set once per process (idempotent)
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

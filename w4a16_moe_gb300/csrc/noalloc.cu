@@ -12,6 +12,7 @@
 // library's device code onto a GPU, and the array stays there until the
 // process exits.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -24,17 +25,44 @@ void set_last_error(const char* fmt, ...);
 
 // The scratch array.  In host code this name is only a host-side stand-in for
 // the symbol, never a device address: the address a kernel may use comes from
-// cudaGetSymbolAddress, per device, below.
+// cudaGetSymbolAddress, per device and context, below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[B4_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
+// Driver entry points for the identity of the current context, fetched through
+// the runtime (the library links no libcuda).  cuCtxGetId gives every context
+// a process-unique id, so a context that replaced an earlier one (after a
+// cudaDeviceReset, or a teardown and re-creation of the primary context) has
+// a new id even where the driver reuses the old handle.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<F>(p);
+  return nullptr;
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct Cached {
+  unsigned long long ctx_id;
+  void* addr;
+};
+Cached g_cache[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device; looked up on the
-// first call per device (which may load this library's device code there).
+// Device address of g_noalloc_scratch in the context now current on this
+// device.  Set-up: the first call in each context (per device) looks the
+// address up with cudaGetSymbolAddress, which allocates nothing but may load
+// this library's device code into that context; later calls in the same
+// context reuse it.  A new context (after cudaDeviceReset or a primary-context
+// teardown) has a new id, so its first call looks the address up again and a
+// stale address is never passed to a kernel.
 b4_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -42,23 +70,29 @@ b4_status scratch_address(void** out) {
     b4::set_last_error("b4_fused_moe_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(e));
     return B4_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    b4::set_last_error("b4_fused_moe_noalloc: device ordinal %d is beyond the %d this library tracks", dev,
-                       kMaxDevices);
-    return B4_ERR_UNSUPPORTED_DEVICE;
-  }
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  auto current_id = [&](unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    return dev >= 0 && dev < kMaxDevices && get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+           get_id(ctx, id) == CUDA_SUCCESS;
+  };
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      b4::set_last_error("b4_fused_moe_noalloc: cudaGetSymbolAddress of the static scratch failed on device %d: %s",
-                         dev, cudaGetErrorString(e));
-      return B4_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  if (current_id(&id) && g_cache[dev].addr && g_cache[dev].ctx_id == id) {
+    *out = g_cache[dev].addr;
+    return B4_OK;
   }
-  *out = g_scratch_addr[dev];
+  // (the lookup also binds the device's primary context when none is current yet)
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    b4::set_last_error("b4_fused_moe_noalloc: cudaGetSymbolAddress of the static scratch failed on device %d: %s",
+                       dev, cudaGetErrorString(e));
+    return B4_ERR_CUDA;
+  }
+  if (current_id(&id)) g_cache[dev] = Cached{id, p};  // without a context id, look up on every call
+  *out = p;
   return B4_OK;
 }
 

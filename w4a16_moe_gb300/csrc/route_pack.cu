@@ -24,6 +24,8 @@
 
 namespace b4 {
 
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
+
 constexpr int kPackThreads = 512;
 constexpr int kPackWarps = kPackThreads / 32;
 constexpr int kBatch = 8;  // 32-route groups whose keys a warp loads before using any
@@ -172,12 +174,8 @@ size_t route_pack_smem_bytes(int num_local_experts) {
 
 cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream) {
   const size_t smem = route_pack_smem_bytes(p.num_local_experts);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(route_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(route_pack_kernel), smem);
+  if (e != cudaSuccess) return e;
   int grid = p.num_local_experts < 2 * num_sms ? p.num_local_experts : 2 * num_sms;
   if (grid < 1) grid = 1;
   route_pack_kernel<<<grid, kPackThreads, smem, stream>>>(p);
