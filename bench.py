@@ -164,7 +164,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm
 class Bench:
-    def __init__(self, wl, m, seed=7):
+    def __init__(self, wl, m, seed=7, path=None):
         import torch
 
         import w4a16_moe_gb300 as b4
@@ -175,8 +175,9 @@ class Bench:
         self.act = b4.ACTIVATIONS[wl.act]
         self.em_np = W.expert_map(wl)
         em = None if self.em_np is None else torch.from_numpy(self.em_np).cuda()
+        self.path = b4.PATH_AUTO if path is None else path
         self.cfg = b4.MoEConfig(m, wl.top_k, wl.num_global_experts, wl.num_local_experts, wl.hidden, wl.inter,
-                                format=b4.FORMATS[wl.fmt], expert_map=em)
+                                format=b4.FORMATS[wl.fmt], path=self.path, expert_map=em)
         self.host = {}
         dev = {}
         for which, name in ((0, "13"), (1, "2")):
@@ -201,7 +202,8 @@ class Bench:
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         self.flush_sink = torch.empty(1, dtype=torch.int32, device="cuda")
         self.stream = torch.cuda.Stream()
-        self.decode = m <= 4
+        # the library's AUTO rule: a small-m kernel (one cooperative launch) up to m = 16
+        self.decode = self.path == b4.PATH_DECODE or (self.path == b4.PATH_AUTO and m <= 16)
         self.n_kernels = 1 if self.decode else 4  # timed intervals: decode kernel; pack, permute + FC1, FC2, finalize
         self.launches = 1 if self.decode else 5  # this library's kernels per call
 

@@ -66,9 +66,13 @@ typedef enum b4_format { B4_NVFP4_E4M3_K16 = 0, B4_MXFP4_E8M0_K32 = 1 } b4_forma
  * RELU2:       W1 has inter rows; h = max(a, 0)^2. */
 typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activation;
 
-/* Execution path of b4_fused_moe.  AUTO takes the decode path for m <= 4
- * (the cap flashinfer PR #4255, Reviewer Notes, chose) and the route-packed
- * grouped path otherwise.  DECODE is accepted for m <= B4_DECODE_MAX_M. */
+/* Execution path of b4_fused_moe.  DECODE is the small-m path (accepted for
+ * m <= B4_DECODE_MAX_M): one cooperative launch, a per-route kernel for
+ * m <= 4 and a route-grouped kernel (an expert's weights streamed once per
+ * group of up to 16 of its routes) above.  GROUPED is the route-packed
+ * tcgen05 path.  AUTO takes DECODE for m <= 16 and GROUPED above: the
+ * crossover flashinfer PR #4255 (Reviewer Notes) leaves to each card, as
+ * measured on GB300; b4_linear's AUTO takes its small-m kernel for m <= 4. */
 typedef enum b4_path { B4_PATH_AUTO = 0, B4_PATH_DECODE = 1, B4_PATH_GROUPED = 2 } b4_path;
 
 #define B4_DECODE_MAX_M 64
@@ -163,10 +167,12 @@ b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32
  * FC1 accumulates gs13 * (x . w13) in fp32, applies the activation in fp32 and
  * rounds h to bf16; FC2 accumulates in fp32, multiplies by gs2 and the router
  * weight and sums the routes of a token in fp32 before one bf16 rounding.
- * Enqueues 1 (decode: one cooperative launch, grid no larger than the
- * resident CTA count) or 5 (grouped: route pack, x permutation, FC1, FC2,
- * finalize, chained by programmatic dependent launch) launches on `stream`;
- * no allocation, no synchronisation. */
+ * Enqueues 1 (the small-m path: one cooperative launch of one CTA per SM
+ * for m > 4, grid no larger than the resident CTA count for m <= 4) or 5
+ * (grouped: route pack, x permutation, FC1, FC2, finalize, chained by
+ * programmatic dependent launch) launches on `stream`; no allocation, no
+ * synchronisation.  The small-m path's output is bitwise reproducible (every
+ * sum in a fixed order); the grouped path's top-k sum uses fp32 atomics. */
 b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
                        const float* gs13, const uint8_t* w2, const uint8_t* s2, const float* gs2,
                        const int32_t* topk_ids, const float* topk_weights, int32_t activation, uint16_t* out,
@@ -187,18 +193,20 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
 b4_status b4_set_timing_events(void* const* events, int32_t n);
 
 /* Optional kernel timeline for profiling: while `device_buffer` is set
- * (>= 163840 bytes = [10][2048] int64, or NULL to turn it off), the kernels
+ * (>= 262144 bytes = [16][2048] int64, or NULL to turn it off), the kernels
  * of each b4_fused_moe / b4_linear call on this thread write timestamps into
- * it.  Grouped path: clock64() of CTA 0 as [5][2048] per GEMM, indexed by the
- * CTA's running counters, FC1 at int64 offset 0 and FC2 at 10240; kinds:
- * weight stage issued, A stage written to tensor memory (weights on M) or B
- * stage dequantised (weights on N), MMA stage issued, activation stage
- * ready, unit epilogue done.  Decode path (one kernel): kinds 0-4 are
- * clock64() of CTA 0 -- weight slot issued, weight slot consumed, kernel
- * start (index 0), activation row ready, unit done; kinds 5-9 are
- * %globaltimer nanoseconds indexed by CTA -- CTA start, last FC2 partial
- * stored, last FC1 partial stored, compute warps done, output warp done.
- * Entries not reached are left untouched. */
+ * it.  Grouped path (built with B4_TRACE defined only; otherwise nothing is
+ * written): clock64() of CTA 0 as [5][2048] per GEMM, indexed by the CTA's
+ * running counters, FC1 at int64 offset 0 and FC2 at 10240; kinds: weight
+ * stage issued, A stage written to tensor memory (weights on M) or B stage
+ * dequantised (weights on N), MMA stage issued, activation stage ready, unit
+ * epilogue done.  Small-m path (one kernel): %globaltimer nanoseconds of each
+ * CTA at phase boundaries, entry [kind][CTA]: 0 start, 1 group table built,
+ * 2 first unit published, 3 first weight copy issued, 4 first slot
+ * computed, 5 last FC1 unit stored, 6 first FC2 slot computed, 7 compute
+ * done, 8 epilogue done, 9 first FC2 unit's FC1 tiles ready, 10 grid
+ * barrier seen, 11 weight stream done, 12 last FC1 tile's h built, 13 last
+ * output row written.  Entries not reached are left untouched. */
 b4_status b4_set_trace(void* device_buffer, size_t bytes);
 
 /* Synchronises `stream`, then reads the device status word of `workspace`

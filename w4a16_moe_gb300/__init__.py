@@ -321,7 +321,7 @@ def set_timing_events(events):
 
 
 def set_trace(buffer):
-    """Kernel timeline (see b4_set_trace): an int64 CUDA tensor of >= 20480 entries, or None."""
+    """Kernel timeline (see b4_set_trace): an int64 CUDA tensor of >= 32768 entries, or None."""
     if buffer is None:
         _check(_lib.b4_set_trace(None, 0))
     else:

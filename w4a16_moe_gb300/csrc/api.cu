@@ -22,7 +22,9 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t st
 template <int MODE, int FMT>
 cudaError_t launch_gemm_wn(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int num_sms, cudaStream_t stream);
-cudaError_t launch_decode_grouped(const DecodeParams& p, int fmt, int sets, int grid, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream);
+cudaError_t decode_occupancy(int fmt, int* blocks_per_sm);
+cudaError_t launch_decode_grouped(const SmallGroupParams& p, int fmt, int sets, int grid, cudaStream_t stream);
 cudaError_t decode_grouped_occupancy(int fmt, int sets, size_t smem, int* blocks_per_sm);
 size_t decode_grouped_smem(int fmt, int sets, int routes);
 cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream);
@@ -67,9 +69,18 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
   return fail(B4_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr int kDecodeAutoMaxM = 4;  // flashinfer PR #4255, Reviewer Notes: decode path up to m = 4
+// Path choice.  flashinfer PR #4255 (Reviewer Notes) caps its decode path at
+// m = 4 and notes that the crossover varies by card; on GB300 the small-m
+// kernels were measured against the grouped tcgen05 GEMMs (one call, L2
+// cold): the per-route decode kernel is fastest up to m = 4, the route-grouped
+// kernel from m = 8 to 16 (decode E128 k8 m = 8: 178 vs 213 us; small-batch
+// E64 k6 m = 16: 97 vs 101 us), the grouped GEMMs from m = 32 (small-batch
+// m = 32: 133 vs 141 us).
+constexpr int kDecodeAutoMaxM = 16;  // AUTO takes a small-m kernel up to here
+constexpr int kPerRouteMaxM = 4;     // the small-m path's per-route kernel up to here, route-grouped above
+constexpr int kLinearSmallMaxM = 4;  // b4_linear's AUTO takes the small-m kernel up to here
 constexpr int kDecodeW0 = 4;        // small-m partition: a stage costs kDecodeW0 + its route column sets
-constexpr size_t kDecodePrefetch = 48u << 20;  // FC2 weights prefetched into L2 at launch, whole grid
+constexpr int kMaxSplits = 8;
 
 int32_t next_pow2(int64_t n) {
   int64_t p = 1;
@@ -116,10 +127,12 @@ b4_status check_config(const b4_moe_config* cfg, int32_t act) {
 struct WsLayout {
   size_t status, counts, offsets, sorted, chunks, chunk_count;
   size_t h, acc, xp;                     // grouped path
-  size_t dp, dq, dh, dcnt;               // small-m path
+  size_t dp, dq, dh, dcnt;               // route-grouped small-m path
+  size_t op, oq;                         // per-route decode path
   size_t total;
   int t_cap, r_cap, max_chunks, inter_pad, wnat;
   int dec_tcap, dec_rcap, dec_pmax;      // small-m path sizes (tokens capped at B4_DECODE_MAX_M)
+  int dec_splits;                        // per-route decode path: most K splits
   bool decode_ok;
 };
 
@@ -156,12 +169,27 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.xp = take(sizeof(uint16_t) * (size_t)L.r_cap * cfg->hidden);
   const size_t grouped_end = off;
   off = region;
-  const int nt1 = cdiv(L.wnat, kTileRows) + 1, nt2 = cdiv(cfg->hidden, kTileRows);
+  const int nt1 = cdiv(L.wnat, kTileRows) + 1;
   L.dp = take(sizeof(float) * (size_t)L.dec_rcap * L.wnat * L.dec_pmax);
   L.dq = take(sizeof(float) * (size_t)L.dec_pmax * L.dec_rcap * cfg->hidden);
   L.dh = take(sizeof(uint16_t) * (size_t)L.dec_rcap * L.inter_pad);
-  L.dcnt = take(sizeof(int32_t) * ((size_t)L.dec_rcap * (nt1 + nt2) + (size_t)L.dec_tcap * nt2));
-  L.total = off > grouped_end ? off : grouped_end;
+  L.dcnt = take(sizeof(int32_t) * (size_t)L.dec_rcap * nt1);
+  const size_t small_end = off;
+  // per-route decode path: K splits of about 256 units over the routes (a
+  // unit covers at most 128 K stages), FC1 partials with the splits
+  // innermost padded to a power of two, FC2 partials per split
+  off = region;
+  int sp = 256 / L.dec_rcap;
+  sp = sp < 1 ? 1 : (sp > kMaxSplits ? kMaxSplits : sp);
+  const int kst = cdiv(cfg->hidden > L.inter_pad ? cfg->hidden : L.inter_pad, kBK);
+  const int need = (kst + 127) / 128;
+  L.dec_splits = sp > need ? sp : need;
+  int p_splits = 1;
+  while (p_splits < L.dec_splits) p_splits <<= 1;
+  L.op = take(sizeof(float) * (size_t)p_splits * L.dec_rcap * L.wnat);
+  L.oq = take(sizeof(float) * (size_t)L.dec_splits * L.dec_rcap * cfg->hidden);
+  size_t end = off > grouped_end ? off : grouped_end;
+  L.total = end > small_end ? end : small_end;
   return L;
 }
 
@@ -195,6 +223,43 @@ b4_status device_info(DevInfo& info) {
   }
   if (!info.ok) return fail(B4_ERR_UNSUPPORTED_DEVICE, "device is not sm_103 (GB300); no fallback path exists");
   return B4_OK;
+}
+
+// Decode schedule: K splits of FC1 and FC2 and the grid.  CTAs take their
+// first unit statically and claim the rest in unit order, so load balance is
+// dynamic; the splits aim at about two units per CTA of each GEMM with at
+// least 12 (or 20, below) K stages per unit (a unit holds at most 128; FC1
+// needs at most 4 splits below 512 K stages).  The FC1 partials
+// are stored with a power-of-two split stride of at most max_splits rounded
+// up.
+struct DecodePlan {
+  int s1, s2, grid;
+};
+
+DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, int grid_cap, int max_splits) {
+  int stride_cap = 1;
+  while (stride_cap < max_splits) stride_cap <<= 1;
+  // When FC1 has at most half as many (route, tile) pairs as CTAs (m = 1 on
+  // the decode workload), units of >= 20 stages measured faster than >= 12:
+  // every unit adds about a microsecond of hand-over.
+  const int min_stages = 2LL * routes * g1.n_tiles <= grid_cap ? 20 : 12;
+  auto pick = [&](const TensorGeom& g, int cap) {
+    const long long base = (long long)routes * g.n_tiles;
+    int s = (int)((2LL * grid_cap + base - 1) / base);
+    const int most = g.k_stages / min_stages > 1 ? g.k_stages / min_stages : 1;
+    if (s > most) s = most;
+    if (s > cap) s = cap;
+    const int least = (g.k_stages + 127) / 128;
+    return s < least ? least : s;
+  };
+  DecodePlan plan;
+  // at most 4 FC1 splits: an FC2 unit sums that many partials per h element,
+  // and with a stride of 8 its loads take more round trips
+  plan.s1 = pick(g1, stride_cap < 4 ? stride_cap : 4);
+  plan.s2 = pick(g2, max_splits);
+  const long long U = (long long)routes * (g1.n_tiles * plan.s1 + g2.n_tiles * plan.s2);
+  plan.grid = (int)(U < grid_cap ? U : grid_cap);
+  return plan;
 }
 
 template <int MODE>
@@ -407,14 +472,64 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   fp.out = out;
 
   cudaError_t e;
-  if (decode) {
+  if (decode && cfg->m <= kPerRouteMaxM) {
+    // the per-route kernel: one unit per (route, tile, K split)
     const int R = cfg->m * cfg->top_k;
-    const int sets = R <= 8 ? 1 : 4;  // groups of at most 8 or 32 routes
+    int occ = 0;
+    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
+    const DecodePlan plan = plan_decode(R, g1, g2, occ * dev.sms, L.dec_splits);
+    DecodeParams dp{};
+    dp.w1_codes = w13;
+    dp.w1_scales = s13;
+    dp.gs1 = gs13;
+    dp.w2_codes = w2;
+    dp.w2_scales = s2;
+    dp.gs2 = gs2;
+    dp.n_tiles1 = g1.n_tiles;
+    dp.k_stages1 = g1.k_stages;
+    dp.n_tiles2 = g2.n_tiles;
+    dp.k_stages2 = g2.k_stages;
+    dp.m = cfg->m;
+    dp.top_k = cfg->top_k;
+    dp.num_global_experts = cfg->num_global_experts;
+    dp.num_local_experts = cfg->num_local_experts;
+    dp.hidden = cfg->hidden;
+    dp.inter_pad = L.inter_pad;
+    dp.act = act;
+    dp.topk_ids = topk_ids;
+    dp.topk_weights = topk_weights;
+    dp.expert_map = cfg->expert_map;
+    dp.x = x;
+    dp.out = out;
+    dp.s1 = plan.s1;
+    dp.s2 = plan.s2;
+    dp.s1_stride = 1;
+    while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
+    dp.units1 = R * g1.n_tiles * plan.s1;
+    dp.units2 = R * g2.n_tiles * plan.s2;
+    dp.p = reinterpret_cast<float*>(ws + L.op);
+    dp.q = reinterpret_cast<float*>(ws + L.oq);
+    dp.p_floats = (size_t)R * fc1_natural_width(act, L.inter_pad) * dp.s1_stride;
+    dp.ticket = reinterpret_cast<int*>(ws + L.status + 64);
+    dp.q_floats = (size_t)plan.s2 * R * cfg->hidden;
+    dp.status = status;
+    dp.trace = g_trace;
+    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    if ((e = launch_decode(dp, fmt, plan.grid, s)) != cudaSuccess) return cuda_fail(e, "decode");
+    if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    return B4_OK;
+  }
+
+  if (decode) {
+    // the route-grouped kernel: an expert's weights stream once per group of routes
+    const int R = cfg->m * cfg->top_k;
+    const int sets = R <= 8 ? 1 : 2;  // groups of at most 8 or 16 routes
     const size_t smem = decode_grouped_smem(fmt, sets, R);
     int occ = 0;
     if ((e = decode_grouped_occupancy(fmt, sets, smem, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
     if (occ < 1) return fail(B4_ERR_CUDA, "the small-m kernel does not fit on an SM");
-    DecodeParams dp{};
+    SmallGroupParams dp{};
     dp.w1_codes = w13;
     dp.w1_scales = s13;
     dp.gs1 = gs13;
@@ -441,15 +556,15 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     dp.p_stride = L.dec_pmax;
     dp.q = reinterpret_cast<float*>(ws + L.dq);
     dp.q_pieces = L.dec_pmax;
+    dp.p_floats = (size_t)R * L.wnat * L.dec_pmax;
+    dp.q_floats = (size_t)L.dec_pmax * R * cfg->hidden;
     dp.h = reinterpret_cast<uint16_t*>(ws + L.dh);
-    dp.hcount = reinterpret_cast<int*>(ws + L.dcnt);
-    dp.pcount = dp.hcount + (size_t)R * g1.n_tiles;
-    dp.ocount = dp.pcount + (size_t)R * g2.n_tiles;
-    dp.n_counters = (size_t)R * (g1.n_tiles + g2.n_tiles) + (size_t)cfg->m * g2.n_tiles;
+    dp.hflag = reinterpret_cast<int*>(ws + L.dcnt);
+    dp.n_flags = (size_t)R * g1.n_tiles;
     dp.pmax = L.dec_pmax;
     dp.w0 = kDecodeW0;
-    dp.l2_prefetch_bytes = (long long)(kDecodePrefetch / (size_t)dev.sms);
     dp.status = status;
+    dp.trace = g_trace;
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     if ((e = launch_decode_grouped(dp, fmt, sets, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "decode");
     if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
@@ -558,7 +673,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
 
   const int fmt = cfg->format;
   const int m = cfg->m, N = cfg->inter, K = cfg->hidden;
-  bool small = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && m <= kDecodeAutoMaxM);
+  bool small = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && m <= kLinearSmallMaxM);
   if (small && !L.decode_ok) small = false;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
@@ -566,16 +681,72 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
   const TensorGeom g1 = tensor_geom(0, 1, K, N);
   cudaError_t e;
 
+  if (small && m <= kPerRouteMaxM) {
+    // The fused small-m kernel: K-split GEMV units, then one output unit per
+    // (token, 128 columns) that sums the split partials into out.
+    int occ = 0;
+    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
+    // K splits: about two GEMV units per CTA, at least 8 stages each, at
+    // most the partial buffer's split count (summing up to 8 partials per
+    // output is cheap here: no activation row is built from them).
+    const int cap = occ * dev.sms;
+    const long long base = (long long)m * g1.n_tiles;
+    int s1 = (int)((2LL * cap + base - 1) / base);
+    const int most = g1.k_stages / 8 > 1 ? g1.k_stages / 8 : 1;
+    if (s1 > most) s1 = most;
+    if (s1 > L.dec_splits) s1 = L.dec_splits;
+    const int least = (g1.k_stages + 127) / 128;
+    if (s1 < least) s1 = least;
+    const DecodePlan plan{s1, 1, 0};
+    DecodeParams dp{};
+    dp.w1_codes = w;
+    dp.w1_scales = sc;
+    dp.gs1 = gs;
+    dp.n_tiles1 = g1.n_tiles;
+    dp.k_stages1 = g1.k_stages;
+    dp.n_tiles2 = g1.n_tiles;
+    dp.k_stages2 = 1;
+    dp.m = m;
+    dp.top_k = 1;
+    dp.num_global_experts = 1;
+    dp.num_local_experts = 1;
+    dp.hidden = K;
+    dp.inter_pad = L.inter_pad;
+    dp.act = 1;  // the non-gated FC1 partial layout; no activation is applied
+    dp.linear = 1;
+    dp.n_out = N;
+    dp.x = x;
+    dp.out = out;
+    dp.s1 = plan.s1;
+    dp.s2 = 1;
+    dp.s1_stride = 1;
+    while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
+    dp.units1 = m * g1.n_tiles * plan.s1;
+    dp.units2 = m * g1.n_tiles;
+    dp.p = reinterpret_cast<float*>(ws + L.op);
+    dp.p_floats = (size_t)m * L.inter_pad * dp.s1_stride;
+    dp.ticket = reinterpret_cast<int*>(ws + L.status + 64);
+    dp.status = status;
+    dp.trace = g_trace;
+    const long long U = (long long)dp.units1 + dp.units2;
+    const int grid = (int)(U < cap ? U : cap);
+    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    if ((e = launch_decode(dp, fmt, grid, s)) != cudaSuccess) return cuda_fail(e, "linear (fused small-m)");
+    if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
+    return B4_OK;
+  }
+
   if (small) {
     // The small-m kernel's FC1 phase alone: the routes are the tokens (every
     // one to the single expert), and the last piece of each 128-column tile
     // writes out.
-    const int sets = m <= 8 ? 1 : 4;
+    const int sets = m <= 8 ? 1 : 2;
     const size_t smem = decode_grouped_smem(fmt, sets, m);
     int occ = 0;
     if ((e = decode_grouped_occupancy(fmt, sets, smem, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
     if (occ < 1) return fail(B4_ERR_CUDA, "the small-m kernel does not fit on an SM");
-    DecodeParams dp{};
+    SmallGroupParams dp{};
     dp.w1_codes = w;
     dp.w1_scales = sc;
     dp.gs1 = gs;
@@ -594,13 +765,13 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
     dp.p = reinterpret_cast<float*>(ws + L.dp);
     dp.p_stride = L.dec_pmax;
     dp.q_pieces = L.dec_pmax;
-    dp.hcount = reinterpret_cast<int*>(ws + L.dcnt);
-    dp.pcount = dp.hcount + (size_t)m * g1.n_tiles;
-    dp.ocount = dp.pcount;
-    dp.n_counters = (size_t)m * g1.n_tiles;
+    dp.p_floats = (size_t)m * L.wnat * L.dec_pmax;
+    dp.hflag = reinterpret_cast<int*>(ws + L.dcnt);
+    dp.n_flags = 0;
     dp.pmax = L.dec_pmax;
     dp.w0 = kDecodeW0;
     dp.status = status;
+    dp.trace = g_trace;
     if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
     if ((e = launch_decode_grouped(dp, fmt, sets, dev.sms, s)) != cudaSuccess)
       return cuda_fail(e, "linear (fused small-m)");
@@ -720,8 +891,8 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
 }
 
 b4_status b4_set_trace(void* device_buffer, size_t bytes) {
-  if (device_buffer && bytes < 10 * kTraceLen * sizeof(long long))
-    return fail(B4_ERR_INVALID_ARGUMENT, "trace buffer needs %zu bytes", 10 * kTraceLen * sizeof(long long));
+  if (device_buffer && bytes < 16 * kTraceLen * sizeof(long long))
+    return fail(B4_ERR_INVALID_ARGUMENT, "trace buffer needs %zu bytes", 16 * kTraceLen * sizeof(long long));
   g_trace = static_cast<long long*>(device_buffer);
   return B4_OK;
 }

@@ -1,0 +1,795 @@
+// Small-m decode path of the fused W4A16 MoE layer (flashinfer PR #4255,
+// Description: "A tensor-core decode path for small batches on the packed
+// serving weights"): ONE cooperative persistent kernel for FC1, the
+// activation, FC2 and the top-k combine.
+//
+// With one route per work unit both GEMMs are matrix-vector products over the
+// expert's weights: HBM-bound at 4 bits per weight.  The kernel is built so
+// the weight stream runs from launch to exit and nothing on the path between
+// FC1 and FC2 waits for a memory fence.
+//
+// Work units, in this order: FC1 units (route, 128-row tile, K split), then FC2
+// units (route, 128-row tile of H, K split).  CTA b takes units b, b + G, ...,
+// in increasing order.
+//
+//   warp 0        streams the unit's packed codes and scales, two 64-wide K
+//                 stages per slot of a 4-slot shared-memory ring; weights
+//                 depend on nothing, so the next unit's stream (FC2 included)
+//                 starts while this one computes.
+//   warp 1        resolves each unit once (expert, scale factors, the token's
+//                 valid top-k slots) and passes it to the compute warps with
+//                 the FC1 x slice (one bulk copy).
+//   warps 2..9    16 weight rows each: register dequantisation (E2M1 table
+//                 lookup by PRMT, one bf16x2 multiply by the block scale)
+//                 feeding warp-level m16n8k16 bf16 MMAs, fp32 accumulation;
+//                 each unit ends with an fp32 split partial store.  An FC2
+//                 unit first builds its h slice, act(sum of the FC1 partials)
+//                 in bf16.
+//   warp 10       stores the bf16 output of a token's 128-column tile: it sums
+//                 the FC2 partials of the token's valid routes (ascending
+//                 top-k slot, then split) for the tile's last unit in unit
+//                 order.  Fixed orders: the output is bitwise reproducible.
+//
+// Hand-offs between CTAs without counters or fences: before one grid barrier
+// at launch, the CTAs fill both partial buffers with a signalling-NaN bit
+// pattern that no arithmetic produces; a reader polls the values it needs
+// until none of them holds the marker (a 4-byte store is seen whole or not at
+// all).  The barrier is split: a CTA arrives as soon as its share of the fill
+// is done, and only its first partial store or read waits for the other
+// CTAs, so the first unit's weight stream and arithmetic run meanwhile.  A reader only ever waits for units earlier in unit order, each CTA
+// runs its units in order, and a cooperative launch keeps every CTA resident,
+// so every wait ends; every wait is bounded as well.  Before the barrier the
+// CTAs also clear the status word and zero the output rows of tokens without
+// a valid route.
+//
+// The dense W4A16 linear layer (one weight matrix, top-1, no activation, no
+// FC2) runs in the same kernel: its FC1 units are the layer's K-split GEMV
+// units, and each "FC2" unit is an output tile (token, 128 columns) that sums
+// the FC1 split partials straight into out; those units stream no weights.
+//
+// Why warp-level MMAs and not tcgen05 here: the register dequantiser feeds
+// m16n8k16 fragments directly, while a tcgen05.mma reads its weight operand
+// from shared or tensor memory, so every dequantised weight would make a
+// round trip there first; with one token per unit the MMA work is tiny either
+// way, which leaves the dequantiser's integer work as the limit: per code word (8 weights) two LOP3 and three
+// shifts, per weight pair a PRMT and a bf16x2 multiply, all on the SM's
+// half-rate integer/bf16 pipe (measured: 2 warp-instructions per clock per SM
+// for each of them, 1 for a multiply-high), which caps the stage arithmetic
+// near 4.7 TB/s at two CTAs per SM.
+//
+// K order inside an MMA: thread t of a quad owns physical 16-element block t
+// of the 64-wide stage (one NVFP4 scale block); MMA j takes its pairs 2j and
+// 2j+1 as the fragment's logical K pairs t and t + 4.  Weights and
+// activations use the same permutation, so every dot product is unchanged.
+// The activation is replicated into all eight B columns, so every thread
+// holds its two rows' results.
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "decode_stage.cuh"
+#include "dequant.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace b4 {
+
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
+
+namespace cg = cooperative_groups;
+
+constexpr int kDThreads = 352;        // weights, schedule, 8 compute warps, output
+constexpr int kDComputeWarps = 8;
+constexpr int kDSlots = 4;            // weight ring slots
+constexpr int kDSlotStages = 2;       // 64-wide K stages per slot
+constexpr int kDMaxStages = 128;      // K stages of one unit (its activation row is in shared memory)
+constexpr int kDRowBytes = kDMaxStages * kBK * 2;
+constexpr float kDTwo63 = 9.223372036854775808e18f;
+constexpr uint32_t kNotWritten = 0x7F800001u;  // signalling NaN: never an arithmetic result
+
+template <int FMT>
+struct DSmem {
+  static constexpr int kScaleStage = scale_bytes_per_stage(FMT);
+  static constexpr size_t codes = 0;
+  static constexpr size_t scales = (size_t)kDSlots * kDSlotStages * kCodeBytesPerStage;
+  static constexpr size_t rows = scales + (size_t)kDSlots * kDSlotStages * kScaleStage;
+  static constexpr size_t bars = rows + 2 * (size_t)kDRowBytes;
+  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 12);  // 11 barrier pairs used, one spare
+  static constexpr size_t desc = misc + 16;
+  static constexpr size_t total = desc + 4 * 16;  // four 16-byte unit descriptors
+};
+
+__device__ __forceinline__ int d_local_expert(const DecodeParams& p, int route) {
+  if (!p.topk_ids) return 0;  // dense linear layer: one expert, every route valid
+  const int id = __ldg(p.topk_ids + route);
+  if (id < 0 || id >= p.num_global_experts) return -1;
+  const int l = p.expert_map ? __ldg(p.expert_map + id) : id;
+  return (l >= 0 && l < p.num_local_experts) ? l : -1;
+}
+
+struct DUnit {
+  int fc2, route, tile, split, kbeg, kend, expert;
+};
+
+// A unit as passed between the warps of a CTA through shared memory.
+struct DDesc {
+  int u;          // unit index, or -1: no more units
+  int expert;     // local expert
+  float scale;    // gs * 2^63 (FC1) or gs * 2^63 * router weight (FC2)
+  uint32_t mask;  // FC2: the token's valid top-k slots
+};
+static_assert(sizeof(DDesc) == 16, "unit descriptors are 16 bytes");
+
+// The arithmetic part of d_unit: route, tile, split and K range of unit u.
+__device__ __forceinline__ void d_unit_shape(const DecodeParams& p, int u, DUnit& U) {
+  int nt, ns, ks;
+  if (u < p.units1) {
+    U.fc2 = 0, nt = p.n_tiles1, ns = p.s1, ks = p.k_stages1;
+  } else {
+    u -= p.units1;
+    U.fc2 = 1, nt = p.n_tiles2, ns = p.s2, ks = p.k_stages2;
+  }
+  const int per_route = nt * ns;
+  U.route = u / per_route;
+  const int rem = u - U.route * per_route;
+  U.tile = rem / ns;
+  U.split = rem - U.tile * ns;
+  U.kbeg = U.split * ks / ns;  // ks <= 1024 stages, ns <= 8 splits: no overflow
+  U.kend = (U.split + 1) * ks / ns;
+  U.expert = -1;
+}
+
+__device__ __forceinline__ bool d_unit(const DecodeParams& p, int u, DUnit& U) {
+  d_unit_shape(p, u, U);
+  U.expert = d_local_expert(p, U.route);
+  return U.expert >= 0 && U.kend > U.kbeg;
+}
+
+__device__ __forceinline__ void d_trace(const DecodeParams& p, int kind, uint32_t idx) {
+  if (p.trace && blockIdx.x == 0 && idx < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + idx] = clock64();
+}
+// Per-CTA global timestamps (ns), indexed by CTA: kinds 5 start, 6 last FC2
+// partial stored, 7 last FC1 partial stored, 8 compute warps done, 9 output
+// warp done.
+__device__ __forceinline__ void d_trace_cta(const DecodeParams& p, int kind) {
+  if (p.trace && blockIdx.x < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + blockIdx.x] = (long long)globaltimer();
+}
+
+// Split grid barrier on the word a cooperative launch provides for
+// grid.sync(), with grid.sync()'s arithmetic: every CTA adds 1 once, except
+// CTA 0, which adds 2^31 - (G - 1), so the top bit flips exactly when all G
+// CTAs have arrived and the low bits end where they started.  The add
+// releases the CTA's earlier writes; the polling load acquires every CTA's.
+__device__ __forceinline__ uint32_t grid_arrive(uint32_t* word) {
+  const uint32_t add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(word), "r"(add) : "memory");
+  return old;
+}
+__device__ __forceinline__ bool grid_wait(const uint32_t* word, uint32_t old, const Abort& ab) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    uint32_t cur;
+    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(word) : "memory");
+    if ((cur ^ old) & 0x80000000u) return true;
+    if (ab.raised()) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      ab.raise(30);
+      return false;
+    }
+  }
+}
+
+// The split partials of one element, stored contiguously with stride S
+// (s1 <= S of them written), summed in ascending split order.
+template <int S>
+__device__ __forceinline__ void load_splits(float (&v)[S], const float* src) {
+  if (!src) {
+#pragma unroll
+    for (int i = 0; i < S; ++i) v[i] = 0.f;
+  } else if constexpr (S == 1) {
+    v[0] = __ldcg(src);
+  } else if constexpr (S == 2) {
+    const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
+    v[0] = a.x, v[1] = a.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < S; i += 4) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(src + i));
+      v[i] = a.x, v[i + 1] = a.y, v[i + 2] = a.z, v[i + 3] = a.w;
+    }
+  }
+}
+template <int S>
+__device__ __forceinline__ float sum_splits(const float (&v)[S], int s1) {
+  float a = v[0];
+#pragma unroll
+  for (int i = 1; i < S; ++i)
+    if (i < s1) a += v[i];
+  return a;
+}
+
+// FC2 activation row of one unit, built by the 256 compute threads:
+// h[k0 + i] = bf16(act(sum of the FC1 split partials)).  All of a batch's
+// partial loads are issued before the first sum; a batch that still holds a
+// not-written marker is read again.  Returns false on timeout (the row is
+// then incomplete and the abort flag is raised).
+template <int S>
+__device__ __forceinline__ bool build_h(const DecodeParams& p, const DUnit& U, uint8_t* row, int tid, int wnat,
+                                        const Abort& ab) {
+  constexpr int B = 16 / S;  // elements per thread per batch
+  const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
+  const float* gate = p.p + ((size_t)U.route * wnat + k0) * S;
+  const float* up = gate + (size_t)p.inter_pad * S;
+  const bool glu = p.act == 0;
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(row);
+  bool ok = true;
+  for (int i0 = 0; i0 < nk; i0 += 256 * B) {
+    float g[B][S], u[B][S];
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+#pragma unroll
+      for (int c = 0; c < B; ++c) {
+        const int i = i0 + c * 256 + tid;
+        load_splits<S>(g[c], i < nk ? gate + (size_t)i * S : nullptr);
+        load_splits<S>(u[c], glu && i < nk ? up + (size_t)i * S : nullptr);
+      }
+      bool ready = true;
+#pragma unroll
+      for (int c = 0; c < B; ++c)
+#pragma unroll
+        for (int sp = 0; sp < S; ++sp)
+          if (sp < p.s1 && (__float_as_uint(g[c][sp]) == kNotWritten || __float_as_uint(u[c][sp]) == kNotWritten))
+            ready = false;
+      if (ready) break;
+      if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
+        if (!ab.raised()) ab.raise(40);
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+#pragma unroll
+    for (int c = 0; c < B; ++c) {
+      const int i = i0 + c * 256 + tid;
+      if (i < nk) {
+        const float a = sum_splits<S>(g[c], p.s1);
+        const float hv = glu ? a / (1.0f + __expf(-a)) * sum_splits<S>(u[c], p.s1) : (a > 0.f ? a * a : 0.f);
+        h[i] = __float2bfloat16_rn(hv);
+      }
+    }
+    if (!ok) break;
+  }
+  return ok;
+}
+
+// Dense linear layer: out[token][n] = bf16(sum of the FC1 split partials of
+// column n, ascending split order) for the unit's 128 columns, one compute
+// thread per column; a partial still holding the not-written marker is read
+// again.  Returns false on timeout (the abort flag is raised).
+template <int S>
+__device__ __forceinline__ bool linear_out(const DecodeParams& p, const DUnit& U, int tid, const Abort& ab) {
+  const int n = U.tile * kTileRows + tid;
+  if (tid >= kTileRows || n >= p.n_out) return true;
+  const float* src = p.p + ((size_t)U.route * p.inter_pad + n) * S;
+  const unsigned long long t0 = globaltimer();
+  float v[S];
+  while (true) {
+    load_splits<S>(v, src);
+    bool ready = true;
+#pragma unroll
+    for (int sp = 0; sp < S; ++sp)
+      if (sp < p.s1 && __float_as_uint(v[sp]) == kNotWritten) ready = false;
+    if (ready) break;
+    if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
+      if (!ab.raised()) ab.raise(45);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  p.out[(size_t)(U.route / p.top_k) * p.n_out + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum_splits<S>(v, p.s1)));
+  return true;
+}
+
+// ------------------------------------------------------------------ fused
+template <int FMT>
+__global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_constant__ DecodeParams p) {
+  using L = DSmem<FMT>;
+  constexpr int SB = scale_bytes_per_row(FMT);
+  constexpr int kSS = L::kScaleStage;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* s_codes = smem + L::codes;
+  uint8_t* s_scales = smem + L::scales;
+  uint8_t* s_rows = smem + L::rows;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint64_t* full_w = bars;
+  uint64_t* empty_w = full_w + kDSlots;
+  uint64_t* full_b = empty_w + kDSlots;
+  uint64_t* empty_b = full_b + 2;
+  uint64_t* epi_full = empty_b + 2;
+  uint64_t* epi_empty = epi_full + 2;
+  uint64_t* desc_full = epi_empty + 2;  // a unit descriptor is ready (for the weight stream)
+  uint64_t* grid_bar = desc_full + 2;   // completes once every CTA has arrived at the grid barrier
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::misc);
+  DDesc* s_desc = reinterpret_cast<DDesc*>(smem + L::desc);  // [2] with the rows
+  DDesc* s_edesc = s_desc + 2;                                  // [2] for the output warp
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Abort ab{p.status, s_abort};
+  const int n_units = p.units1 + p.units2;
+  const int R = p.m * p.top_k;
+  if (threadIdx.x == 0) {
+    d_trace(p, 2, 0);
+    d_trace_cta(p, 5);
+    *s_abort = 0;
+    for (int i = 0; i < kDSlots; ++i) {
+      mbar_init(&full_w[i], 1);
+      mbar_init(&empty_w[i], kDComputeWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full_b[i], 1);
+      mbar_init(&empty_b[i], kDComputeWarps);
+      mbar_init(&epi_full[i], kDComputeWarps);
+      mbar_init(&epi_empty[i], 1);
+      mbar_init(&desc_full[i], 1);
+    }
+    mbar_init(grid_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // The producers resolve the CTA's first unit and start its weight stream
+  // and (FC1) x slice before the grid barrier: neither touches the partial
+  // buffers.
+  DUnit U0;
+  const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
+  uint32_t pre_slots = 0;
+  bool pre_row = false;
+  if (warp == 0 && lane == 0 && u0_ok && !(U0.fc2 && p.linear)) {
+    const size_t tile_id = (size_t)U0.expert * (U0.fc2 ? p.n_tiles2 : p.n_tiles1) + U0.tile;
+    const int ks = U0.fc2 ? p.k_stages2 : p.k_stages1;
+    const uint8_t* gc = (U0.fc2 ? p.w2_codes : p.w1_codes) + tile_id * ks * kCodeBytesPerStage;
+    const uint8_t* gsc = (U0.fc2 ? p.w2_scales : p.w1_scales) + tile_id * ks * kSS;
+    for (int s = U0.kbeg; s < U0.kend && pre_slots < (uint32_t)kDSlots; s += kDSlotStages, ++pre_slots) {
+      const int n = min(kDSlotStages, U0.kend - s);
+      mbar_arrive_expect_tx(&full_w[pre_slots], n * (kCodeBytesPerStage + kSS));
+      bulk_g2s(s_codes + pre_slots * kDSlotStages * kCodeBytesPerStage, gc + (size_t)s * kCodeBytesPerStage,
+               n * kCodeBytesPerStage, &full_w[pre_slots]);
+      bulk_g2s(s_scales + pre_slots * kDSlotStages * kSS, gsc + (size_t)s * kSS, n * kSS, &full_w[pre_slots]);
+      d_trace(p, 0, pre_slots);
+    }
+  }
+  if (warp == 1 && lane == 0 && u0_ok && !U0.fc2) {
+    uint8_t* row = s_rows;
+    const int k0 = U0.kbeg * kBK, nk = (U0.kend - U0.kbeg) * kBK;
+    const int kv = min(nk, p.hidden - k0);
+    mbar_expect_tx(&full_b[0], (uint32_t)kv * 2);
+    bulk_g2s(row, p.x + (size_t)(U0.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, &full_b[0]);
+    for (int i = kv * 2; i < nk * 2; i += 16) *reinterpret_cast<uint4*>(row + i) = make_uint4(0, 0, 0, 0);
+    s_desc[0].u = blockIdx.x;
+    s_desc[0].expert = U0.expert;
+    s_desc[0].scale = (p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f) * kDTwo63;
+    mbar_arrive(&full_b[0]);
+    mbar_arrive(&desc_full[0]);
+    pre_row = true;
+  }
+  pre_row = __shfl_sync(0xffffffffu, pre_row, 0);
+
+  // Before the grid barrier: fill both partial buffers with the not-written
+  // marker, clear the status word, and zero the output rows of tokens without
+  // a valid route (no unit writes them).
+  {
+    const size_t gt = (size_t)blockIdx.x * kDThreads + threadIdx.x, gstride = (size_t)gridDim.x * kDThreads;
+    const uint4 mark = make_uint4(kNotWritten, kNotWritten, kNotWritten, kNotWritten);
+    for (size_t i = gt; i < p.p_floats / 4; i += gstride) reinterpret_cast<uint4*>(p.p)[i] = mark;
+    for (size_t i = gt; i < p.q_floats / 4; i += gstride) reinterpret_cast<uint4*>(p.q)[i] = mark;
+    if (gt == 0) {
+      *p.ticket = 0;
+      if (p.status) {
+        p.status[0] = 0;
+        p.status[1] = 0;
+      }
+    }
+    const int gw = (int)(gt >> 5), nw = (int)(gstride >> 5);
+    for (int tk = gw; tk < p.m; tk += nw) {
+      const bool v = lane < p.top_k && d_local_expert(p, tk * p.top_k + lane) >= 0;
+      if (__ballot_sync(0xffffffffu, v) == 0) {
+        uint4* o = reinterpret_cast<uint4*>(p.out + (size_t)tk * p.hidden);
+        for (int i = lane; i < p.hidden / 8; i += 32) o[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  cg::grid_group grid = cg::this_grid();
+  if (!grid.is_valid()) {  // not a cooperative launch: there is no grid barrier to wait on
+    if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0u, 4u);  // B4_ERR_CUDA
+    return;
+  }
+  // Every thread's fill precedes the CTA's arrival (a release at GPU scope);
+  // warp 1 then waits for the other CTAs and completes grid_bar, which the
+  // first partial store or read of each warp waits on (acquire).
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      uint32_t* word = &cg::details::get_grid_workspace()->barrier;
+      const uint32_t old = grid_arrive(word);
+      if (grid_wait(word, old, ab)) mbar_arrive(grid_bar);
+    }
+    __syncwarp();
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------ weight stream
+    // follows the unit sequence that warp 1 publishes in the descriptors
+    if (lane == 0) {
+      uint32_t ws = 0;
+      for (uint32_t ds = 0; !ab.raised(); ++ds) {
+        const uint32_t rb = ds & 1;
+        if (!mbar_wait(&desc_full[rb], (ds >> 1) & 1, ab, 31)) break;
+        const int u = s_desc[rb].u;
+        if (u < 0) break;
+        DUnit U;
+        d_unit_shape(p, u, U);
+        if (U.fc2 && p.linear) continue;  // an output unit of the dense linear layer streams no weights
+        U.expert = s_desc[rb].expert;
+        const size_t tile_id = (size_t)U.expert * (U.fc2 ? p.n_tiles2 : p.n_tiles1) + U.tile;
+        const int ks = U.fc2 ? p.k_stages2 : p.k_stages1;
+        const uint8_t* gc = (U.fc2 ? p.w2_codes : p.w1_codes) + tile_id * ks * kCodeBytesPerStage;
+        const uint8_t* gsc = (U.fc2 ? p.w2_scales : p.w1_scales) + tile_id * ks * kSS;
+        for (int s = U.kbeg; s < U.kend; s += kDSlotStages, ++ws) {
+          if (ws < pre_slots) continue;  // issued before the grid barrier
+          const uint32_t slot = ws % kDSlots;
+          if (!mbar_wait(&empty_w[slot], ((ws / kDSlots) & 1) ^ 1, ab, 32)) break;
+          const int n = min(kDSlotStages, U.kend - s);
+          mbar_arrive_expect_tx(&full_w[slot], n * (kCodeBytesPerStage + kSS));
+          bulk_g2s(s_codes + slot * kDSlotStages * kCodeBytesPerStage, gc + (size_t)s * kCodeBytesPerStage,
+                   n * kCodeBytesPerStage, &full_w[slot]);
+          bulk_g2s(s_scales + slot * kDSlotStages * kSS, gsc + (size_t)s * kSS, n * kSS, &full_w[slot]);
+          d_trace(p, 0, ws);
+        }
+      }
+      if (ab.raised()) {  // let issued copies land before the CTA exits
+        const uint32_t n = ws < (uint32_t)kDSlots ? ws : (uint32_t)kDSlots;
+        for (uint32_t i = ws - n; i < ws; ++i) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(&full_w[i % kDSlots], (i / kDSlots) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  if (warp == 1) {
+    // ------------------------------------- unit schedule and activation rows
+    // The CTA's first unit is unit blockIdx.x; later ones are claimed from a
+    // counter in unit order (a CTA that runs faster takes more).  Each unit is
+    // resolved once and published with the FC1 x slice in one of two
+    // descriptor/row slots; a unit index of -1 ends the sequence.
+    uint32_t bs = 0;
+    DUnit U = U0;
+    int u = blockIdx.x;
+    bool have = u0_ok;
+    if (pre_row) {  // the first unit went out before the grid barrier
+      bs = 1;
+      have = false;
+    }
+    while (!ab.raised()) {
+      // next valid unit: claims are issued one unit ahead of their use
+      while (!have) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(p.ticket, 1);
+        u = (int)gridDim.x + __shfl_sync(0xffffffffu, t, 0);
+        if (u >= n_units) break;
+        have = d_unit(p, u, U);
+      }
+      const uint32_t rb = bs & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty_b[rb], ((bs >> 1) & 1) ^ 1, ab, 33))) break;
+      DDesc* dsc = s_desc + rb;
+      if (!have) {
+        if (lane == 0) {
+          dsc->u = -1;
+          mbar_arrive(&full_b[rb]);
+          mbar_arrive(&desc_full[rb]);
+        }
+        break;
+      }
+      if (!U.fc2) {
+        if (lane == 0) {
+          // the copy goes out first; the phase also needs the arrival below,
+          // which follows the descriptor (its scale load overlaps the copy)
+          uint8_t* row = s_rows + rb * kDRowBytes;
+          const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
+          const int kv = min(nk, p.hidden - k0);
+          mbar_expect_tx(&full_b[rb], (uint32_t)kv * 2);
+          bulk_g2s(row, p.x + (size_t)(U.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, &full_b[rb]);
+          for (int i = kv * 2; i < nk * 2; i += 16) *reinterpret_cast<uint4*>(row + i) = make_uint4(0, 0, 0, 0);
+          dsc->u = u;
+          dsc->expert = U.expert;
+          mbar_arrive(&desc_full[rb]);  // the weight stream needs only the unit
+          dsc->scale = (p.gs1 ? __ldg(p.gs1 + U.expert) : 1.0f) * kDTwo63;
+          mbar_arrive(&full_b[rb]);
+        }
+      } else if (p.linear) {
+        if (lane == 0) {
+          dsc->u = u;
+          dsc->expert = U.expert;
+          mbar_arrive(&desc_full[rb]);
+          dsc->scale = 1.0f;
+          dsc->mask = 1u;
+          mbar_arrive(&full_b[rb]);
+        }
+      } else {
+        if (lane == 0) {
+          dsc->u = u;
+          dsc->expert = U.expert;
+          mbar_arrive(&desc_full[rb]);
+        }
+        const int token = U.route / p.top_k;
+        const bool v = lane < p.top_k && d_local_expert(p, token * p.top_k + lane) >= 0;
+        const uint32_t mask = __ballot_sync(0xffffffffu, v);
+        if (lane == 0) {
+          dsc->scale = (p.gs2 ? __ldg(p.gs2 + U.expert) : 1.0f) * kDTwo63 * __ldg(p.topk_weights + U.route);
+          dsc->mask = mask;
+          mbar_arrive(&full_b[rb]);
+        }
+      }
+      ++bs;
+      have = false;
+    }
+    if (ab.raised() && lane == 0) {
+      for (uint32_t i = bs > 2 ? bs - 2 : 0; i < bs; ++i) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(&full_b[i & 1], (i >> 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  if (warp == 2 + kDComputeWarps) {
+    // ------------------------------------------------------ output tiles
+    if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 42))) return;
+    for (uint32_t es = 0;; ++es) {
+      const uint32_t eb = es & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&epi_full[eb], (es >> 1) & 1, ab, 37))) break;
+      const DDesc dsc = *(s_edesc + eb);
+      if (dsc.u < 0) break;
+      DUnit U;
+      d_unit_shape(p, dsc.u, U);
+      const int token = U.route / p.top_k;
+      const uint32_t mask = dsc.mask;
+      // out = bf16(sum over valid routes and splits); each lane has 4 outputs
+      // and 8 routes' partial loads are in flight at once.  Order: ascending
+      // top-k slot within groups of 8, splits outer within a group.
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int nb = U.tile * kTileRows + lane;
+      for (int jb = 0; jb < p.top_k; jb += 8) {
+        for (int sp = 0; sp < p.s2; ++sp) {
+          float v[8][4];
+          const unsigned long long t0 = globaltimer();
+          while (true) {
+            bool ready = true;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int j = jb + jj;
+              const bool valid = j < p.top_k && ((mask >> j) & 1u);
+              const float* qr = p.q + ((size_t)sp * R + token * p.top_k + j) * p.hidden + nb;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                v[jj][c] = valid && nb + 32 * c < p.hidden ? __ldcg(qr + 32 * c) : 0.f;
+                if (__float_as_uint(v[jj][c]) == kNotWritten) ready = false;
+              }
+            }
+            if (__all_sync(0xffffffffu, ready)) break;
+            if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
+              if (!ab.raised()) ab.raise(41);
+              break;
+            }
+            __nanosleep(64);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[c] += v[jj][c];
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (nb + 32 * c < p.hidden)
+          p.out[(size_t)token * p.hidden + nb + 32 * c] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&epi_empty[eb]);
+    }
+    if (lane == 0) d_trace_cta(p, 9);
+    return;
+  }
+
+  // --------------------------------------------------------- compute warps
+  const int cw = warp - 2;
+  const int g = lane >> 2, t = lane & 3;
+  const int r0 = 16 * cw + g, r1 = r0 + 8;
+  const int tid = threadIdx.x - 64;
+  // this thread's 8 code bytes of row r0 (block t of the stage) and of row r1
+  const uint32_t code_off = (t >> 1) * (kCodeBytesPerStage / 2) + r0 * 16 + (t & 1) * 8;
+  const uint32_t sc_off = FMT == 0 ? r0 * SB + t : r0 * SB + (t >> 1);
+  const int wnat = fc1_natural_width(p.act, p.inter_pad);
+  uint32_t ws = 0, bs = 0, es = 0;
+  bool synced = false;  // grid_bar seen complete
+  while (true) {
+    const uint32_t rb = bs & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full_b[rb], (bs >> 1) & 1, ab, 35))) break;
+    const DDesc dsc = *(s_desc + rb);
+    if (dsc.u < 0) break;
+    DUnit U;
+    d_unit_shape(p, dsc.u, U);
+    if (U.fc2 && p.linear) {
+      // dense linear layer: this unit writes 128 columns of out
+      if (!synced) {
+        if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 46))) break;
+        synced = true;
+      }
+      switch (p.s1_stride) {
+        case 1: linear_out<1>(p, U, tid, ab); break;
+        case 2: linear_out<2>(p, U, tid, ab); break;
+        case 4: linear_out<4>(p, U, tid, ab); break;
+        default: linear_out<8>(p, U, tid, ab); break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_b[rb]);
+      ++bs;
+      if (ab.raised()) break;
+      continue;
+    }
+    const uint8_t* row = s_rows + rb * kDRowBytes + t * 32;  // block t of each stage
+    if (U.fc2) {
+      if (!synced) {
+        if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 43))) break;
+        synced = true;
+      }
+      // h = act(sum over FC1 splits) in bf16 for this unit's K range
+      uint8_t* hrow = s_rows + rb * kDRowBytes;
+      switch (p.s1_stride) {
+        case 1: build_h<1>(p, U, hrow, tid, wnat, ab); break;
+        case 2: build_h<2>(p, U, hrow, tid, wnat, ab); break;
+        case 4: build_h<4>(p, U, hrow, tid, wnat, ab); break;
+        default: build_h<8>(p, U, hrow, tid, wnat, ab); break;
+      }
+      named_bar_sync(1, 32 * kDComputeWarps);
+    }
+    if (tid == 0) d_trace(p, 3, bs);
+    float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+    float f[4] = {0.f, 0.f, 0.f, 0.f}, h4[4] = {0.f, 0.f, 0.f, 0.f};
+    bool ok = !ab.raised();
+    for (int s = U.kbeg; ok && s < U.kend; s += kDSlotStages, ++ws) {
+      const uint32_t slot = ws % kDSlots;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (ws / kDSlots) & 1, ab, 36))) {
+        ok = false;
+        break;
+      }
+      const int n = min(kDSlotStages, U.kend - s);
+      const uint8_t* cs = s_codes + slot * kDSlotStages * kCodeBytesPerStage + code_off;
+      const uint8_t* ss = s_scales + slot * kDSlotStages * kSS + sc_off;
+      const uint8_t* xr = row + (s - U.kbeg) * (kBK * 2);
+      StageIn a;
+      load_stage<SB>(a, cs, ss, xr);
+      if (n == kDSlotStages) {
+        // both stages' shared-memory loads are in flight before any math
+        StageIn b;
+        load_stage<SB>(b, cs + kCodeBytesPerStage, ss + kSS, xr + kBK * 2);
+        compute_stage<FMT>(a, d, e);
+        compute_stage<FMT>(b, f, h4);
+      } else {
+        compute_stage<FMT>(a, d, e);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_w[slot]);
+      if (tid == 0) d_trace(p, 1, ws);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_b[rb]);
+    ++bs;
+    if (!ok) break;
+    if (!synced) {
+      if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 44))) break;
+      synced = true;
+    }
+    // every column of D holds the same dot products: d[0] row r0, d[2] row r1
+    const float v0 = (d[0] + e[0]) + (f[0] + h4[0]), v1 = (d[2] + e[2]) + (f[2] + h4[2]);
+    if (t < 2) {
+      const int r = t ? r1 : r0;
+      const float v = (t ? v1 : v0) * dsc.scale;
+      if (!U.fc2) {
+        // FC1 split partial in natural row order (splits innermost), times gs13 * 2^63
+        int nat;
+        if (p.act == 0) {
+          const int i = U.tile * 64 + (r >> 5) * 16 + (r & 15);
+          nat = (r & 31) >= 16 ? p.inter_pad + i : i;
+        } else {
+          nat = U.tile * kTileRows + r;
+          if (nat >= p.inter_pad) nat = -1;
+        }
+        if (nat >= 0) p.p[((size_t)U.route * wnat + nat) * p.s1_stride + U.split] = v;
+      } else {
+        // FC2 split partial times gs2 * 2^63 and the router weight
+        const int n = U.tile * kTileRows + r;
+        if (n < p.hidden) p.q[((size_t)U.split * R + U.route) * p.hidden + n] = v;
+      }
+    }
+    if (tid == 0) d_trace_cta(p, U.fc2 ? 6 : 7);
+    if (!U.fc2) {
+    } else if (U.split == p.s2 - 1 && (U.route % p.top_k) == 31 - __clz(dsc.mask)) {
+      // the token tile's last unit in unit order: the output warp sums it
+      const uint32_t eb = es & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 38))) break;
+      if (tid == 0) s_edesc[eb] = dsc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&epi_full[eb]);
+      ++es;
+    }
+    if (tid == 0) d_trace(p, 4, bs - 1);
+  }
+  // end of the output-tile sequence
+  const uint32_t eb = es & 1;
+  if (__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 39))) {
+    if (tid == 0) s_edesc[eb].u = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&epi_full[eb]);
+  }
+  if (tid == 0) d_trace_cta(p, 8);
+}
+
+template <int FMT>
+cudaError_t launch_decode_fmt(const DecodeParams& p, int grid, cudaStream_t stream) {
+  auto kern = decode_moe_kernel<FMT>;
+  const size_t smem = DSmem<FMT>::total;
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Resident CTAs per SM of the fused decode kernel on the current device: a
+// cooperative launch never exceeds the resident count, so every CTA runs at
+// once and a wait on another CTA's unit always ends (each wait is bounded as
+// well).  Kept per device, under a lock.
+cudaError_t decode_occupancy(int fmt, int* blocks_per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static int cached[64][2] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && cached[dev][fmt]) {
+    *blocks_per_sm = cached[dev][fmt];
+    return cudaSuccess;
+  }
+  const void* k = fmt == 0 ? reinterpret_cast<const void*>(decode_moe_kernel<0>)
+                           : reinterpret_cast<const void*>(decode_moe_kernel<1>);
+  const size_t smem = fmt == 0 ? DSmem<0>::total : DSmem<1>::total;
+  e = ensure_smem_limit(k, smem);
+  int occ = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kDThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (dev < 64) cached[dev][fmt] = occ;
+  *blocks_per_sm = occ;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream) {
+  return fmt == 0 ? launch_decode_fmt<0>(p, grid, stream) : launch_decode_fmt<1>(p, grid, stream);
+}
+
+}  // namespace b4

@@ -97,8 +97,40 @@ struct GemmParams {
 
 constexpr int kTraceLen = 2048;
 
-// The small-m path: one cooperative kernel (decode_grouped.cu).
+// The per-route decode path: one cooperative kernel (decode_moe.cu).
 struct DecodeParams {
+  const uint8_t* w1_codes;   // prepared W13 / W1
+  const uint8_t* w1_scales;
+  const float* gs1;          // [E_l] or null (MXFP4)
+  const uint8_t* w2_codes;   // prepared W2
+  const uint8_t* w2_scales;
+  const float* gs2;
+  int n_tiles1, k_stages1, n_tiles2, k_stages2;
+  int m, top_k, num_global_experts, num_local_experts, hidden, inter_pad;
+  int act;                   // 0 SwiGLU, 1 ReLU^2
+  // Dense linear layer (E = 1, top-1, no activation, no FC2): the FC2 units
+  // become output units (route, 128-column tile of N) that sum the FC1 split
+  // partials into out [m, n_out] bf16; topk_ids, topk_weights, w2 and q are
+  // unused.
+  int linear, n_out;
+  const int32_t* topk_ids;   // [m, top_k], or null: every route goes to local expert 0
+  const float* topk_weights;
+  const int32_t* expert_map;  // or null
+  const uint16_t* x;         // [m, H] bf16
+  uint16_t* out;             // [m, H] bf16
+  int s1, s2;                // K splits of FC1 and FC2
+  int s1_stride;             // split stride of the FC1 partials: s1 rounded up to 1, 2, 4 or 8
+  int units1, units2;        // R * n_tiles1 * s1 and R * n_tiles2 * s2
+  float* p;                  // FC1 split partials [R][N1 natural][s1_stride]
+  float* q;                  // FC2 split partials [s2][R][H]
+  size_t p_floats, q_floats; // sizes of p and q (filled with the not-yet-written marker)
+  int* ticket;               // units [grid, units1 + units2) are claimed from this counter
+  uint32_t* status;
+  long long* trace;          // optional timeline (see b4_set_trace)
+};
+
+// The route-grouped small-m path: one cooperative kernel (decode_grouped.cu).
+struct SmallGroupParams {
   const uint8_t* w1_codes;   // prepared W13 / W1
   const uint8_t* w1_scales;
   const float* gs1;          // [E_l] or null (MXFP4)
@@ -119,15 +151,16 @@ struct DecodeParams {
   int p_stride;
   float* q;                  // FC2 partials [q_pieces][R][H]
   int q_pieces;
+  size_t p_floats, q_floats;  // sizes of p and q (filled with the not-written marker)
   uint16_t* h;               // [R][inter_pad] bf16
-  int* hcount;               // [R][n_tiles1] FC1 pieces done (+ ready mark); pcount and ocount follow
-  int* pcount;               // [R][n_tiles2] FC2 pieces done
-  int* ocount;               // [m][n_tiles2] routes of a token done
-  size_t n_counters;         // ints from hcount through ocount (zeroed at launch)
+  int* hflag;                // [R][n_tiles1] FC1 tile's h built (zeroed at launch)
+  size_t n_flags;
   int pmax;                  // most CTAs sharing one tile (<= p_stride, <= q_pieces)
   int w0;                    // partition cost of a stage: w0 + the group's column sets
-  long long l2_prefetch_bytes;  // FC2 weight bytes each CTA prefetches into L2 at launch
   uint32_t* status;
+  // Optional timeline (b4_set_trace), or null: %globaltimer ns per CTA at
+  // phase boundaries, trace[kind * kTraceLen + blockIdx.x].
+  long long* trace;
 };
 
 struct RoutePackParams {

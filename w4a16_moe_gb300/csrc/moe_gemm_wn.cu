@@ -127,9 +127,15 @@ __device__ __forceinline__ bool get_unit(const GemmParams& p, int u, int ns, Uni
   return U.rows > 0 && U.kend > U.kbeg;
 }
 
-// Timeline hook: CTA 0 records clock64() of event `kind` number `idx`.
+// Timeline hook: CTA 0 records clock64() of event `kind` number `idx`.  It
+// sits in the pipelines' per-stage loops, so it is compiled in only when the
+// library is built with B4_TRACE defined (a profiling build).
 __device__ __forceinline__ void trace_mark(const GemmParams& p, int kind, uint32_t idx) {
+#ifdef B4_TRACE
   if (p.trace && blockIdx.x == 0 && idx < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + idx] = clock64();
+#else
+  (void)p, (void)kind, (void)idx;
+#endif
 }
 
 // Warp-uniform bounded wait.
