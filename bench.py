@@ -6,23 +6,31 @@
 A step is one call of the whole layer (route handling, FC1 + activation, FC2 +
 top-k combine) on one batch of synthetic inputs.  The headline workload is
 the decode MoE (NVFP4, E=128, top_k=8, H=4096, I=1536, ReLU^2, m=1); the
-metric is microseconds per call (lower is better).  Timed with CUDA events
-around CUDA-graph replays of the call on the launching stream, L2 flushed
-before every timed step (a 512 MiB buffer written, then read back so that the
-dirty lines are written back outside the timed region), inputs already
-resident in HBM.
+metric is microseconds per call (lower is better).
+
+Timed region: one replay of a CUDA graph holding exactly K back-to-back calls,
+bracketed by CUDA events on the launching stream, inputs already resident in
+HBM.  Consecutive calls cycle through several device copies of the prepared
+weights (as consecutive MoE layers of a model read different weights) and
+eight routing/activation draws, so that at least three times the L2 size of
+other weights is read between two calls on the same copy: the inputs are
+larger than L2 and every call streams its experts from HBM.  L2 is flushed
+(512 MiB written, then read back) before the timed replay.  The single-call
+figure of earlier measurements (one call per graph replay, L2 and code cold
+before each) is kept beside it as "us_per_call_single".
 
 Besides the headline it reports, in "secondary", the same measurement for
 the other workloads (decode m=2, 4; small-batch m=16, 64; prefill m=2048 with
 SwiGLU and ReLU^2; MXFP4 m=512; the dense W4A16 linear layer b4_linear,
 N = K = 4096, m = 1, 16, 2048), each with its weight-stream TB/s and bf16
-TFLOP/s, "roofline" for the dominant kernel (the W4A16 GEMM, timed per launch
-with the library's timing events), "cpu_baseline" (the float64 CPU oracle on a
-bounded sample), "e2e" (the same call through the Python API with host
-buffers: every step replays a CUDA graph of one host->device copy of the
-step's inputs from pinned memory, the call and the device->host copy of the
-result; wall clock around replay and synchronize) and the SM clocks sampled
-during the timed region.
+TFLOP/s; in "crossover", the decode workload at m = 4..64 with the small-m and
+the grouped path each forced; "roofline" for the dominant kernel (timed per
+launch with the library's timing events in a second graph of the same calls),
+"cpu_baseline" (the float64 CPU oracle on a bounded sample), "e2e" (the same
+calls through the Python API with host buffers: one graph of K steps, each a
+host->device copy of the step's inputs from pinned memory, the call and the
+device->host copy of the result; wall clock around replay and synchronize)
+and the SM clocks sampled during the timed region.
 
 Replicas only: under torchrun every rank runs the same workload on its own GPU
 with no collective on the data path; rank 0 prints the max over ranks.
@@ -49,6 +57,8 @@ HEADLINE = ("decode", "relu2", 1)
 SECONDARY = [("decode", "relu2", 2), ("decode", "relu2", 4), ("small", "silu", 16), ("small", "silu", 64),
              ("prefill", "silu", 2048), ("prefill", "relu2", 2048), ("mxfp4", "silu", 512),
              ("linear", "none", 1), ("linear", "none", 16), ("linear", "none", 2048)]
+# the small-m / grouped crossover: the same workload with each path forced
+CROSSOVER = [("decode", "relu2", m, path) for m in (4, 8, 16, 32, 64) for path in ("decode", "grouped")]
 L2_FLUSH_BYTES = 512 << 20
 DRAWS = 8  # independent routing / activation draws cycled through the steps
 
@@ -106,6 +116,19 @@ def call_accounting(wl, m, ids, em):
     f2 = 2.0 * r_valid * wl.hidden * wl.inter
     return {"bytes": b13 + b2 + io, "weight_bytes": b13 + b2, "fc1_bytes": b13 + m * wl.hidden * 2,
             "fc2_bytes": b2, "flops": f13 + f2, "experts_hit": int(len(hit)), "routes": r_valid}
+
+
+def weight_copies(b, dev):
+    """Device copies of the prepared weights, cycled call by call so that no
+    call finds its weights in L2: enough copies that three times the L2 size
+    passes between two calls on the same copy (at least 2, at most 64)."""
+    import math
+
+    torch = b.torch
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    per_call = statistics.mean(d["acct"]["weight_bytes"] for d in b.draws)
+    n = int(min(64, max(2, math.ceil(3 * l2 / max(per_call, 1)))))
+    return [dev] + [{k: (None if v is None else v.clone()) for k, v in dev.items()} for _ in range(n - 1)]
 
 
 # ------------------------------------------------------------------ clocks
@@ -197,6 +220,7 @@ class Bench:
                 "xd": torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16),
                 "idsd": torch.from_numpy(ids).cuda(), "wtsd": torch.from_numpy(wts).cuda(),
                 "acct": call_accounting(wl, m, ids, self.em_np)})
+        self.devs = weight_copies(self, dev)
         self.ws = torch.empty(b4.workspace_bytes(self.cfg, self.act), dtype=torch.uint8, device="cuda")
         self.out = torch.empty(m, wl.hidden, dtype=torch.bfloat16, device="cuda")
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -214,10 +238,77 @@ class Bench:
         self.flush.zero_()
         self.flush_sink.copy_(self.flush.view(torch_int32()).amax(dim=0, keepdim=True)[:1])
 
-    def call(self, d, stream=None):
-        dv = self.dev
+    def call(self, d, stream=None, dv=None):
+        dv = dv or self.dev
         self.b4.fused_moe(self.cfg, d["xd"], dv["w13"], dv["s13"], dv["g13"], dv["w2"], dv["s2"], dv["g2"], d["idsd"],
                           d["wtsd"], self.act, self.out, self.ws, stream=stream)
+
+    def call_i(self, i, stream):
+        """Call i of a sequence: weight copy i mod copies, draw i mod DRAWS."""
+        self.call(self.draws[i % DRAWS], stream, self.devs[i % len(self.devs)])
+
+    def capture_seq(self, n, events=None):
+        """One CUDA graph of n back-to-back calls (events: per call, the
+        library's timing events, created beforehand; or None)."""
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for i in range(min(n, 2 * len(self.devs))):  # eager warm-up (kernel attributes before capture)
+                self.call_i(i, self.stream)
+        self.stream.synchronize()
+        self.b4.check_status(self.ws, self.stream)
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(n):
+                    if events is not None:
+                        self.b4.set_timing_events(events[i])
+                    self.call_i(i, self.stream)
+        finally:
+            if events is not None:
+                self.b4.set_timing_events(None)
+        return g
+
+    def time_seq(self, steps, warmup, barrier=None):
+        """The timed region: one replay of a graph of exactly `steps` calls,
+        after the L2 flush and >= `warmup` untimed calls; the per-kernel
+        durations come from a second graph of the same calls with the
+        library's timing events between its kernels."""
+        torch = self.torch
+        g = self.capture_seq(steps)
+        with torch.cuda.stream(self.stream):
+            for _ in range(max(1, -(-warmup // steps))):
+                self.flush_l2()
+                g.replay()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            self.flush_l2()
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            start.record(self.stream)
+            g.replay()
+            end.record(self.stream)
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        wall = time.perf_counter() - t_wall
+        ms_total = start.elapsed_time(end)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(self.n_kernels + 1)] for _ in range(steps)]
+        side = torch.cuda.Stream()
+        for ev in evs:  # create the CUDA events outside the capture
+            for e in ev:
+                e.record(side)
+        side.synchronize()
+        tg = self.capture_seq(steps, events=evs)
+        with torch.cuda.stream(self.stream):
+            self.flush_l2()
+            tg.replay()
+        torch.cuda.synchronize()
+        kern = [[ev[j].elapsed_time(ev[j + 1]) for j in range(self.n_kernels)] for ev in evs]
+        return ms_total, kern, wall
 
     def capture(self, timing_events=None):
         torch = self.torch
@@ -272,35 +363,34 @@ class Bench:
         return ms, kern, wall
 
     def run(self, steps, warmup, barrier=None, with_e2e=False, with_clocks=False, gpu_index=0):
-        torch = self.torch
-        graphs = self.capture()
         clocks = None
         if with_clocks:
             with ClockSampler(gpu_index) as cs:
-                ms, _, wall = self.time_steps(graphs, steps, warmup, barrier)
+                ms_total, kern, wall = self.time_seq(steps, warmup, barrier)
             clocks = cs.summary()
         else:
-            ms, _, wall = self.time_steps(graphs, steps, warmup, barrier)
-        # per-kernel durations: the same graphs with timing events between kernels
-        kev = [torch.cuda.Event(enable_timing=True) for _ in range(self.n_kernels + 1)]
-        tgraphs = self.capture(timing_events=kev)
-        _, kern, _ = self.time_steps(tgraphs, steps, 1, None, kernel_events=kev)
+            ms_total, kern, wall = self.time_seq(steps, warmup, barrier)
+        # the single-call measurement: a graph of one call, L2 flushed before each
+        graphs = self.capture()
+        ms_single, _, _ = self.time_steps(graphs, min(steps, 10), 3, None)
         accts = [self.draws[i % DRAWS]["acct"] for i in range(steps)]
-        res = {"ms": ms, "kern": kern, "accts": accts, "wall": wall, "clocks": clocks}
+        res = {"ms": [ms_total / steps], "ms_total": ms_total, "kern": kern, "accts": accts, "wall": wall,
+               "clocks": clocks, "single_ms": ms_single}
         if with_e2e:
             res["e2e_s"] = self.e2e_timed(steps, warmup)
         return res
 
     def e2e_timed(self, steps, warmup):
-        """End to end through the public call with host buffers: every step
-        replays a CUDA graph of one host->device copy of the step's inputs
-        (x, ids and router weights packed in one pinned buffer), the fused
-        call, and one device->host copy of out; wall clock around replay and
-        synchronize."""
+        """End to end through the public call with host buffers: one graph of
+        `steps` steps, each a host->device copy of that step's inputs (x, ids
+        and router weights packed in one pinned buffer), the fused call (weight
+        copies cycled as in the device-timed region) and a device->host copy
+        of out; wall clock around the replay and the synchronize."""
         torch = self.torch
         m, H, k = self.m, self.wl.hidden, self.wl.top_k
         xb, ib, wb = m * H * 2, m * k * 4, m * k * 4
-        x_off, i_off, w_off = 0, (xb + 255) // 256 * 256, 0
+        x_off = 0
+        i_off = (xb + 255) // 256 * 256
         w_off = i_off + (ib + 255) // 256 * 256
         nbytes = w_off + (wb + 255) // 256 * 256
         dstage = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
@@ -308,8 +398,8 @@ class Bench:
         idsd = dstage[i_off:i_off + ib].view(torch.int32).view(m, k)
         wtsd = dstage[w_off:w_off + wb].view(torch.float32).view(m, k)
         out_h = torch.empty(m, H, dtype=torch.int16).pin_memory()
-        dv, s = self.dev, self.stream
-        graphs, stages = [], []
+        s = self.stream
+        stages = []
         for d in self.draws:
             h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
             h[x_off:x_off + xb].view(torch.int16).copy_(torch.from_numpy(d["x_bits"].view(np.int16).reshape(-1)))
@@ -317,33 +407,32 @@ class Bench:
             h[w_off:w_off + wb].view(torch.float32).copy_(torch.from_numpy(d["wts"].reshape(-1)))
             stages.append(h)
 
-            def step(h=h):
-                dstage.copy_(h, non_blocking=True)
-                self.b4.fused_moe(self.cfg, xd, dv["w13"], dv["s13"], dv["g13"], dv["w2"], dv["s2"], dv["g2"],
-                                  idsd, wtsd, self.act, self.out, self.ws, stream=s)
-                out_h.copy_(self.out.view(torch.int16), non_blocking=True)
+        def step(i):
+            dv = self.devs[i % len(self.devs)]
+            dstage.copy_(stages[i % DRAWS], non_blocking=True)
+            self.b4.fused_moe(self.cfg, xd, dv["w13"], dv["s13"], dv["g13"], dv["w2"], dv["s2"], dv["g2"],
+                              idsd, wtsd, self.act, self.out, self.ws, stream=s)
+            out_h.copy_(self.out.view(torch.int16), non_blocking=True)
 
+        with torch.cuda.stream(s):
+            step(0)  # eager first: kernel attributes are set outside capture
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                step(i)
+        for _ in range(max(1, -(-warmup // steps))):
             with torch.cuda.stream(s):
-                step()  # eager first: kernel attributes are set outside capture
+                g.replay()
             s.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                step()
-            graphs.append(g)
-        for i in range(warmup):
-            with torch.cuda.stream(s):
-                graphs[i % len(graphs)].replay()
-            s.synchronize()
-        total = 0.0
-        for i in range(steps):
-            with torch.cuda.stream(s):
-                self.flush_l2()
-            torch.cuda.synchronize()
-            ta = time.perf_counter()
-            with torch.cuda.stream(s):  # a graph replays on the current stream
-                graphs[i % len(graphs)].replay()
-            s.synchronize()
-            total += time.perf_counter() - ta
+        with torch.cuda.stream(s):
+            self.flush_l2()
+        torch.cuda.synchronize()
+        ta = time.perf_counter()
+        with torch.cuda.stream(s):  # a graph replays on the current stream
+            g.replay()
+        s.synchronize()
+        total = time.perf_counter() - ta
         return {"seconds": total, "h2d": xb + ib + wb, "d2h": m * H * 2}
 
 
@@ -352,7 +441,8 @@ class Bench:
 # give the commands).  A figure is reported only while the kernel sources still
 # hash to the profiled ones; after any change it is null until re-measured.
 KERNEL_SOURCES = {
-    "decode": ["decode_grouped.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
+    "decode": ["decode_moe.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
+    "decode_grouped": ["decode_grouped.cu", "decode_stage.cuh", "dequant.cuh", "ptx.cuh", "kernels.cuh"],
     "grouped": ["moe_gemm.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
@@ -388,6 +478,7 @@ class LinearBench(Bench):
             xb, x = W.activations(wl, m, seed=100 + d)
             self.draws.append({"x_bits": xb, "x": x, "acct": acct,
                                "xd": torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)})
+        self.devs = weight_copies(self, self.dev)
         self.ws = torch.empty(b4.linear_workspace_bytes(self.cfg), dtype=torch.uint8, device="cuda")
         self.out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -403,8 +494,8 @@ class LinearBench(Bench):
         self.n_kernels = 1 if self.decode else (3 if k_split else 2)
         self.launches = 1 if self.decode else (3 if k_split else 2)  # pack, GEMM (, rounding pass)
 
-    def call(self, d, stream=None):
-        dv = self.dev
+    def call(self, d, stream=None, dv=None):
+        dv = dv or self.dev
         self.b4.linear(self.cfg, d["xd"], dv["w"], dv["s"], dv["g"], self.out, self.ws, stream=stream)
 
 
@@ -432,10 +523,11 @@ def kernel_source_hash(path):
 
 
 def kernel_family(b):
-    """Which GEMM kernels serve the call: the fused decode kernel, or the
-    grouped weights-on-N / weights-on-M kernels (api.cu's dispatch rule)."""
+    """Which GEMM kernels serve the call: the per-route small-m kernel
+    (m <= 4), the route-grouped small-m kernel, or the grouped weights-on-N /
+    weights-on-M kernels (api.cu's dispatch rule)."""
     if b.decode:
-        return "decode"
+        return "decode" if b.m <= 4 else "decode_grouped"
     wl = b.wl
     return "grouped_wn" if b.m * wl.top_k < 96 * wl.num_local_experts else "grouped"
 
@@ -462,10 +554,11 @@ def summarize(b: Bench, res, peaks):
     gemm_ms = [sum(k[j] for j in gi) for k in kern]
     gemm_s = 1e-3 * statistics.mean(gemm_ms)
     g_bytes = statistics.mean(a["fc1_bytes"] + a["fc2_bytes"] for a in res["accts"])
+    single = res.get("single_ms") or ms
     out = {
         "workload": describe(wl, m),
         "us_per_call": round(us, 3),
-        "us_per_call_median": round(1e3 * statistics.median(ms), 3),
+        "us_per_call_single": round(1e3 * statistics.mean(single), 3),
         "tokens_per_s": round(m / (us * 1e-6), 1),
         "weight_stream_TBps": round(wbytes / (us * 1e-6) / 1e12, 4),
         "algorithmic_TBps": round(acct_bytes / (us * 1e-6) / 1e12, 4),
@@ -474,16 +567,22 @@ def summarize(b: Bench, res, peaks):
         "kernel_us_mean": [round(1e3 * statistics.mean(k[j] for k in kern), 3) for j in range(len(kern[0]))],
         "gemm_us": round(gemm_s * 1e6, 3),
     }
+    # frac: the dominant kernel(s) alone (per-launch duration from the timing
+    # events); frac_per_call: the same algorithmic figure over the whole call
     if b.decode or m <= 64:
         ach = g_bytes / gemm_s / 1e9
+        per_call = acct_bytes / (us * 1e-6) / 1e9
         out["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(b),
+                           "frac": round(ach / peaks["hbm_gbs"], 4),
+                           "frac_per_call": round(per_call / peaks["hbm_gbs"], 4), "traffic": measured_traffic(b),
                            "peak_src": peaks["src"]}
     else:
         ach = acct_flops / gemm_s / 1e12
+        per_call = acct_flops / (us * 1e-6) / 1e12
         out["roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
-                           "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": measured_traffic(b),
-                           "peak_src": peaks["src"]}
+                           "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                           "frac_per_call": round(per_call / peaks["bf16_tflops"], 4),
+                           "traffic": measured_traffic(b), "peak_src": peaks["src"]}
     return out
 
 
@@ -562,6 +661,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-crossover", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode:relu2:1",
                     help="name:act:m of the timed workload (default: the decode headline)")
@@ -588,6 +688,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         barrier = dist.barrier
 
+    import w4a16_moe_gb300 as b4
     import workloads as W
 
     peaks = load_peaks()
@@ -606,18 +707,25 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(us / 1e3, 5), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random FP4 codes, softmax top-k routing)",
         "config": {"workload": head["workload"], "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step: 512 MiB written then read back (cold, clean L2)",
-                   "launch": "CUDA graph per call",
+                   "l2": (f"inputs larger than L2: consecutive calls cycle {len(b.devs)} device copies of the "
+                          f"prepared weights and {DRAWS} routing/activation draws, so >= 3x the L2 size of other "
+                          "weights is read between two calls on the same copy; L2 flushed (512 MiB written, then "
+                          "read back) before the timed region"),
+                   "launch": f"one CUDA graph of the {args.steps} timed calls, replayed once",
+                   "us_per_call_single": head["us_per_call_single"],
+                   "single_note": "one call per graph replay, L2 flushed before each (cold L2 and cold code)",
                    "tokens_per_s": round(head["tokens_per_s"] * world, 1),
                    "weight_stream_TBps": head["weight_stream_TBps"], "bf16_TFLOPs": head["bf16_TFLOPs"]},
         "roofline": {k: v for k, v in head["roofline"].items() if k != "peak_src"},
         "roofline_note": (("dominant kernel: the fused decode kernel (FC1, FC2 and combine in one launch)"
                            if b.decode else "dominant kernels: the grouped FC1 and FC2 GEMM launches")
+                          + "; frac over those kernels' event-timed duration, frac_per_call over the whole call"
                           + f"; peak of {head['roofline']['peak_src']} MEASURED_PEAKS.json; traffic = ncu DRAM "
                           "bytes per call of those launches (null if their sources changed since the capture)"),
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": b.launches * args.steps,
+        "gpu_launches_note": "kernels of this library per call x steps; memset nodes are not counted",
         "clocks": res["clocks"],
         "kernel_us_mean": head["kernel_us_mean"],
     }
@@ -632,6 +740,20 @@ def main():
             del bb
             torch.cuda.empty_cache()
         line["secondary"] = sec
+    if not args.no_crossover:
+        cross = []
+        for nm, ac, mm, pth in CROSSOVER:
+            path = {"decode": b4.PATH_DECODE, "grouped": b4.PATH_GROUPED}[pth]
+            bb = Bench(W.WORKLOADS[nm].with_act(ac), mm, path=path)
+            r = bb.run(min(args.steps, 10), 3, barrier)
+            sm_ = summarize(bb, r, peaks)
+            cross.append({"m": mm, "path": pth, "us_per_call": sm_["us_per_call"],
+                          "us_per_call_single": sm_["us_per_call_single"],
+                          "weight_stream_TBps": sm_["weight_stream_TBps"]})
+            del bb
+            torch.cuda.empty_cache()
+        line["crossover"] = {"workload": describe(W.WORKLOADS["decode"].with_act("relu2"), 0).replace(" m=0", ""),
+                             "lines": cross}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -239,6 +239,32 @@ __global__ void probe_dequant_kernel(const uint8_t* codes, const uint8_t* scales
   }
 }
 
+// The small-m kernels' dequantiser: serving words -> plain nibble pairs ->
+// hardware FP4 conversion to f16, times the fp32 block scale; one thread per
+// weight row, one block per 64-wide stage, fp32 output in K order.
+template <int FMT>
+__global__ void probe_dequant_f16_kernel(const uint8_t* codes, const uint8_t* scales, float* out) {
+  const int blk = blockIdx.x, r = threadIdx.x;
+  constexpr int SB = scale_bytes_per_row(FMT);
+  constexpr int G = FMT == 0 ? 16 : 32;
+  const uint8_t* cs = codes + (size_t)blk * kCodeBytesPerStage;
+  const uint8_t* ss = scales + ((size_t)blk * kTileRows + r) * SB;
+  float* o = out + ((size_t)blk * kTileRows + r) * kBK;
+  // byte b of a converted word holds elements (lo, hi) of the word's eight
+  const int el_lo[4] = {0, 1, 4, 5}, el_hi[4] = {2, 3, 6, 7};
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + (q >> 2) * 2048 + r * 16 + (q & 3) * 4);
+    uint32_t h[4];
+    e2m1x8_to_f16x2(serving_to_nibbles(w), h[0], h[1], h[2], h[3]);
+    for (int b = 0; b < 4; ++b) {
+      const __half2 v = *reinterpret_cast<const __half2*>(&h[b]);
+      const int klo = q * 8 + el_lo[b], khi = q * 8 + el_hi[b];
+      o[klo] = __low2float(v) * f32_scale<FMT>(ss[klo / G], 0);
+      o[khi] = __high2float(v) * f32_scale<FMT>(ss[khi / G], 0);
+    }
+  }
+}
+
 // bf16x2 multiply on chosen bit patterns (subnormal-input behaviour).
 __global__ void probe_bf16_mul_kernel(const uint32_t* a, const uint32_t* b, uint32_t* d, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -279,6 +305,13 @@ int probe_dequant(const uint8_t* codes, const uint8_t* scales, int fmt, int nblo
   if (nblocks <= 0) return -1;
   if (fmt == 0) probe_dequant_kernel<0><<<nblocks, 128>>>(codes, scales, out);
   else probe_dequant_kernel<1><<<nblocks, 128>>>(codes, scales, out);
+  return (int)cudaDeviceSynchronize();
+}
+
+int probe_dequant_f16(const uint8_t* codes, const uint8_t* scales, int fmt, int nblocks, float* out) {
+  if (nblocks <= 0) return -1;
+  if (fmt == 0) probe_dequant_f16_kernel<0><<<nblocks, 128>>>(codes, scales, out);
+  else probe_dequant_f16_kernel<1><<<nblocks, 128>>>(codes, scales, out);
   return (int)cudaDeviceSynchronize();
 }
 

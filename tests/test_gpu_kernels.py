@@ -32,7 +32,8 @@ def probe():
     if not os.path.exists(PROBE):
         pytest.fail("tests/csrc/libb4probe.so missing: run __graft_entry__.build()")
     lib = ctypes.CDLL(PROBE)
-    for name in ("probe_mma_ts", "probe_mma_rowb", "probe_dequant", "probe_bf16_mul", "probe_tma", "probe_mma_sw128"):
+    for name in ("probe_mma_ts", "probe_mma_rowb", "probe_dequant", "probe_dequant_f16", "probe_bf16_mul", "probe_tma",
+                 "probe_mma_sw128"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -220,6 +221,42 @@ def test_prepare_and_dequant_bit_exact(probe, b4, fmt, which, act, hidden, inter
     zg, ze = (got & 0x7FFF) == 0, (expect & 0x7FFF) == 0
     bad = np.argwhere((got != expect) & ~(zg & ze))
     assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[0].tolist()}: got {got[tuple(bad[0])]:#06x} want {expect[tuple(bad[0])]:#06x}"
+
+
+@pytest.mark.parametrize("fmt,which,act,hidden,inter", [
+    (Q.NVFP4, 0, 0, 128, 96),
+    (Q.NVFP4, 1, 0, 144, 96),
+    (Q.MXFP4, 0, 0, 96, 64),
+    (Q.MXFP4, 1, 0, 160, 96),
+])
+def test_prepare_and_f16_dequant_exact(probe, b4, fmt, which, act, hidden, inter):
+    """The small-m kernels' dequantiser (bit-pair exchange of the serving
+    word, hardware E2M1 -> f16 conversion, fp32 block scale) reproduces the
+    oracle's dequantised weights exactly: every E2M1 value times an E4M3 or
+    E8M0 scale is exact in fp32."""
+    rng = np.random.default_rng(hidden * 5 + inter + which)
+    e_l = 3
+    n, k = ((2 * inter if act == 0 else inter), hidden) if which == 0 else (hidden, inter)
+    g = Q.GROUP[fmt]
+    codes = Q.pack_nibbles(rng.integers(0, 16, size=(e_l, n, k), dtype=np.uint8))
+    if fmt == Q.NVFP4:
+        pool = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    else:
+        pool = np.arange(65, 192, dtype=np.uint8)
+    scales = pool[rng.integers(0, len(pool), size=(e_l, n, k // g))]
+    expect_bits, (tiles, stages) = _serving_expected(codes, scales, fmt, which, act, hidden, inter)
+    # the bf16 expectation is exact (times 2^-63): undo the factor
+    expect = F.bf16_from_bits(expect_bits).astype(np.float64) * 2.0 ** 63
+    cfg = b4.MoEConfig(m=1, top_k=1, num_global_experts=e_l, num_local_experts=e_l, hidden=hidden, inter=inter,
+                       format=0 if fmt == Q.NVFP4 else 1)
+    pc, ps = b4.prepare_weights(cfg, which, act, dev(codes), dev(scales))
+    nblk = e_l * tiles * stages
+    out = torch.zeros(nblk * 128 * 64, dtype=torch.float32, device="cuda")
+    assert probe.probe_dequant_f16(ctypes.c_void_p(pc.data_ptr()), ctypes.c_void_p(ps.data_ptr()),
+                                   0 if fmt == Q.NVFP4 else 1, nblk, ctypes.c_void_p(out.data_ptr())) == 0
+    got = out.cpu().numpy().astype(np.float64).reshape(expect.shape)
+    bad = np.argwhere(got != expect)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[0].tolist()}: got {got[tuple(bad[0])]} want {expect[tuple(bad[0])]}"
 
 
 def test_prepare_rejects_invalid_scales(b4):

@@ -12,20 +12,26 @@
 // units (route, 128-row tile of H, K split).  CTA b takes units b, b + G, ...,
 // in increasing order.
 //
-//   warp 0        streams the unit's packed codes and scales, two 64-wide K
-//                 stages per slot of a 4-slot shared-memory ring; weights
-//                 depend on nothing, so the next unit's stream (FC2 included)
-//                 starts while this one computes.
+//   warp 0        streams the unit's packed codes and scales, four 64-wide K
+//                 stages per slot of a shared-memory ring (two copies of
+//                 16 KB + 2 KB: the bulk-copy engine streams large copies
+//                 faster); weights depend on nothing, so the next unit's
+//                 stream (FC2 included) starts while this one computes.  It
+//                 also issues the CTA's first x slice, ahead of its weights.
 //   warp 1        resolves each unit once (expert, scale factors, the token's
-//                 valid top-k slots) and passes it to the compute warps with
-//                 the FC1 x slice (one bulk copy).
-//   warps 2..9    16 weight rows each: register dequantisation (E2M1 table
-//                 lookup by PRMT, one bf16x2 multiply by the block scale)
-//                 feeding warp-level m16n8k16 bf16 MMAs, fp32 accumulation;
-//                 each unit ends with an fp32 split partial store.  An FC2
-//                 unit first builds its h slice, act(sum of the FC1 partials)
-//                 in bf16.
-//   warp 10       stores the bf16 output of a token's 128-column tile: it sums
+//                 valid top-k slots), copies an FC1 unit's bf16 x slice into
+//                 a row buffer (one bulk copy) and converts it there to the
+//                 f16 slots the compute warps read.
+//   warps 2..     compute warps, 16 weight rows each (two of a K group's
+//                 128): hardware E2M1 -> f16 conversion feeding warp-level
+//                 m16n8k16 f16 MMAs whose activation operand is block
+//                 diagonal, block scales applied to the fp32 block sums
+//                 (decode_stage.cuh); each unit ends with an fp32 split
+//                 partial store.  An FC2 unit first builds its h slice,
+//                 bf16(act(sum of the FC1 partials)), as f16 slots.  With two
+//                 K groups (one CTA per SM) the second group takes the second
+//                 half of every slot and hands its row sums to the first.
+//   last warp     stores the bf16 output of a token's 128-column tile: it sums
 //                 the FC2 partials of the token's valid routes (ascending
 //                 top-k slot, then split) for the tile's last unit in unit
 //                 order.  Fixed orders: the output is bitwise reproducible.
@@ -47,22 +53,30 @@
 // units, and each "FC2" unit is an output tile (token, 128 columns) that sums
 // the FC1 split partials straight into out; those units stream no weights.
 //
-// Why warp-level MMAs and not tcgen05 here: the register dequantiser feeds
-// m16n8k16 fragments directly, while a tcgen05.mma reads its weight operand
-// from shared or tensor memory, so every dequantised weight would make a
-// round trip there first; with one token per unit the MMA work is tiny either
-// way, which leaves the dequantiser's integer work as the limit: per code word (8 weights) two LOP3 and three
-// shifts, per weight pair a PRMT and a bf16x2 multiply, all on the SM's
-// half-rate integer/bf16 pipe (measured: 2 warp-instructions per clock per SM
-// for each of them, 1 for a multiply-high), which caps the stage arithmetic
-// near 4.7 TB/s at two CTAs per SM.
+// Why warp-level MMAs and not tcgen05 here: with one token per unit the MMA
+// work is tiny and the limit is turning 4-bit codes into MMA operands.  The
+// register path reaches its fragments straight from the converted codes; a
+// tcgen05.mma would need every weight written to shared or tensor memory
+// first.  Measured on GB300 with the data in shared memory: the PRMT table
+// lookup + bf16x2 scale multiply of the grouped kernels ran near 4.7 TB/s of
+// weights at two CTAs per SM; the conversion instruction with f16 MMAs and
+// block-diagonal activations near 11 TB/s, and about 6.5 TB/s including the
+// bit-pair exchange the serving layout needs (four logic ops per word), which
+// is above what HBM delivers.
 //
 // K order inside an MMA: thread t of a quad owns physical 16-element block t
-// of the 64-wide stage (one NVFP4 scale block); MMA j takes its pairs 2j and
-// 2j+1 as the fragment's logical K pairs t and t + 4.  Weights and
-// activations use the same permutation, so every dot product is unchanged.
-// The activation is replicated into all eight B columns, so every thread
-// holds its two rows' results.
+// of each 64-wide stage; its bytes pair elements (0,2), (1,3), (4,6), (5,7)
+// of every code word (decode_stage.cuh), and the activation slots are stored
+// in the same pairing, so every dot product is unchanged.  MMA column c of a
+// 128-wide chunk is the chunk's block c: only the thread that owns that block
+// in that stage loads nonzero activations for it, so column c accumulates the
+// block's unscaled sum.  Activations are prescaled per 128-wide slot by a
+// power of two (exact) so that they fit f16; the scale and the prescale are
+// applied to the fp32 block sum.
+//
+// Control flow of the compute warps: they share named barriers, so a failed
+// bounded wait never makes one warp leave alone; the loop ends on an OR taken
+// over all of them (bar.red.or), and every wait stays bounded.
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -80,13 +94,16 @@ cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 
 namespace cg = cooperative_groups;
 
-constexpr int kDThreads = 352;        // weights, schedule, 8 compute warps, output
-constexpr int kDComputeWarps = 8;
-constexpr int kDSlots = 4;            // weight ring slots
-constexpr int kDSlotStages = 2;       // 64-wide K stages per slot
+constexpr int kDGroups = 1;           // K groups of 8 compute warps (128 weight rows each) per CTA
+constexpr int kDGroupWarps = 8;
+constexpr int kDComputeWarps = kDGroups * kDGroupWarps;
+constexpr int kDThreads = 32 * (3 + kDComputeWarps);  // weights, schedule, compute, output
+constexpr int kDMinBlocks = 2 / kDGroups;              // resident CTAs per SM
+constexpr int kDSlots = kDGroups == 1 ? 4 : 6;  // weight ring slots
+constexpr int kDSlotStages = 4;       // 64-wide K stages per slot (two copies of 16 KB + 2 KB: large copies stream faster)
 constexpr int kDMaxStages = 128;      // K stages of one unit (its activation row is in shared memory)
+constexpr int kDMaxSlots = kDMaxStages / 2;  // 128-wide slots of one unit's activation row
 constexpr int kDRowBytes = kDMaxStages * kBK * 2;
-constexpr float kDTwo63 = 9.223372036854775808e18f;
 constexpr uint32_t kNotWritten = 0x7F800001u;  // signalling NaN: never an arithmetic result
 
 template <int FMT>
@@ -96,9 +113,12 @@ struct DSmem {
   static constexpr size_t scales = (size_t)kDSlots * kDSlotStages * kCodeBytesPerStage;
   static constexpr size_t rows = scales + (size_t)kDSlots * kDSlotStages * kScaleStage;
   static constexpr size_t bars = rows + 2 * (size_t)kDRowBytes;
-  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 12);  // 11 barrier pairs used, one spare
+  static constexpr size_t misc = bars + 8 * (2 * kDSlots + 14);  // 13 barriers besides the ring, one spare
   static constexpr size_t desc = misc + 16;
-  static constexpr size_t total = desc + 4 * 16;  // four 16-byte unit descriptors
+  static constexpr size_t xexp = desc + 4 * 16;            // four 16-byte unit descriptors
+  static constexpr size_t zero = xexp + 2 * kDMaxSlots * 4;  // per row buffer: prescale exponent of each slot
+  static constexpr size_t red = zero + 32;                   // 32 zero bytes: inactive activation columns
+  static constexpr size_t total = red + 2 * kTileRows * 4;   // per row buffer: the second K group's row sums
 };
 
 __device__ __forceinline__ int d_local_expert(const DecodeParams& p, int route) {
@@ -152,7 +172,8 @@ __device__ __forceinline__ void d_trace(const DecodeParams& p, int kind, uint32_
 }
 // Per-CTA global timestamps (ns), indexed by CTA: kinds 5 start, 6 last FC2
 // partial stored, 7 last FC1 partial stored, 8 compute warps done, 9 output
-// warp done.
+// warp done, 11 first weight slot computed, 12 first x row converted, 13 grid
+// barrier complete; kind 10 holds the CTA's SM.
 __device__ __forceinline__ void d_trace_cta(const DecodeParams& p, int kind) {
   if (p.trace && blockIdx.x < (uint32_t)kTraceLen) p.trace[kind * kTraceLen + blockIdx.x] = (long long)globaltimer();
 }
@@ -211,58 +232,118 @@ __device__ __forceinline__ float sum_splits(const float (&v)[S], int s1) {
   return a;
 }
 
-// FC2 activation row of one unit, built by the 256 compute threads:
-// h[k0 + i] = bf16(act(sum of the FC1 split partials)).  All of a batch's
-// partial loads are issued before the first sum; a batch that still holds a
-// not-written marker is read again.  Returns false on timeout (the row is
-// then incomplete and the abort flag is raised).
+// FC1 activation row of one unit: lane 0 copies the token's bf16 x[k0 ..
+// k0 + kv) into the row buffer (one bulk copy, completing on xbar), positions
+// past the hidden size are zeroed; then the warp converts the row in place to
+// 128-wide f16 slots, each prescaled by a power of two (exps[j]).  Lane l
+// owns K positions 4l .. 4l+3 of a slot (block l / 4, quarter l % 4), whose
+// eight bytes are the same in the bf16 and the f16 row.
+__device__ __forceinline__ void issue_x_row(const DecodeParams& p, const DUnit& U, uint8_t* row, uint64_t* xbar) {
+  const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
+  const int kv = min(nk, p.hidden - k0);  // hidden is a multiple of 16: whole 32-byte pieces
+  mbar_arrive_expect_tx(xbar, (uint32_t)kv * 2);
+  bulk_g2s(row, p.x + (size_t)(U.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, xbar);
+}
+__device__ __forceinline__ bool convert_x_row(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps,
+                                              uint64_t* xbar, uint32_t parity, int lane, const Abort& ab) {
+  if (!__all_sync(0xffffffffu, mbar_wait(xbar, parity, ab, 34))) return false;
+  const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
+  for (int j = 0; 128 * j < nk; ++j) {
+    const int i = 128 * j + 4 * lane;  // four positions: all below the hidden size or all past it
+    uint8_t* dst = row + 256 * j + 8 * lane;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < nk && k0 + i < p.hidden) {
+      const uint2 w = *reinterpret_cast<const uint2*>(dst);
+      v[0] = __uint_as_float(w.x << 16), v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(w.y << 16), v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    }
+    float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const int e = slot_prescale(a);
+    store_x4_f16(dst, v[0], v[1], v[2], v[3], e);
+    if (lane == 0) exps[j] = e;
+  }
+  return true;
+}
+
+// Sums (ascending split order) of the split partials of four consecutive
+// elements at src (splits innermost, stride S; s1 <= S written), read again by
+// the whole warp while any written one still holds the not-written marker.
+// Lanes with valid == false take zeros.  False on timeout (abort raised).
 template <int S>
-__device__ __forceinline__ bool build_h(const DecodeParams& p, const DUnit& U, uint8_t* row, int tid, int wnat,
-                                        const Abort& ab) {
-  constexpr int B = 16 / S;  // elements per thread per batch
+__device__ __forceinline__ bool poll_sum4(float (&sum)[4], const float* src, bool valid, int s1, const Abort& ab) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    float v[4 * S];
+    bool ready = true;
+    if (valid) {
+#pragma unroll
+      for (int c = 0; c < 4 * S; c += 4) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(src + c));
+        v[c] = a.x, v[c + 1] = a.y, v[c + 2] = a.z, v[c + 3] = a.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 4 * S; ++c)
+        if (c % S < s1 && __float_as_uint(v[c]) == kNotWritten) ready = false;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4 * S; ++c) v[c] = 0.f;
+    }
+    if (__all_sync(0xffffffffu, ready)) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a = v[e * S];
+#pragma unroll
+        for (int sp = 1; sp < S; ++sp)
+          if (sp < s1) a += v[e * S + sp];
+        sum[e] = a;
+      }
+      return true;
+    }
+    if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
+      if (!ab.raised()) ab.raise(40);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// FC2 activation row of one unit, built by the eight compute warps (warp w
+// takes slots w, w + 8, ...): h[i] = bf16(act(sum of the FC1 split partials,
+// ascending split order)), then the slot's power-of-two prescale and f16 as
+// in build_x_row.  Returns false on timeout (the abort flag is raised).
+template <int S>
+__device__ __forceinline__ bool build_h_f16(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps, int cw,
+                                            int lane, int wnat, const Abort& ab) {
   const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
   const float* gate = p.p + ((size_t)U.route * wnat + k0) * S;
   const float* up = gate + (size_t)p.inter_pad * S;
   const bool glu = p.act == 0;
-  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(row);
-  bool ok = true;
-  for (int i0 = 0; i0 < nk; i0 += 256 * B) {
-    float g[B][S], u[B][S];
-    const unsigned long long t0 = globaltimer();
-    while (true) {
+  for (int j = cw; 128 * j < nk; j += kDComputeWarps) {
+    const int i = 128 * j + 4 * lane;
+    const bool valid = i < nk;
+    float h[4];
+    if (!poll_sum4<S>(h, gate + (size_t)i * S, valid, p.s1, ab)) return false;
+    if (glu) {
+      float u[4];
+      if (!poll_sum4<S>(u, up + (size_t)i * S, valid, p.s1, ab)) return false;
 #pragma unroll
-      for (int c = 0; c < B; ++c) {
-        const int i = i0 + c * 256 + tid;
-        load_splits<S>(g[c], i < nk ? gate + (size_t)i * S : nullptr);
-        load_splits<S>(u[c], glu && i < nk ? up + (size_t)i * S : nullptr);
-      }
-      bool ready = true;
+      for (int c = 0; c < 4; ++c) h[c] = h[c] / (1.0f + __expf(-h[c])) * u[c];
+    } else {
 #pragma unroll
-      for (int c = 0; c < B; ++c)
-#pragma unroll
-        for (int sp = 0; sp < S; ++sp)
-          if (sp < p.s1 && (__float_as_uint(g[c][sp]) == kNotWritten || __float_as_uint(u[c][sp]) == kNotWritten))
-            ready = false;
-      if (ready) break;
-      if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
-        if (!ab.raised()) ab.raise(40);
-        ok = false;
-        break;
-      }
-      __nanosleep(64);
+      for (int c = 0; c < 4; ++c) h[c] = h[c] > 0.f ? h[c] * h[c] : 0.f;
     }
 #pragma unroll
-    for (int c = 0; c < B; ++c) {
-      const int i = i0 + c * 256 + tid;
-      if (i < nk) {
-        const float a = sum_splits<S>(g[c], p.s1);
-        const float hv = glu ? a / (1.0f + __expf(-a)) * sum_splits<S>(u[c], p.s1) : (a > 0.f ? a * a : 0.f);
-        h[i] = __float2bfloat16_rn(hv);
-      }
-    }
-    if (!ok) break;
+    for (int c = 0; c < 4; ++c) h[c] = valid ? __bfloat162float(__float2bfloat16_rn(h[c])) : 0.f;
+    float a = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const int e = slot_prescale(a);
+    store_x4_f16(row + 256 * j + 8 * lane, h[0], h[1], h[2], h[3], e);
+    if (lane == 0) exps[j] = e;
   }
-  return ok;
+  return true;
 }
 
 // Dense linear layer: out[token][n] = bf16(sum of the FC1 split partials of
@@ -295,7 +376,7 @@ __device__ __forceinline__ bool linear_out(const DecodeParams& p, const DUnit& U
 
 // ------------------------------------------------------------------ fused
 template <int FMT>
-__global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(const __grid_constant__ DecodeParams p) {
   using L = DSmem<FMT>;
   constexpr int SB = scale_bytes_per_row(FMT);
   constexpr int kSS = L::kScaleStage;
@@ -312,9 +393,13 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   uint64_t* epi_empty = epi_full + 2;
   uint64_t* desc_full = epi_empty + 2;  // a unit descriptor is ready (for the weight stream)
   uint64_t* grid_bar = desc_full + 2;   // completes once every CTA has arrived at the grid barrier
+  uint64_t* xbar = grid_bar + 1;        // [2] the bf16 x slice of an FC1 unit has landed
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::misc);
   DDesc* s_desc = reinterpret_cast<DDesc*>(smem + L::desc);  // [2] with the rows
   DDesc* s_edesc = s_desc + 2;                                  // [2] for the output warp
+  int* s_xexp = reinterpret_cast<int*>(smem + L::xexp);        // [2][kDMaxSlots]
+  float* s_red = reinterpret_cast<float*>(smem + L::red);       // [2][128]
+  uint8_t* s_zero = smem + L::zero;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Abort ab{p.status, s_abort};
@@ -323,6 +408,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   if (threadIdx.x == 0) {
     d_trace(p, 2, 0);
     d_trace_cta(p, 5);
+    if (p.trace && blockIdx.x < (uint32_t)kTraceLen) p.trace[10 * kTraceLen + blockIdx.x] = smid();
     *s_abort = 0;
     for (int i = 0; i < kDSlots; ++i) {
       mbar_init(&full_w[i], 1);
@@ -336,8 +422,11 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
       mbar_init(&desc_full[i], 1);
     }
     mbar_init(grid_bar, 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     fence_mbar_init();
   }
+  if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(s_zero)[threadIdx.x] = 0u;
   __syncthreads();
 
   // The producers resolve the CTA's first unit and start its weight stream
@@ -347,6 +436,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
   uint32_t pre_slots = 0;
   bool pre_row = false;
+  if (warp == 0 && lane == 0 && u0_ok && !U0.fc2) issue_x_row(p, U0, s_rows, &xbar[0]);  // ahead of the weights
   if (warp == 0 && lane == 0 && u0_ok && !(U0.fc2 && p.linear)) {
     const size_t tile_id = (size_t)U0.expert * (U0.fc2 ? p.n_tiles2 : p.n_tiles1) + U0.tile;
     const int ks = U0.fc2 ? p.k_stages2 : p.k_stages1;
@@ -360,22 +450,23 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
       bulk_g2s(s_scales + pre_slots * kDSlotStages * kSS, gsc + (size_t)s * kSS, n * kSS, &full_w[pre_slots]);
       d_trace(p, 0, pre_slots);
     }
+    d_trace_cta(p, 14);
   }
-  if (warp == 1 && lane == 0 && u0_ok && !U0.fc2) {
-    uint8_t* row = s_rows;
-    const int k0 = U0.kbeg * kBK, nk = (U0.kend - U0.kbeg) * kBK;
-    const int kv = min(nk, p.hidden - k0);
-    mbar_expect_tx(&full_b[0], (uint32_t)kv * 2);
-    bulk_g2s(row, p.x + (size_t)(U0.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, &full_b[0]);
-    for (int i = kv * 2; i < nk * 2; i += 16) *reinterpret_cast<uint4*>(row + i) = make_uint4(0, 0, 0, 0);
-    s_desc[0].u = blockIdx.x;
-    s_desc[0].expert = U0.expert;
-    s_desc[0].scale = (p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f) * kDTwo63;
-    mbar_arrive(&full_b[0]);
-    mbar_arrive(&desc_full[0]);
-    pre_row = true;
+  if (warp == 1 && u0_ok && !U0.fc2) {
+    if (lane == 0) {
+      s_desc[0].u = blockIdx.x;
+      s_desc[0].expert = U0.expert;
+      mbar_arrive(&desc_full[0]);
+      s_desc[0].scale = p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f;
+    }
+    pre_row = true;  // its x slice was issued by warp 0
+    convert_x_row(p, U0, s_rows, s_xexp, &xbar[0], 0, lane, ab);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&full_b[0]);
+      d_trace_cta(p, 12);
+    }
   }
-  pre_row = __shfl_sync(0xffffffffu, pre_row, 0);
 
   // Before the grid barrier: fill both partial buffers with the not-written
   // marker, clear the status word, and zero the output rows of tokens without
@@ -411,10 +502,12 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   // first partial store or read of each warp waits on (acquire).
   __syncthreads();
   if (warp == 1) {
-    if (lane == 0) {
-      uint32_t* word = &cg::details::get_grid_workspace()->barrier;
-      const uint32_t old = grid_arrive(word);
-      if (grid_wait(word, old, ab)) mbar_arrive(grid_bar);
+    uint32_t* word = &cg::details::get_grid_workspace()->barrier;
+    uint32_t old = 0;
+    if (lane == 0) old = grid_arrive(word);
+    if (lane == 0 && grid_wait(word, old, ab)) {
+      mbar_arrive(grid_bar);
+      d_trace_cta(p, 13);
     }
     __syncwarp();
   }
@@ -469,11 +562,13 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
     // resolved once and published with the FC1 x slice in one of two
     // descriptor/row slots; a unit index of -1 ends the sequence.
     uint32_t bs = 0;
+    uint32_t xuse0 = 0, xuse1 = 0;  // FC1 x copies per row buffer (phase of xbar)
     DUnit U = U0;
     int u = blockIdx.x;
     bool have = u0_ok;
     if (pre_row) {  // the first unit went out before the grid barrier
       bs = 1;
+      xuse0 = 1;
       have = false;
     }
     while (!ab.raised()) {
@@ -497,21 +592,20 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         break;
       }
       if (!U.fc2) {
+        uint8_t* row = s_rows + rb * kDRowBytes;
         if (lane == 0) {
-          // the copy goes out first; the phase also needs the arrival below,
-          // which follows the descriptor (its scale load overlaps the copy)
-          uint8_t* row = s_rows + rb * kDRowBytes;
-          const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
-          const int kv = min(nk, p.hidden - k0);
-          mbar_expect_tx(&full_b[rb], (uint32_t)kv * 2);
-          bulk_g2s(row, p.x + (size_t)(U.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, &full_b[rb]);
-          for (int i = kv * 2; i < nk * 2; i += 16) *reinterpret_cast<uint4*>(row + i) = make_uint4(0, 0, 0, 0);
           dsc->u = u;
           dsc->expert = U.expert;
           mbar_arrive(&desc_full[rb]);  // the weight stream needs only the unit
-          dsc->scale = (p.gs1 ? __ldg(p.gs1 + U.expert) : 1.0f) * kDTwo63;
-          mbar_arrive(&full_b[rb]);
+          issue_x_row(p, U, row, &xbar[rb]);
+          dsc->scale = p.gs1 ? __ldg(p.gs1 + U.expert) : 1.0f;
         }
+        const uint32_t xu = rb ? xuse1 : xuse0;
+        convert_x_row(p, U, row, s_xexp + rb * kDMaxSlots, &xbar[rb], xu & 1, lane, ab);
+        if (rb) ++xuse1;
+        else ++xuse0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_b[rb]);
       } else if (p.linear) {
         if (lane == 0) {
           dsc->u = u;
@@ -531,7 +625,7 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         const bool v = lane < p.top_k && d_local_expert(p, token * p.top_k + lane) >= 0;
         const uint32_t mask = __ballot_sync(0xffffffffu, v);
         if (lane == 0) {
-          dsc->scale = (p.gs2 ? __ldg(p.gs2 + U.expert) : 1.0f) * kDTwo63 * __ldg(p.topk_weights + U.route);
+          dsc->scale = (p.gs2 ? __ldg(p.gs2 + U.expert) : 1.0f) * __ldg(p.topk_weights + U.route);
           dsc->mask = mask;
           mbar_arrive(&full_b[rb]);
         }
@@ -539,10 +633,12 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
       ++bs;
       have = false;
     }
-    if (ab.raised() && lane == 0) {
-      for (uint32_t i = bs > 2 ? bs - 2 : 0; i < bs; ++i) {
+    if (ab.raised() && lane == 0) {  // let issued x copies land before the CTA exits
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t n = i ? xuse1 : xuse0;
+        if (n == 0) continue;
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(&full_b[i & 1], (i >> 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(&xbar[i], (n - 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
     }
@@ -609,101 +705,153 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
   }
 
   // --------------------------------------------------------- compute warps
+  // The sixteen compute warps share named barriers, so none of them leaves the
+  // unit loop alone: a failed (bounded) wait sets `bad`, the warp skips the
+  // work but still passes every barrier, and the loop ends only by an OR
+  // taken over all of them.
   const int cw = warp - 2;
+  const int grp = cw / kDGroupWarps;  // K group: the first or the second 128-wide half of every slot
   const int g = lane >> 2, t = lane & 3;
-  const int r0 = 16 * cw + g, r1 = r0 + 8;
+  const int r0 = 16 * (cw % kDGroupWarps) + g, r1 = r0 + 8;
   const int tid = threadIdx.x - 64;
+  constexpr uint32_t kNC = 32 * kDComputeWarps;
   // this thread's 8 code bytes of row r0 (block t of the stage) and of row r1
   const uint32_t code_off = (t >> 1) * (kCodeBytesPerStage / 2) + r0 * 16 + (t & 1) * 8;
-  const uint32_t sc_off = FMT == 0 ? r0 * SB + t : r0 * SB + (t >> 1);
+  // accumulator columns 2t, 2t+1 hold the sums of blocks 2t, 2t+1 of a chunk
+  // (stage t >> 1 of it): their scale bytes
+  const uint32_t sc_off = (t >> 1) * kSS + (FMT == 0 ? r0 * SB + 2 * (t & 1) : r0 * SB + (t & 1));
+  // MMA column g is block g of a chunk: this thread's activation operand is
+  // nonzero in the chunk's first stage when g == t and in its second when g == t + 4
+  const bool col0 = g == t, col1 = g == t + 4;
   const int wnat = fc1_natural_width(p.act, p.inter_pad);
   uint32_t ws = 0, bs = 0, es = 0;
   bool synced = false;  // grid_bar seen complete
+  bool bad = false;     // a wait of this warp failed (the abort flag is raised)
   while (true) {
     const uint32_t rb = bs & 1;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full_b[rb], (bs >> 1) & 1, ab, 35))) break;
+    if (!bad && !__all_sync(0xffffffffu, mbar_wait(&full_b[rb], (bs >> 1) & 1, ab, 35))) bad = true;
+    if (named_bar_or(3, kNC, bad || ab.raised())) break;
     const DDesc dsc = *(s_desc + rb);
     if (dsc.u < 0) break;
     DUnit U;
     d_unit_shape(p, dsc.u, U);
+    if (U.fc2 && !synced) {  // an FC2 or output unit reads other CTAs' partials
+      if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 43))) bad = true;
+      synced = true;
+    }
     if (U.fc2 && p.linear) {
       // dense linear layer: this unit writes 128 columns of out
-      if (!synced) {
-        if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 46))) break;
-        synced = true;
-      }
-      switch (p.s1_stride) {
-        case 1: linear_out<1>(p, U, tid, ab); break;
-        case 2: linear_out<2>(p, U, tid, ab); break;
-        case 4: linear_out<4>(p, U, tid, ab); break;
-        default: linear_out<8>(p, U, tid, ab); break;
+      if (!bad) {
+        switch (p.s1_stride) {
+          case 1: linear_out<1>(p, U, tid, ab); break;
+          case 2: linear_out<2>(p, U, tid, ab); break;
+          case 4: linear_out<4>(p, U, tid, ab); break;
+          default: linear_out<8>(p, U, tid, ab); break;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_b[rb]);
       ++bs;
-      if (ab.raised()) break;
       continue;
     }
-    const uint8_t* row = s_rows + rb * kDRowBytes + t * 32;  // block t of each stage
+    uint8_t* row = s_rows + rb * kDRowBytes;
+    int* xexp = s_xexp + rb * kDMaxSlots;
     if (U.fc2) {
-      if (!synced) {
-        if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 43))) break;
-        synced = true;
+      // h = act(sum over FC1 splits) for this unit's K range, as f16 slots
+      if (!bad) {
+        bool built;
+        switch (p.s1_stride) {
+          case 1: built = build_h_f16<1>(p, U, row, xexp, cw, lane, wnat, ab); break;
+          case 2: built = build_h_f16<2>(p, U, row, xexp, cw, lane, wnat, ab); break;
+          default: built = build_h_f16<4>(p, U, row, xexp, cw, lane, wnat, ab); break;
+        }
+        bad = !built;
       }
-      // h = act(sum over FC1 splits) in bf16 for this unit's K range
-      uint8_t* hrow = s_rows + rb * kDRowBytes;
-      switch (p.s1_stride) {
-        case 1: build_h<1>(p, U, hrow, tid, wnat, ab); break;
-        case 2: build_h<2>(p, U, hrow, tid, wnat, ab); break;
-        case 4: build_h<4>(p, U, hrow, tid, wnat, ab); break;
-        default: build_h<8>(p, U, hrow, tid, wnat, ab); break;
-      }
-      named_bar_sync(1, 32 * kDComputeWarps);
+      bad = named_bar_or(1, kNC, bad);
     }
     if (tid == 0) d_trace(p, 3, bs);
-    float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-    float f[4] = {0.f, 0.f, 0.f, 0.f}, h4[4] = {0.f, 0.f, 0.f, 0.f};
-    bool ok = !ab.raised();
-    for (int s = U.kbeg; ok && s < U.kend; s += kDSlotStages, ++ws) {
+    const uint8_t* xb0 = col0 ? row + g * 32 : s_zero;
+    const uint8_t* xb1 = col1 ? row + g * 32 : s_zero;
+    const int xstep0 = col0 ? 256 : 0, xstep1 = col1 ? 256 : 0;
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int s = U.kbeg, k = 0; !bad && s < U.kend; s += kDSlotStages, ++ws, ++k) {
       const uint32_t slot = ws % kDSlots;
       if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (ws / kDSlots) & 1, ab, 36))) {
-        ok = false;
+        bad = true;
         break;
       }
-      const int n = min(kDSlotStages, U.kend - s);
-      const uint8_t* cs = s_codes + slot * kDSlotStages * kCodeBytesPerStage + code_off;
-      const uint8_t* ss = s_scales + slot * kDSlotStages * kSS + sc_off;
-      const uint8_t* xr = row + (s - U.kbeg) * (kBK * 2);
-      StageIn a;
-      load_stage<SB>(a, cs, ss, xr);
-      if (n == kDSlotStages) {
-        // both stages' shared-memory loads are in flight before any math
-        StageIn b;
-        load_stage<SB>(b, cs + kCodeBytesPerStage, ss + kSS, xr + kBK * 2);
-        compute_stage<FMT>(a, d, e);
-        compute_stage<FMT>(b, f, h4);
-      } else {
-        compute_stage<FMT>(a, d, e);
+      if (tid == 0 && ws == 0) d_trace_cta(p, 15);
+      const int ns = min(kDSlotStages, U.kend - s);
+#pragma unroll
+      for (int c = 2 * grp; c < kDSlotStages; c += 2 * kDGroups) {  // this group's 128-wide chunks of the slot
+        if (c >= ns) break;
+        const int j = 2 * k + c / 2;  // its activation slot
+        const bool two = ns - c >= 2;
+        const uint8_t* cs = s_codes + (slot * kDSlotStages + c) * kCodeBytesPerStage + code_off;
+        const uint8_t* ss = s_scales + (slot * kDSlotStages + c) * kSS + sc_off;
+        const int xe = xexp[j];
+        float de[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const uint2 w0 = *reinterpret_cast<const uint2*>(cs);
+          const uint2 w1 = *reinterpret_cast<const uint2*>(cs + 8 * 16);
+          stage_mma_f16(w0, w1, xb0 + j * xstep0, de, dq);
+        }
+        if (two) {
+          const uint2 w0 = *reinterpret_cast<const uint2*>(cs + kCodeBytesPerStage);
+          const uint2 w1 = *reinterpret_cast<const uint2*>(cs + kCodeBytesPerStage + 8 * 16);
+          stage_mma_f16(w0, w1, xb1 + j * xstep1, de, dq);
+        }
+        // columns of a missing second stage are zero and their scale bytes were not loaded
+        if (two || t < 2) {
+          if constexpr (FMT == 0) {
+            const uint32_t u0 = *reinterpret_cast<const uint16_t*>(ss);
+            const uint32_t u1 = *reinterpret_cast<const uint16_t*>(ss + 8 * SB);
+            acc0 = fmaf(de[0] + dq[0], f32_scale<0>(u0 & 0xFFu, xe), acc0);
+            acc0 = fmaf(de[1] + dq[1], f32_scale<0>(u0 >> 8, xe), acc0);
+            acc1 = fmaf(de[2] + dq[2], f32_scale<0>(u1 & 0xFFu, xe), acc1);
+            acc1 = fmaf(de[3] + dq[3], f32_scale<0>(u1 >> 8, xe), acc1);
+          } else {
+            acc0 = fmaf((de[0] + dq[0]) + (de[1] + dq[1]), f32_scale<1>(ss[0], xe), acc0);
+            acc1 = fmaf((de[2] + dq[2]) + (de[3] + dq[3]), f32_scale<1>(ss[8 * SB], xe), acc1);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_w[slot]);
-      if (tid == 0) d_trace(p, 1, ws);
+      if (tid == 0) {
+        d_trace(p, 1, ws);
+        if (ws == 0) d_trace_cta(p, 11);
+      }
+    }
+    // row totals: the quad's four threads hold two blocks of each chunk each;
+    // the second K group hands its rows to the first (fixed order)
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
+    if constexpr (kDGroups == 2) {
+      float* red = s_red + rb * kTileRows;
+      if (grp == 1 && t < 2) red[t ? r1 : r0] = t ? acc1 : acc0;
+      bad = named_bar_or(2, kNC, bad);
+      if (t == 0) acc0 += red[r0];
+      if (t == 1) acc1 += red[r1];
+    } else {
+      bad = named_bar_or(2, kNC, bad);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_b[rb]);
     ++bs;
-    if (!ok) break;
+    if (bad) continue;  // the loop ends at the next agreement
     if (!synced) {
-      if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 44))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 44))) bad = true;
       synced = true;
+      if (bad) continue;
     }
-    // every column of D holds the same dot products: d[0] row r0, d[2] row r1
-    const float v0 = (d[0] + e[0]) + (f[0] + h4[0]), v1 = (d[2] + e[2]) + (f[2] + h4[2]);
-    if (t < 2) {
+    if (grp == 0 && t < 2) {
       const int r = t ? r1 : r0;
-      const float v = (t ? v1 : v0) * dsc.scale;
+      const float v = (t ? acc1 : acc0) * dsc.scale;
       if (!U.fc2) {
-        // FC1 split partial in natural row order (splits innermost), times gs13 * 2^63
+        // FC1 split partial in natural row order (splits innermost), times gs13
         int nat;
         if (p.act == 0) {
           const int i = U.tile * 64 + (r >> 5) * 16 + (r & 15);
@@ -714,17 +862,19 @@ __global__ void __launch_bounds__(kDThreads, 2) decode_moe_kernel(const __grid_c
         }
         if (nat >= 0) p.p[((size_t)U.route * wnat + nat) * p.s1_stride + U.split] = v;
       } else {
-        // FC2 split partial times gs2 * 2^63 and the router weight
+        // FC2 split partial times gs2 and the router weight
         const int n = U.tile * kTileRows + r;
         if (n < p.hidden) p.q[((size_t)U.split * R + U.route) * p.hidden + n] = v;
       }
     }
     if (tid == 0) d_trace_cta(p, U.fc2 ? 6 : 7);
-    if (!U.fc2) {
-    } else if (U.split == p.s2 - 1 && (U.route % p.top_k) == 31 - __clz(dsc.mask)) {
+    if (U.fc2 && U.split == p.s2 - 1 && (U.route % p.top_k) == 31 - __clz(dsc.mask)) {
       // the token tile's last unit in unit order: the output warp sums it
       const uint32_t eb = es & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 38))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 38))) {
+        bad = true;
+        continue;
+      }
       if (tid == 0) s_edesc[eb] = dsc;
       __syncwarp();
       if (lane == 0) mbar_arrive(&epi_full[eb]);
