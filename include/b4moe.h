@@ -214,6 +214,19 @@ b4_status b4_set_trace(void* device_buffer, size_t bytes);
  * device wait ran out.  Resets the word to B4_OK.  Not capture-safe. */
 b4_status b4_check_status(void* workspace, b4_stream_t stream);
 
+/* Diagnostic of the device failure path (no passage of the pages defines it:
+ * it exercises the bounded waits every kernel above relies on).  Enqueues on
+ * `stream` one CTA that waits, through the same bounded-wait routine the
+ * kernels use, on an mbarrier phase that no thread completes, with a limit of
+ * `limit_us` microseconds.  When the limit runs out the kernel writes
+ * B4_ERR_TIMEOUT and wait site 90 into the status word at the start of
+ * `workspace` (device memory, at least 8 bytes, caller-owned) and exits
+ * normally: it never traps and never waits longer than the limit.  Read the
+ * result with b4_check_status.  Returns B4_ERR_INVALID_ARGUMENT for a NULL or
+ * short workspace or a limit outside 1 .. 1000000 us, otherwise B4_OK once
+ * launched (B4_ERR_CUDA if the launch fails).  Capture-safe. */
+b4_status b4_wait_self_test(void* workspace, size_t workspace_bytes, uint32_t limit_us, b4_stream_t stream);
+
 /* Allocation-free variant of b4_fused_moe.  The paper has no counterpart:
  * the layer it describes always takes its scratch from the caller.
  *

@@ -42,7 +42,20 @@ def _declared():
 def test_header_declares_the_expected_entry_points():
     names = set(_declared())
     assert {"b4_route_capacity_tokens", "b4_workspace_bytes", "b4_prepared_sizes", "b4_prepare_weights",
-            "b4_route_pack", "b4_fused_moe", "b4_check_status", "b4_status_string", "b4_last_error"} <= names
+            "b4_route_pack", "b4_fused_moe", "b4_check_status", "b4_wait_self_test", "b4_status_string",
+            "b4_last_error"} <= names
+
+
+def test_wait_self_test_validates_before_launch(b4):
+    """The bounded-wait diagnostic refuses a missing or short status word and
+    a limit outside 1 .. 1000000 us before it touches a device."""
+    lib = b4.raw_lib()
+    assert lib.b4_wait_self_test(None, 0, 1000, None) == b4.B4_ERR_INVALID_ARGUMENT
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    assert lib.b4_wait_self_test(fake, 4, 1000, None) == b4.B4_ERR_INVALID_ARGUMENT
+    assert lib.b4_wait_self_test(fake, 8, 0, None) == b4.B4_ERR_INVALID_ARGUMENT
+    assert lib.b4_wait_self_test(fake, 8, 1000001, None) == b4.B4_ERR_INVALID_ARGUMENT
+    assert "limit_us" in b4.last_error()
 
 
 def test_library_exports_every_declared_symbol(b4):

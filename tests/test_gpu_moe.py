@@ -5,9 +5,12 @@ and sum|gpu - oracle| / sum|oracle| <= 5e-3, per call.
 
 * scaled-down workloads with N(0, 0.02) weights quantised by the oracle,
   spanning several tiles and ragged tails, both paths and both activations;
-* the five workloads at full size (random codes), compared on sampled tokens
-  the oracle computes one by one, in the launch configuration the benchmark
-  times;
+* the five workloads at full size (random codes), in the launch
+  configuration the benchmark times, compared on every token up to m = 64 and
+  on 64 chosen tokens above (the most and least loaded experts, both sides of
+  every route-chunk boundary); the MXFP4 shape at full size with the small-m
+  path forced;
+* tokens that select one expert in several top-k slots, on every path;
 * edge cases: m = 0, every route dropped, top-1 single expert, repeated
   calls with one workspace (capacity reuse), a workspace one byte short.
 """
@@ -20,6 +23,7 @@ import torch
 
 import workloads as W
 from gpu_util import DeviceLayer, assert_parity, host_layer, oracle_out
+from oracle import moe as M
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +72,40 @@ FULL = [("tiny", "silu", 4), ("decode", "relu2", 1), ("decode", "relu2", 2), ("d
         ("mxfp4", "silu", 512)]
 
 
+def pick_tokens(hl, n=64, seed=11):
+    """At most n tokens for a full-size comparison: every token when m <= n;
+    otherwise the first and last token, for the two most loaded local experts
+    the tokens of their first and last route and of the routes on both sides
+    of every 128- and 160-route chunk boundary (the grouped kernels' route
+    chunks, in packed route order), two tokens of each of the three least
+    loaded experts, then random tokens."""
+    m, k = hl.ids.shape
+    if m <= n:
+        return np.arange(m)
+    loc = M.local_experts(hl.ids, hl.wl.num_global_experts, hl.wl.num_local_experts, hl.em)
+    routes = {}
+    for t in range(m):
+        for j in range(k):
+            if loc[t, j] >= 0:
+                routes.setdefault(int(loc[t, j]), []).append(t)
+    by_load = sorted(routes, key=lambda e: (len(routes[e]), e))
+    pick = [0, m - 1]
+    for e in by_load[-2:]:
+        r = routes[e]
+        idx = [0, len(r) - 1]
+        for chunk in (128, 160):
+            for c in range(chunk, len(r), chunk):
+                idx += [c - 1, c]
+        pick += [r[i] for i in idx]
+    for e in by_load[:3]:
+        pick += routes[e][:2]
+    pick = list(dict.fromkeys(pick))[:n]
+    rng = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(m), pick)
+    pick += rng.choice(rest, size=n - len(pick), replace=False).tolist()
+    return np.array(sorted(pick))
+
+
 @pytest.mark.parametrize("name,act,m", FULL, ids=[f"{n}-{a}-m{m}" for n, a, m in FULL])
 def test_parity_full_size_sampled(b4, name, act, m):
     wl = W.WORKLOADS[name].with_act(act)
@@ -75,10 +113,45 @@ def test_parity_full_size_sampled(b4, name, act, m):
     dl = DeviceLayer(hl)
     dl.run()
     got = dl.result()
-    rng = np.random.default_rng(11)
-    toks = np.unique(np.concatenate([[0, m - 1], rng.choice(m, size=min(m, 2 if m > 64 else 6), replace=False)]))
+    toks = pick_tokens(hl)
+    assert len(toks) == min(m, 64)
     ref = oracle_out(hl, tokens=toks)
-    assert_parity(got[toks], ref, f"{name}/{act}/m={m} tokens {toks.tolist()}")
+    assert_parity(got[toks], ref, f"{name}/{act}/m={m} ({len(toks)} tokens)")
+
+
+FORCED = [("mxfp4", "silu", 4), ("mxfp4", "relu2", 4), ("mxfp4", "silu", 24), ("decode", "silu", 8)]
+
+
+@pytest.mark.parametrize("name,act,m", FORCED, ids=[f"{n}-{a}-m{m}" for n, a, m in FORCED])
+def test_parity_full_size_decode_forced(b4, name, act, m):
+    """Full-size shapes on the small-m path whatever AUTO would pick: the
+    MXFP4 workload (E8M0 scales per 32, H = 2880 and I = 1440 not multiples of
+    128) on the per-route kernel (m = 4) and the route-grouped one (m = 24)."""
+    wl = W.WORKLOADS[name].with_act(act)
+    hl = host_layer(wl, m, seed=13, weights="random")
+    dl = DeviceLayer(hl, path=b4.PATH_DECODE)
+    dl.run()
+    assert_parity(dl.result(), oracle_out(hl), f"{name}/{act}/m={m} decode forced")
+
+
+DUP = [("decode_s", "relu2", 3), ("decode_s", "silu", 4), ("small_s", "silu", 16), ("mxfp4_s", "silu", 40)]
+
+
+@pytest.mark.parametrize("name,act,m", DUP, ids=[f"{n}-{a}-m{m}" for n, a, m in DUP])
+@pytest.mark.parametrize("path", ["auto", "decode", "grouped"])
+def test_duplicate_expert_ids_within_a_token(b4, name, act, m, path):
+    """A token may select the same expert in several top-k slots: each slot is
+    its own route, weighted by its own router weight."""
+    wl = SCALED[name].with_act(act)
+    hl = host_layer(wl, m, seed=zlib.crc32(f"dup/{name}/{m}".encode()) % 1000)
+    k = wl.top_k
+    hl.ids[0, 1] = hl.ids[0, 0]                       # two slots, one expert
+    hl.ids[m - 1, :] = hl.ids[m - 1, 0]               # every slot the same expert
+    if m > 2:
+        hl.ids[1, k - 1] = hl.ids[1, 0]               # first and last slot
+    dl = DeviceLayer(hl, path={"auto": b4.PATH_AUTO, "decode": b4.PATH_DECODE, "grouped": b4.PATH_GROUPED}[path])
+    dl.run()
+    assert_parity(dl.result(), oracle_out(hl), f"dup {name}/{act}/m={m}/{path}")
 
 
 def test_m_zero_is_a_noop(b4):

@@ -36,7 +36,8 @@ def _noalloc(dl, out, status, stream=None):
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,wl,m,path", CASES, ids=[c[0] for c in CASES])
 def test_noalloc_matches_workspace_entry_point(name, wl, m, path):
-    hl = host_layer(wl, m, seed=31)
+    # the full-size case compares two GPU entry points only: random codes (no quantiser run)
+    hl = host_layer(wl, m, seed=31, weights="random" if name.endswith("_full") else "quantized")
     dl = DeviceLayer(hl, path=path)
     assert dl.b4.workspace_bytes(dl.cfg, dl.act) <= dl.b4.NOALLOC_SCRATCH_BYTES
     dl.run()
@@ -61,19 +62,34 @@ def test_noalloc_matches_workspace_entry_point(name, wl, m, path):
             assert torch.equal(out, dl.out), f"{name} call {call} differs from b4_fused_moe"
 
 
+AFTER = [("grouped", CASES[1][1], 120, 9, 2), ("decode", CASES[0][1], 64, 4, 1)]
+
+
 @pytest.mark.gpu
-def test_noalloc_after_another_shape():
-    """A call on a smaller shape after a larger one reads nothing the larger left."""
-    big = DeviceLayer(host_layer(CASES[1][1], 120, seed=32), path=2)
-    small = DeviceLayer(host_layer(CASES[1][1], 9, seed=33), path=2)
+@pytest.mark.parametrize("name,wl,m_big,m_small,path", AFTER, ids=[a[0] for a in AFTER])
+def test_noalloc_after_another_shape(name, wl, m_big, m_small, path):
+    """A call on a smaller shape after a larger one reads nothing the larger
+    left (partials, markers, counters), and reports a clear status word.  On
+    the decode path the larger call runs the route-grouped kernel and the
+    smaller one the per-route kernel."""
+    big = DeviceLayer(host_layer(wl, m_big, seed=32), path=path)
+    small = DeviceLayer(host_layer(wl, m_small, seed=33), path=path)
     small.run()
     want = small.result()
     tmp = torch.empty_like(big.out)
     out = torch.empty_like(small.out)
-    _noalloc(big, tmp, None)
-    _noalloc(small, out, None)
+    status = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    _noalloc(big, tmp, status)
     torch.cuda.synchronize()
-    assert_parity(bf16_to_np(out), want, "small after big")
+    assert status.tolist() == [0, 0], f"device status after the larger call {status.tolist()}"
+    status.fill_(-1)
+    _noalloc(small, out, status)
+    torch.cuda.synchronize()
+    assert status.tolist() == [0, 0], f"device status after the smaller call {status.tolist()}"
+    if path == 2:
+        assert_parity(bf16_to_np(out), want, f"{name}: small after big")
+    else:
+        assert torch.equal(out, small.out), f"{name}: small after big differs from b4_fused_moe"
 
 
 def test_noalloc_refuses_oversized_shape():

@@ -83,6 +83,7 @@ def _load():
         "b4_linear_workspace_bytes": (S, [CP]),
         "b4_linear": (I32, [CP, P, P, P, P, P, P, S, P]),
         "b4_check_status": (I32, [P, P]),
+        "b4_wait_self_test": (I32, [P, S, ctypes.c_uint32, P]),
         "b4_set_timing_events": (I32, [ctypes.POINTER(P), I32]),
         "b4_set_trace": (I32, [P, S]),
         "b4_status_string": (ctypes.c_char_p, [I32]),
@@ -107,6 +108,7 @@ EXPORTED = (
     "b4_linear_workspace_bytes",
     "b4_linear",
     "b4_check_status",
+    "b4_wait_self_test",
     "b4_set_timing_events",
     "b4_set_trace",
     "b4_status_string",
@@ -331,6 +333,14 @@ def set_trace(buffer):
 
 def check_status(workspace, stream=None):
     _check(_lib.b4_check_status(_ptr(workspace), _stream(stream)))
+
+
+def wait_self_test(workspace, limit_us, stream=None):
+    """Enqueue the bounded-wait diagnostic (b4_wait_self_test): a wait that no
+    arrival completes runs out after limit_us and leaves B4_ERR_TIMEOUT in the
+    workspace's status word (read it with check_status)."""
+    _need(workspace, torch.uint8, "workspace")
+    _check(_lib.b4_wait_self_test(_ptr(workspace), workspace.numel(), int(limit_us), _stream(stream)))
 
 
 def raw_lib():

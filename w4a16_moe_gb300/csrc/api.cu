@@ -31,6 +31,7 @@ cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stre
 cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream);
 size_t route_pack_smem_bytes(int num_local_experts);
 cudaError_t launch_prepare(const PrepareParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_self_test(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
 }  // namespace b4
 
 using namespace b4;
@@ -901,6 +902,15 @@ b4_status b4_set_timing_events(void* const* events, int32_t n) {
   if (n > 0 && (!events || n < 2)) return fail(B4_ERR_INVALID_ARGUMENT, "need NULL or at least 2 events");
   g_events = n > 0 ? events : nullptr;
   g_num_events = n > 0 ? n : 0;
+  return B4_OK;
+}
+
+b4_status b4_wait_self_test(void* workspace, size_t workspace_bytes, uint32_t limit_us, b4_stream_t stream) {
+  if (!workspace || workspace_bytes < 8) return fail(B4_ERR_INVALID_ARGUMENT, "workspace needs >= 8 bytes");
+  if (limit_us < 1 || limit_us > 1000000) return fail(B4_ERR_INVALID_ARGUMENT, "limit_us must be in 1 .. 1000000");
+  const cudaError_t e = b4::launch_wait_self_test(reinterpret_cast<uint32_t*>(workspace),
+                                                  1000ull * limit_us, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
   return B4_OK;
 }
 

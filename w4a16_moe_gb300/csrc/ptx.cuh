@@ -93,18 +93,24 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 constexpr uint32_t kWaitSuspendNs = 20000;
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab, uint32_t where) {
+// Bounded wait for the phase with the given parity to complete: after
+// limit_ns the wait records B4_ERR_TIMEOUT and the wait site in the status
+// word, raises the CTA's abort flag and returns false (it never traps).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, const Abort& ab, uint32_t where,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) return true;
     if (ab.raised()) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       ab.raise(where);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab, uint32_t where) {
+  return mbar_wait_limit(bar, parity, ab, where, kWaitLimitNs);
 }
 
 // -------------------------------------------------------- async-proxy copies
