@@ -74,6 +74,7 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
+#include "coop_launch.cuh"
 #include "decode_stage.cuh"
 #include "dequant.cuh"
 #include "kernels.cuh"
@@ -552,7 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_grouped_kernel(const __gri
     mbar_init(setup_bar, 1);
     mbar_init(grid_bar, 1);
     fence_mbar_init();
+    pdl_launch_dependents();  // the next kernel may launch and set up meanwhile
   }
+  pdl_wait();  // launched with PDL: nothing of this call is read or written before the kernel before it is done
 
   // Before the grid barrier: fill both partial buffers with the not-written
   // marker, clear the FC1 tile flags and the status word, and zero the output
@@ -1021,17 +1024,7 @@ static cudaError_t launch_dg(const SmallGroupParams& p, int grid, cudaStream_t s
   const size_t smem = dg::Smem<FMT, SETS>::total(p.m * p.top_k);
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(dg::kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_cooperative(kern, grid, dg::kThreads, smem, stream, p);
 }
 
 // Resident CTAs per SM of the kernel with `smem` bytes (the cooperative launch

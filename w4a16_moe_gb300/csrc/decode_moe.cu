@@ -83,6 +83,7 @@
 
 #include <mutex>
 
+#include "coop_launch.cuh"
 #include "decode_stage.cuh"
 #include "dequant.cuh"
 #include "kernels.cuh"
@@ -427,7 +428,9 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     fence_mbar_init();
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(s_zero)[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) pdl_launch_dependents();  // the next kernel may launch and set up meanwhile
   __syncthreads();
+  pdl_wait();  // launched with PDL: nothing of this call is read or written before the kernel before it is done
 
   // The producers resolve the CTA's first unit and start its weight stream
   // and (FC1) x slice before the grid barrier: neither touches the partial
@@ -898,17 +901,7 @@ cudaError_t launch_decode_fmt(const DecodeParams& p, int grid, cudaStream_t stre
   const size_t smem = DSmem<FMT>::total;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kDThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_cooperative(kern, grid, kDThreads, smem, stream, p);
 }
 
 // Resident CTAs per SM of the fused decode kernel on the current device: a
