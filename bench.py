@@ -524,10 +524,12 @@ def kernel_source_hash(path):
 
 def kernel_family(b):
     """Which GEMM kernels serve the call: the per-route small-m kernel
-    (m <= 4), the route-grouped small-m kernel, or the grouped weights-on-N /
-    weights-on-M kernels (api.cu's dispatch rule)."""
+    (m <= 4, or 2 m top_k <= E_local), the route-grouped small-m kernel, or the
+    grouped weights-on-N / weights-on-M kernels (api.cu's dispatch rule)."""
     if b.decode:
-        return "decode" if b.m <= 4 else "decode_grouped"
+        wl = b.wl
+        per_route = b.m <= 4 or (not isinstance(b, LinearBench) and 2 * b.m * wl.top_k <= wl.num_local_experts)
+        return "decode" if per_route else "decode_grouped"
     wl = b.wl
     return "grouped_wn" if b.m * wl.top_k < 96 * wl.num_local_experts else "grouped"
 

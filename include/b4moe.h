@@ -68,8 +68,9 @@ typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activ
 
 /* Execution path of b4_fused_moe.  DECODE is the small-m path (accepted for
  * m <= B4_DECODE_MAX_M): one cooperative launch, a per-route kernel for
- * m <= 4 and a route-grouped kernel (an expert's weights streamed once per
- * group of up to 16 of its routes) above.  GROUPED is the route-packed
+ * m <= 4 or 2 * m * top_k <= num_local_experts (few routes per expert), a
+ * route-grouped kernel (an expert's weights streamed once per group of up to
+ * 16 of its routes) otherwise.  GROUPED is the route-packed
  * tcgen05 path.  AUTO takes DECODE for m <= 16 and GROUPED above: the
  * crossover flashinfer PR #4255 (Reviewer Notes) leaves to each card, as
  * measured on GB300; b4_linear's AUTO takes its small-m kernel for m <= 4. */

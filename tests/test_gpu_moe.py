@@ -34,6 +34,8 @@ SCALED = {
     "small_s": W.WORKLOADS["small"].scaled(hidden=320, inter=192, experts=16),
     "prefill_s": W.WORKLOADS["prefill"].scaled(hidden=512, inter=320, experts=12),
     "mxfp4_s": W.WORKLOADS["mxfp4"].scaled(hidden=352, inter=160, experts=7),
+    # many experts, few routes each: the small-m path's per-route kernel above m = 4
+    "decode_w": W.WORKLOADS["decode"].scaled(hidden=256, inter=192, experts=128),
 }
 CASES = [
     ("tiny", "silu", 4), ("tiny", "silu", 1),
@@ -43,6 +45,7 @@ CASES = [
     ("mxfp4_s", "silu", 100), ("mxfp4_s", "relu2", 9),
     # many routes per expert: the weights-on-M grouped kernel (m * top_k >= 96 * E_l)
     ("mxfp4_s", "silu", 300), ("tiny", "relu2", 512),
+    ("decode_w", "relu2", 6), ("decode_w", "silu", 8), ("decode_w", "relu2", 9),
 ]
 
 

@@ -72,13 +72,17 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
 
 // Path choice.  flashinfer PR #4255 (Reviewer Notes) caps its decode path at
 // m = 4 and notes that the crossover varies by card; on GB300 the small-m
-// kernels were measured against the grouped tcgen05 GEMMs (one call, L2
-// cold): the per-route decode kernel is fastest up to m = 4, the route-grouped
-// kernel from m = 8 to 16 (decode E128 k8 m = 8: 178 vs 213 us; small-batch
-// E64 k6 m = 16: 97 vs 101 us), the grouped GEMMs from m = 32 (small-batch
-// m = 32: 133 vs 141 us).
+// kernels were measured against the grouped tcgen05 GEMMs (K back-to-back
+// calls, weights L2-cold): the route-grouped kernel beats the grouped GEMMs up
+// to m = 16 (decode E128 k8 m = 16: 243 vs 289 us; small-batch E64 k6 m = 16:
+// 85 vs 101 us), the grouped GEMMs win from m = 32 (small-batch m = 32).
+// Inside the small-m path the per-route kernel re-reads an expert's weights
+// for each route that selects it but streams about twice as fast: it wins
+// while routes are few per local expert (decode m = 8, 64 routes on 128
+// experts: 122 vs 165 us), the route-grouped kernel once experts repeat
+// (small-batch m = 8, 48 routes on 64 experts: 62 vs 68 us).
 constexpr int kDecodeAutoMaxM = 16;  // AUTO takes a small-m kernel up to here
-constexpr int kPerRouteMaxM = 4;     // the small-m path's per-route kernel up to here, route-grouped above
+constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while 2 m top_k <= E_local
 constexpr int kLinearSmallMaxM = 4;  // b4_linear's AUTO takes the small-m kernel up to here
 constexpr int kDecodeW0 = 4;        // small-m partition: a stage costs kDecodeW0 + its route column sets
 constexpr int kMaxSplits = 8;
@@ -473,7 +477,9 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   fp.out = out;
 
   cudaError_t e;
-  if (decode && cfg->m <= kPerRouteMaxM) {
+  const bool per_route =
+      cfg->m <= kPerRouteMaxM || 2LL * cfg->m * cfg->top_k <= (long long)cfg->num_local_experts;
+  if (decode && per_route) {
     // the per-route kernel: one unit per (route, tile, K split)
     const int R = cfg->m * cfg->top_k;
     int occ = 0;
