@@ -118,13 +118,16 @@ def call_accounting(wl, m, ids, em):
             "fc2_bytes": b2, "flops": f13 + f2, "experts_hit": int(len(hit)), "routes": r_valid}
 
 
-def weight_copies(b, dev):
+def weight_copies(b, dev, n=None):
     """Device copies of the prepared weights, cycled call by call so that no
     call finds its weights in L2: enough copies that three times the L2 size
-    passes between two calls on the same copy (at least 2, at most 64)."""
+    passes between two calls on the same copy (at least 2, at most 64), or
+    exactly n (a profiling run that keeps the device footprint small)."""
     import math
 
     torch = b.torch
+    if n is not None and n > 0:
+        return [dev] + [{k: (None if v is None else v.clone()) for k, v in dev.items()} for _ in range(n - 1)]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     per_call = statistics.mean(d["acct"]["weight_bytes"] for d in b.draws)
     n = int(min(64, max(2, math.ceil(3 * l2 / max(per_call, 1)))))
@@ -187,7 +190,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm
 class Bench:
-    def __init__(self, wl, m, seed=7, path=None):
+    def __init__(self, wl, m, seed=7, path=None, copies=None):
         import torch
 
         import w4a16_moe_gb300 as b4
@@ -220,14 +223,16 @@ class Bench:
                 "xd": torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16),
                 "idsd": torch.from_numpy(ids).cuda(), "wtsd": torch.from_numpy(wts).cuda(),
                 "acct": call_accounting(wl, m, ids, self.em_np)})
-        self.devs = weight_copies(self, dev)
+        self.devs = weight_copies(self, dev, copies)
         self.ws = torch.empty(b4.workspace_bytes(self.cfg, self.act), dtype=torch.uint8, device="cuda")
         self.out = torch.empty(m, wl.hidden, dtype=torch.bfloat16, device="cuda")
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         self.flush_sink = torch.empty(1, dtype=torch.int32, device="cuda")
         self.stream = torch.cuda.Stream()
-        # the library's AUTO rule: a small-m kernel (one cooperative launch) up to m = 16
-        self.decode = self.path == b4.PATH_DECODE or (self.path == b4.PATH_AUTO and m <= 16)
+        # the library's AUTO rule: a small-m kernel (one cooperative launch) up to m = 16, and up
+        # to m = 64 while there are at most two routes per local expert
+        self.decode = self.path == b4.PATH_DECODE or (self.path == b4.PATH_AUTO and (
+            m <= 16 or (m <= 64 and m * wl.top_k <= 2 * wl.num_local_experts)))
         self.n_kernels = 1 if self.decode else 4  # timed intervals: decode kernel; pack, permute + FC1, FC2, finalize
         self.launches = 1 if self.decode else 5  # this library's kernels per call
 
@@ -447,9 +452,10 @@ KERNEL_SOURCES = {
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
-    ("decode", "decode:relu2", 1): ("eea3645ca0961c6e", 56_748_288 + 338_688),
-    ("grouped", "prefill:silu", 2048): ("104a4a1a5aee0830", 1_041_019_392 + 81_157_376 + 599_991_296 + 81_412_608),
-    ("grouped_wn", "small:silu", 16): ("14dde3c0816bca2d", 114_006_016 + 3_177_472 + 57_212_672 + 78_592),
+    ("decode", "decode:relu2", 1): ("6afbab8cbd419728", 56_730_368 + 516_096),
+    ("decode_grouped", "small:silu", 16): ("fb6fd93ea1c81c44", 172_840_704 + 11_637_248),
+    ("grouped", "prefill:silu", 2048): ("7388b4351aa42727", 1_040_615_168 + 81_186_304 + 599_474_944 + 81_475_584),
+    ("grouped_wn", "small:silu", 64): ("56f8d50e964203f8", 180_107_776 + 4_443_904 + 90_863_616 + 293_888),
 }
 
 
@@ -664,6 +670,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-crossover", action="store_true")
+    ap.add_argument("--weight-copies", type=int, default=0,
+                    help="device copies of the weights cycled by the timed calls (0: enough to keep them L2-cold)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode:relu2:1",
                     help="name:act:m of the timed workload (default: the decode headline)")
@@ -696,7 +704,7 @@ def main():
     peaks = load_peaks()
     name, act, m = args.workload.split(":")
     m = int(m)
-    b = Bench(W.WORKLOADS[name].with_act(act), m)
+    b = Bench(W.WORKLOADS[name].with_act(act), m, copies=args.weight_copies or None)
     res = b.run(args.steps, args.warmup, barrier, with_e2e=True, with_clocks=True, gpu_index=local)
     head = summarize(b, res, peaks)
     us = head["us_per_call"]
@@ -712,7 +720,9 @@ def main():
                    "l2": (f"inputs larger than L2: consecutive calls cycle {len(b.devs)} device copies of the "
                           f"prepared weights and {DRAWS} routing/activation draws, so >= 3x the L2 size of other "
                           "weights is read between two calls on the same copy; L2 flushed (512 MiB written, then "
-                          "read back) before the timed region"),
+                          "read back) before the timed region") if not args.weight_copies else
+                         (f"profiling run: {args.weight_copies} weight copies set by --weight-copies (calls may "
+                          "find weights in L2); L2 flushed before the timed region"),
                    "launch": f"one CUDA graph of the {args.steps} timed calls, replayed once",
                    "us_per_call_single": head["us_per_call_single"],
                    "single_note": "one call per graph replay, L2 flushed before each (cold L2 and cold code)",

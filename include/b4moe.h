@@ -71,9 +71,11 @@ typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activ
  * m <= 4 or 2 * m * top_k <= num_local_experts (few routes per expert), a
  * route-grouped kernel (an expert's weights streamed once per group of up to
  * 16 of its routes) otherwise.  GROUPED is the route-packed
- * tcgen05 path.  AUTO takes DECODE for m <= 16 and GROUPED above: the
- * crossover flashinfer PR #4255 (Reviewer Notes) leaves to each card, as
- * measured on GB300; b4_linear's AUTO takes its small-m kernel for m <= 4. */
+ * tcgen05 path.  AUTO takes DECODE for m <= 16, and for m <= 64 while
+ * m * top_k <= 2 * num_local_experts (at most two routes per expert on
+ * average), GROUPED otherwise: the crossover flashinfer PR #4255 (Reviewer
+ * Notes) leaves to each card, as measured on GB300; b4_linear's AUTO takes its
+ * small-m kernel for m <= 4. */
 typedef enum b4_path { B4_PATH_AUTO = 0, B4_PATH_DECODE = 1, B4_PATH_GROUPED = 2 } b4_path;
 
 #define B4_DECODE_MAX_M 64

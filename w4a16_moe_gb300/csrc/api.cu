@@ -433,7 +433,14 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
 
   const int act = activation == B4_ACT_SILU_SWIGLU ? 0 : 1;
   const int fmt = cfg->format;
-  bool decode = cfg->path == B4_PATH_DECODE || (cfg->path == B4_PATH_AUTO && cfg->m <= kDecodeAutoMaxM);
+  // AUTO: the small-m path up to m = 16, and up to B4_DECODE_MAX_M while an
+  // expert receives at most two routes on average (decode E128 k8 m = 32:
+  // 334 vs 368 us on the grouped GEMMs; small-batch E64 k6 m = 32, three per
+  // expert: the grouped GEMMs win)
+  bool decode = cfg->path == B4_PATH_DECODE ||
+                (cfg->path == B4_PATH_AUTO &&
+                 (cfg->m <= kDecodeAutoMaxM ||
+                  (cfg->m <= B4_DECODE_MAX_M && (long long)cfg->m * cfg->top_k <= 2LL * cfg->num_local_experts)));
   if (decode && !L.decode_ok) decode = false;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
