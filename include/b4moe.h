@@ -203,13 +203,21 @@ b4_status b4_set_timing_events(void* const* events, int32_t n);
  * running counters, FC1 at int64 offset 0 and FC2 at 10240; kinds: weight
  * stage issued, A stage written to tensor memory (weights on M) or B stage
  * dequantised (weights on N), MMA stage issued, activation stage ready, unit
- * epilogue done.  Small-m path (one kernel): %globaltimer nanoseconds of each
- * CTA at phase boundaries, entry [kind][CTA]: 0 start, 1 group table built,
- * 2 first unit published, 3 first weight copy issued, 4 first slot
- * computed, 5 last FC1 unit stored, 6 first FC2 slot computed, 7 compute
- * done, 8 epilogue done, 9 first FC2 unit's FC1 tiles ready, 10 grid
- * barrier seen, 11 weight stream done, 12 last FC1 tile's h built, 13 last
- * output row written.  Entries not reached are left untouched. */
+ * epilogue done.  Small-m path (one kernel), route-grouped kernel:
+ * %globaltimer nanoseconds of each CTA at phase boundaries, entry [kind][CTA]:
+ * 0 start, 1 group table built, 2 first unit published, 3 first weight copy
+ * issued, 4 first slot computed, 5 last FC1 unit stored, 6 first FC2 slot
+ * computed, 7 compute done, 8 epilogue done, 9 first FC2 unit's FC1 tiles
+ * ready, 10 grid barrier seen, 11 weight stream done, 12 last FC1 tile's h
+ * built, 13 last output row written, 14 buffers filled, 15 route ids read.
+ * Per-route kernel: clock64() of CTA 0 as [kind][index] for kinds 0 (weight
+ * slot issued), 1 (slot computed), 2 (start), 3 (unit begun), 4 (unit
+ * done); %globaltimer of each CTA for kinds 5 (start), 6 (last FC2 partial
+ * stored), 7 (last FC1 partial stored), 8 (compute done), 9 (output warp
+ * done), 11 (first slot computed), 12 (first x row converted), 13 (grid
+ * barrier complete), 14 (first unit's weights issued), 15 (first slot
+ * landed); kind 10 holds each CTA's SM.  Entries not reached are left
+ * untouched. */
 b4_status b4_set_trace(void* device_buffer, size_t bytes);
 
 /* Synchronises `stream`, then reads the device status word of `workspace`
