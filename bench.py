@@ -490,11 +490,11 @@ class LinearBench(Bench):
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         self.flush_sink = torch.empty(1, dtype=torch.int32, device="cuda")
         self.stream = torch.cuda.Stream()
-        # the fused small-m kernel (one launch) for m <= 4; above, the grouped
+        # the fused small-m kernels (one launch) for m <= 16; above, the grouped
         # GEMM: with fewer (chunk, tile pair) units than SMs it splits K and adds
         # fp32 partials (events: memset + route pack, GEMM, rounding pass),
         # otherwise it stores bf16 (route pack, GEMM)
-        self.decode = m <= 4
+        self.decode = m <= 16  # AUTO: the small-m kernels (per-route m <= 2, route-grouped above)
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         k_split = m < 96 and -(-m // 128) * ((-(-n // 128) + 1) // 2) < sms
         self.n_kernels = 1 if self.decode else (3 if k_split else 2)
@@ -534,7 +534,10 @@ def kernel_family(b):
     grouped weights-on-N / weights-on-M kernels (api.cu's dispatch rule)."""
     if b.decode:
         wl = b.wl
-        per_route = b.m <= 4 or (not isinstance(b, LinearBench) and 2 * b.m * wl.top_k <= wl.num_local_experts)
+        if isinstance(b, LinearBench):
+            per_route = b.m <= 2
+        else:
+            per_route = b.m <= 4 or 2 * b.m * wl.top_k <= wl.num_local_experts
         return "decode" if per_route else "decode_grouped"
     wl = b.wl
     return "grouped_wn" if b.m * wl.top_k < 96 * wl.num_local_experts else "grouped"

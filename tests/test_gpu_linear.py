@@ -22,7 +22,8 @@ NV, MX = W.NV, W.MX
 CASES = [
     # name, fmt, m, n, k, path ("auto" / "decode" / "grouped"), weights
     ("nv_m1_full", NV, 1, 4096, 4096, "auto", "random"),
-    ("nv_m3", NV, 3, 640, 1024, "auto", "quantized"),
+    ("nv_m2", NV, 2, 768, 1536, "auto", "quantized"),      # per-route small-m kernel
+    ("nv_m3", NV, 3, 640, 1024, "auto", "quantized"),      # route-grouped small-m kernel
     ("nv_m16", NV, 16, 384, 2048, "auto", "quantized"),
     ("nv_m64", NV, 64, 256, 512, "auto", "quantized"),
     ("nv_m40_decode", NV, 40, 256, 1024, "decode", "quantized"),

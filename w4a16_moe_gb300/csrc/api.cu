@@ -83,7 +83,13 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
 // (small-batch m = 8, 48 routes on 64 experts: 62 vs 68 us).
 constexpr int kDecodeAutoMaxM = 16;  // AUTO takes a small-m kernel up to here
 constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while 2 m top_k <= E_local
-constexpr int kLinearSmallMaxM = 4;  // b4_linear's AUTO takes the small-m kernel up to here
+// b4_linear (N = K = 4096, back-to-back calls): the per-route kernel re-reads W
+// per token (m = 1 / 2 / 3 / 4: 9.8 / 13.2 / 16.3 / 18.8 us), the route-grouped
+// kernel reads it once per 8 tokens (14.4 - 14.7 us for m = 1..4, 15.6 at m = 8,
+// 19.8 at m = 16) against the K-split grouped GEMM (21.9 us at m = 8 and 16, on
+// par from m = 32).
+constexpr int kLinearSmallMaxM = 16;    // b4_linear's AUTO takes the small-m kernels up to here
+constexpr int kLinearPerRouteMaxM = 2;  // b4_linear's small-m path: the per-route kernel up to here
 constexpr int kDecodeW0 = 4;        // small-m partition: a stage costs kDecodeW0 + its route column sets
 constexpr int kMaxSplits = 8;
 
@@ -695,7 +701,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
   const TensorGeom g1 = tensor_geom(0, 1, K, N);
   cudaError_t e;
 
-  if (small && m <= kPerRouteMaxM) {
+  if (small && m <= kLinearPerRouteMaxM) {
     // The fused small-m kernel: K-split GEMV units, then one output unit per
     // (token, 128 columns) that sums the split partials into out.
     int occ = 0;
