@@ -68,7 +68,7 @@ typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activ
 
 /* Execution path of b4_fused_moe.  DECODE is the small-m path (accepted for
  * m <= B4_DECODE_MAX_M): one cooperative launch, a per-route kernel for
- * m <= 4 or 2 * m * top_k <= num_local_experts (few routes per expert), a
+ * m <= 4 or m * top_k <= num_local_experts (few routes per expert), a
  * route-grouped kernel (an expert's weights streamed once per group of up to
  * 16 of its routes) otherwise.  GROUPED is the route-packed
  * tcgen05 path.  AUTO takes DECODE for m <= 16, and for m <= 64 while
@@ -125,8 +125,9 @@ b4_status b4_prepared_sizes(const b4_moe_config* cfg, int32_t which, int32_t act
  * src_scales [E_l, N, K/g] uint8 (E4M3 for NVFP4, g = 16; E8M0 for MXFP4, g = 32).
  * dst_codes, dst_scales: b4_prepared_sizes bytes each, 16-byte aligned.
  * The serving layout tiles rows by 128 and K by 64, pads both with zeros,
- * interleaves gate/up rows in groups of 16 for SwiGLU, re-encodes each E2M1
- * nibble for a table-lookup dequantiser, and re-encodes the block scales.
+ * interleaves gate/up rows in groups of 16 for SwiGLU, reorders the E2M1
+ * nibbles of every 8 codes into the pairing of the hardware FP4 conversion,
+ * and re-encodes the block scales.
  * Blocks whose scale decodes to zero are stored with zero codes (the product
  * is zero either way); a negative E4M3 scale is folded into the code signs.
  *

@@ -219,7 +219,8 @@ __global__ void probe_mma_sw128_kernel(const __grid_constant__ CUtensorMap tm, c
   if (warp == 0) tmem_dealloc(base, 512);
 }
 
-// Dequantise serving-layout blocks (one 128-row x 64-element stage each).
+// Dequantise prepared blocks (one 128-row x 64-element stage each) with the
+// table-lookup dequantiser.
 template <int FMT>
 __global__ void probe_dequant_kernel(const uint8_t* codes, const uint8_t* scales, uint16_t* out) {
   const int blk = blockIdx.x, r = threadIdx.x;
@@ -239,8 +240,8 @@ __global__ void probe_dequant_kernel(const uint8_t* codes, const uint8_t* scales
   }
 }
 
-// The small-m kernels' dequantiser: serving words -> plain nibble pairs ->
-// hardware FP4 conversion to f16, times the fp32 block scale; one thread per
+// The per-route small-m kernel's dequantiser: prepared words (plain nibble
+// pairs) -> hardware FP4 conversion to f16, times the fp32 block scale; one thread per
 // weight row, one block per 64-wide stage, fp32 output in K order.
 template <int FMT>
 __global__ void probe_dequant_f16_kernel(const uint8_t* codes, const uint8_t* scales, float* out) {
@@ -255,7 +256,7 @@ __global__ void probe_dequant_f16_kernel(const uint8_t* codes, const uint8_t* sc
   for (int q = 0; q < 8; ++q) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(cs + (q >> 2) * 2048 + r * 16 + (q & 3) * 4);
     uint32_t h[4];
-    e2m1x8_to_f16x2(serving_to_nibbles(w), h[0], h[1], h[2], h[3]);
+    e2m1x8_to_f16x2(w, h[0], h[1], h[2], h[3]);
     for (int b = 0; b < 4; ++b) {
       const __half2 v = *reinterpret_cast<const __half2*>(&h[b]);
       const int klo = q * 8 + el_lo[b], khi = q * 8 + el_hi[b];

@@ -46,6 +46,8 @@ CASES = [
     # many routes per expert: the weights-on-M grouped kernel (m * top_k >= 96 * E_l)
     ("mxfp4_s", "silu", 300), ("tiny", "relu2", 512),
     ("decode_w", "relu2", 6), ("decode_w", "silu", 8), ("decode_w", "relu2", 9),
+    # as many routes as local experts: the per-route kernel's boundary (m * top_k = E_l)
+    ("decode_w", "relu2", 16),
     # AUTO above m = 16 while an expert gets at most two routes: the small-m path
     ("decode_w", "relu2", 24),
 ]

@@ -73,16 +73,17 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
 // Path choice.  flashinfer PR #4255 (Reviewer Notes) caps its decode path at
 // m = 4 and notes that the crossover varies by card; on GB300 the small-m
 // kernels were measured against the grouped tcgen05 GEMMs (K back-to-back
-// calls, weights L2-cold): the route-grouped kernel beats the grouped GEMMs up
-// to m = 16 (decode E128 k8 m = 16: 243 vs 289 us; small-batch E64 k6 m = 16:
-// 85 vs 101 us), the grouped GEMMs win from m = 32 (small-batch m = 32).
+// calls, weights L2-cold): the small-m kernels beat the grouped GEMMs up to
+// m = 16 (decode E128 k8 m = 16: 195 vs 289 us; small-batch E64 k6 m = 16:
+// 91 vs 101 us), the grouped GEMMs win from m = 32 (small-batch m = 32).
 // Inside the small-m path the per-route kernel re-reads an expert's weights
-// for each route that selects it but streams about twice as fast: it wins
-// while routes are few per local expert (decode m = 8, 64 routes on 128
-// experts: 122 vs 165 us), the route-grouped kernel once experts repeat
-// (small-batch m = 8, 48 routes on 64 experts: 62 vs 68 us).
+// for each route that selects it but streams about twice as fast (4.6 against
+// 2.1 TB/s): it wins while there are no more routes than local experts
+// (decode m = 16, 128 routes on 128 experts: 195 vs 271 us; small-batch m = 8,
+// 48 routes on 64 experts: 60 vs 66 us), the route-grouped kernel once experts
+// repeat (small-batch m = 16, 96 routes on 64 experts: 112 vs 91 us).
 constexpr int kDecodeAutoMaxM = 16;  // AUTO takes a small-m kernel up to here
-constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while 2 m top_k <= E_local
+constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while m top_k <= E_local
 // b4_linear (N = K = 4096, back-to-back calls): the per-route kernel re-reads W
 // per token (m = 1 / 2 / 3 / 4: 9.8 / 13.2 / 16.3 / 18.8 us), the route-grouped
 // kernel reads it once per 8 tokens (14.4 - 14.7 us for m = 1..4, 15.6 at m = 8,
@@ -491,7 +492,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
 
   cudaError_t e;
   const bool per_route =
-      cfg->m <= kPerRouteMaxM || 2LL * cfg->m * cfg->top_k <= (long long)cfg->num_local_experts;
+      cfg->m <= kPerRouteMaxM || (long long)cfg->m * cfg->top_k <= (long long)cfg->num_local_experts;
   if (decode && per_route) {
     // the per-route kernel: one unit per (route, tile, K split)
     const int R = cfg->m * cfg->top_k;

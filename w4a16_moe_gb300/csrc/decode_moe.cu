@@ -9,8 +9,8 @@
 // FC1 and FC2 waits for a memory fence.
 //
 // Work units, in this order: FC1 units (route, 128-row tile, K split), then FC2
-// units (route, 128-row tile of H, K split).  CTA b takes units b, b + G, ...,
-// in increasing order.
+// units (route, 128-row tile of H, K split).  CTA b's first two units are b and
+// b + G (G CTAs); later ones are claimed from a counter in unit order.
 //
 //   warp 0        streams the unit's packed codes and scales, four 64-wide K
 //                 stages per slot of a shared-memory ring (two copies of
@@ -31,7 +31,8 @@
 //                 bf16(act(sum of the FC1 partials)), as f16 slots.  With two
 //                 K groups (one CTA per SM) the second group takes the second
 //                 half of every slot and hands its row sums to the first.
-//   last warp     stores the bf16 output of a token's 128-column tile: it sums
+//   last warp     makes the CTA's grid-barrier arrival and wait (below), then
+//                 stores the bf16 output of a token's 128-column tile: it sums
 //                 the FC2 partials of the token's valid routes (ascending
 //                 top-k slot, then split) for the tile's last unit in unit
 //                 order.  Fixed orders: the output is bitwise reproducible.
@@ -42,9 +43,11 @@
 // until none of them holds the marker (a 4-byte store is seen whole or not at
 // all).  The barrier is split: a CTA arrives as soon as its share of the fill
 // is done, and only its first partial store or read waits for the other
-// CTAs, so the first unit's weight stream and arithmetic run meanwhile.  A reader only ever waits for units earlier in unit order, each CTA
-// runs its units in order, and a cooperative launch keeps every CTA resident,
-// so every wait ends; every wait is bounded as well.  Before the barrier the
+// CTAs, so the first two units' weight streams and the first unit's
+// arithmetic run meanwhile.  A reader only ever waits for units earlier in
+// unit order, each CTA runs its units in increasing order, and a cooperative
+// launch keeps every CTA resident, so every wait ends; every wait is bounded
+// as well.  Before the barrier the
 // CTAs also clear the status word and zero the output rows of tokens without
 // a valid route.
 //
@@ -60,9 +63,10 @@
 // first.  Measured on GB300 with the data in shared memory: the PRMT table
 // lookup + bf16x2 scale multiply of the grouped kernels ran near 4.7 TB/s of
 // weights at two CTAs per SM; the conversion instruction with f16 MMAs and
-// block-diagonal activations near 11 TB/s, and about 6.5 TB/s including the
-// bit-pair exchange the serving layout needs (four logic ops per word), which
-// is above what HBM delivers.
+// block-diagonal activations near 11 TB/s.  The prepared layout stores plain
+// E2M1 nibbles in the conversion's pairing, so the kernel converts code words
+// as loaded (a bit-pair exchange per word, which the table lookup needs
+// instead, cost this kernel 10-15 % of its time when it paid it).
 //
 // K order inside an MMA: thread t of a quad owns physical 16-element block t
 // of each 64-wide stage; its bytes pair elements (0,2), (1,3), (4,6), (5,7)
@@ -269,37 +273,45 @@ __device__ __forceinline__ bool convert_x_row(const DecodeParams& p, const DUnit
 }
 
 // Sums (ascending split order) of the split partials of four consecutive
-// elements at src (splits innermost, stride S; s1 <= S written), read again by
-// the whole warp while any written one still holds the not-written marker.
-// Lanes with valid == false take zeros.  False on timeout (abort raised).
-template <int S>
-__device__ __forceinline__ bool poll_sum4(float (&sum)[4], const float* src, bool valid, int s1, const Abort& ab) {
+// elements at each of N sources (splits innermost, stride S; s1 <= S
+// written), read again by the whole warp while any written one still holds the
+// not-written marker: the N sources share every round trip.  Sources with
+// valid[q] == false take zeros and are not read.  False on timeout (abort
+// raised).
+template <int S, int N>
+__device__ __forceinline__ bool poll_sum4(float (&sum)[N][4], const float* const (&src)[N], const bool (&valid)[N],
+                                          int s1, const Abort& ab) {
   const unsigned long long t0 = globaltimer();
   while (true) {
-    float v[4 * S];
+    float v[N][4 * S];
     bool ready = true;
-    if (valid) {
 #pragma unroll
-      for (int c = 0; c < 4 * S; c += 4) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(src + c));
-        v[c] = a.x, v[c + 1] = a.y, v[c + 2] = a.z, v[c + 3] = a.w;
+    for (int q = 0; q < N; ++q) {
+      if (valid[q]) {
+#pragma unroll
+        for (int c = 0; c < 4 * S; c += 4) {
+          const float4 a = __ldcg(reinterpret_cast<const float4*>(src[q] + c));
+          v[q][c] = a.x, v[q][c + 1] = a.y, v[q][c + 2] = a.z, v[q][c + 3] = a.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4 * S; ++c)
+          if (c % S < s1 && __float_as_uint(v[q][c]) == kNotWritten) ready = false;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4 * S; ++c) v[q][c] = 0.f;
       }
-#pragma unroll
-      for (int c = 0; c < 4 * S; ++c)
-        if (c % S < s1 && __float_as_uint(v[c]) == kNotWritten) ready = false;
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4 * S; ++c) v[c] = 0.f;
     }
     if (__all_sync(0xffffffffu, ready)) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float a = v[e * S];
+      for (int q = 0; q < N; ++q)
 #pragma unroll
-        for (int sp = 1; sp < S; ++sp)
-          if (sp < s1) a += v[e * S + sp];
-        sum[e] = a;
-      }
+        for (int e = 0; e < 4; ++e) {
+          float a = v[q][e * S];
+#pragma unroll
+          for (int sp = 1; sp < S; ++sp)
+            if (sp < s1) a += v[q][e * S + sp];
+          sum[q][e] = a;
+        }
       return true;
     }
     if (ab.raised() || globaltimer() - t0 > kWaitLimitNs) {
@@ -310,39 +322,61 @@ __device__ __forceinline__ bool poll_sum4(float (&sum)[4], const float* src, boo
   }
 }
 
-// FC2 activation row of one unit, built by the eight compute warps (warp w
-// takes slots w, w + 8, ...): h[i] = bf16(act(sum of the FC1 split partials,
-// ascending split order)), then the slot's power-of-two prescale and f16 as
-// in build_x_row.  Returns false on timeout (the abort flag is raised).
+// One 128-wide slot j of an FC2 activation row from this lane's four h values
+// (already act()-ed; lanes past the unit's K range pass valid == false):
+// rounded to bf16, then the slot's power-of-two prescale and f16 as in
+// convert_x_row.
+__device__ __forceinline__ void store_h_slot(uint8_t* row, int* exps, int j, int lane, bool valid, float (&h)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) h[c] = valid ? __bfloat162float(__float2bfloat16_rn(h[c])) : 0.f;
+  float a = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const int e = slot_prescale(a);
+  store_x4_f16(row + 256 * j + 8 * lane, h[0], h[1], h[2], h[3], e);
+  if (lane == 0) exps[j] = e;
+}
+
+// FC2 activation row of one unit, built by the eight compute warps: h[i] =
+// bf16(act(sum of the FC1 split partials, ascending split order)), then the
+// slot's power-of-two prescale and f16 as in convert_x_row.  Warp w takes
+// slots w, w + 8, ...; one poll reads a SwiGLU slot's gate and up partials,
+// or two ReLU^2 slots (w + 16 i and w + 16 i + 8).  Returns false on timeout
+// (the abort flag is raised).
 template <int S>
 __device__ __forceinline__ bool build_h_f16(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps, int cw,
                                             int lane, int wnat, const Abort& ab) {
   const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
   const float* gate = p.p + ((size_t)U.route * wnat + k0) * S;
-  const float* up = gate + (size_t)p.inter_pad * S;
-  const bool glu = p.act == 0;
-  for (int j = cw; 128 * j < nk; j += kDComputeWarps) {
-    const int i = 128 * j + 4 * lane;
-    const bool valid = i < nk;
-    float h[4];
-    if (!poll_sum4<S>(h, gate + (size_t)i * S, valid, p.s1, ab)) return false;
-    if (glu) {
-      float u[4];
-      if (!poll_sum4<S>(u, up + (size_t)i * S, valid, p.s1, ab)) return false;
+  if (p.act == 0) {
+    const float* up = gate + (size_t)p.inter_pad * S;
+    for (int j = cw; 128 * j < nk; j += kDComputeWarps) {
+      const int i = 128 * j + 4 * lane;
+      const bool valid = i < nk;
+      const float* const src[2] = {gate + (valid ? (size_t)i * S : 0), up + (valid ? (size_t)i * S : 0)};
+      const bool vv[2] = {valid, valid};
+      float gu[2][4];
+      if (!poll_sum4<S, 2>(gu, src, vv, p.s1, ab)) return false;
+      float h[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) h[c] = h[c] / (1.0f + __expf(-h[c])) * u[c];
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) h[c] = h[c] > 0.f ? h[c] * h[c] : 0.f;
+      for (int c = 0; c < 4; ++c) h[c] = gu[0][c] / (1.0f + __expf(-gu[0][c])) * gu[1][c];
+      store_h_slot(row, exps, j, lane, valid, h);
     }
+  } else {
+    for (int j = cw; 128 * j < nk; j += 2 * kDComputeWarps) {
+      const int j2 = j + kDComputeWarps;
+      const int i0 = 128 * j + 4 * lane, i1 = 128 * j2 + 4 * lane;
+      const bool vv[2] = {i0 < nk, i1 < nk};
+      const float* const src[2] = {gate + (vv[0] ? (size_t)i0 * S : 0), gate + (vv[1] ? (size_t)i1 * S : 0)};
+      float hh[2][4];
+      if (!poll_sum4<S, 2>(hh, src, vv, p.s1, ab)) return false;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) h[c] = valid ? __bfloat162float(__float2bfloat16_rn(h[c])) : 0.f;
-    float a = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-    for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const int e = slot_prescale(a);
-    store_x4_f16(row + 256 * j + 8 * lane, h[0], h[1], h[2], h[3], e);
-    if (lane == 0) exps[j] = e;
+        for (int c = 0; c < 4; ++c) hh[q][c] = hh[q][c] > 0.f ? hh[q][c] * hh[q][c] : 0.f;
+      store_h_slot(row, exps, j, lane, vv[0], hh[0]);
+      if (128 * j2 < nk) store_h_slot(row, exps, j2, lane, vv[1], hh[1]);
+    }
   }
   return true;
 }
@@ -431,15 +465,19 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
   if (threadIdx.x == 0) pdl_launch_dependents();  // the next kernel may launch and set up meanwhile
   __syncthreads();
   pdl_wait();  // launched with PDL: nothing of this call is read or written before the kernel before it is done
+  if (!cg::this_grid().is_valid()) {  // not a cooperative launch: there is no grid barrier to wait on
+    if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0u, 4u);  // B4_ERR_CUDA
+    return;
+  }
 
   // The producers resolve the CTA's first unit and start its weight stream
   // and (FC1) x slice before the grid barrier: neither touches the partial
   // buffers.
   DUnit U0;
   const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
+  const bool x_pre = u0_ok && !U0.fc2;  // warp 0 issues the first unit's x slice
   uint32_t pre_slots = 0;
-  bool pre_row = false;
-  if (warp == 0 && lane == 0 && u0_ok && !U0.fc2) issue_x_row(p, U0, s_rows, &xbar[0]);  // ahead of the weights
+  if (warp == 0 && lane == 0 && x_pre) issue_x_row(p, U0, s_rows, &xbar[0]);  // ahead of the weights
   if (warp == 0 && lane == 0 && u0_ok && !(U0.fc2 && p.linear)) {
     const size_t tile_id = (size_t)U0.expert * (U0.fc2 ? p.n_tiles2 : p.n_tiles1) + U0.tile;
     const int ks = U0.fc2 ? p.k_stages2 : p.k_stages1;
@@ -455,14 +493,16 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     }
     d_trace_cta(p, 14);
   }
-  if (warp == 1 && u0_ok && !U0.fc2) {
+  // Warp 1 publishes the first unit and converts its x slice before the
+  // CTA's grid-barrier arrival: the arriving atomic (a release at GPU scope)
+  // made while the first copies are in flight delays them.
+  if (warp == 1 && x_pre) {
     if (lane == 0) {
       s_desc[0].u = blockIdx.x;
       s_desc[0].expert = U0.expert;
       mbar_arrive(&desc_full[0]);
       s_desc[0].scale = p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f;
     }
-    pre_row = true;  // its x slice was issued by warp 0
     convert_x_row(p, U0, s_rows, s_xexp, &xbar[0], 0, lane, ab);
     __syncwarp();
     if (lane == 0) {
@@ -495,25 +535,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
       }
     }
   }
-  cg::grid_group grid = cg::this_grid();
-  if (!grid.is_valid()) {  // not a cooperative launch: there is no grid barrier to wait on
-    if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0u, 4u);  // B4_ERR_CUDA
-    return;
-  }
-  // Every thread's fill precedes the CTA's arrival (a release at GPU scope);
-  // warp 1 then waits for the other CTAs and completes grid_bar, which the
-  // first partial store or read of each warp waits on (acquire).
+  // Every thread's fill precedes the CTA's arrival (a release at GPU scope),
+  // which the output warp makes: the arriving atomic can hold its warp for
+  // microseconds, and that warp has nothing to do before the first partials
+  // exist, while warp 1 goes on to publish the CTA's second unit.  It then waits for the other CTAs and completes grid_bar, which the
+  // first partial store or read of each warp and the first claimed unit wait
+  // on (acquire).
   __syncthreads();
-  if (warp == 1) {
-    uint32_t* word = &cg::details::get_grid_workspace()->barrier;
-    uint32_t old = 0;
-    if (lane == 0) old = grid_arrive(word);
-    if (lane == 0 && grid_wait(word, old, ab)) {
-      mbar_arrive(grid_bar);
-      d_trace_cta(p, 13);
-    }
-    __syncwarp();
-  }
 
   if (warp == 0) {
     // ------------------------------------------------------ weight stream
@@ -560,29 +588,39 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
 
   if (warp == 1) {
     // ------------------------------------- unit schedule and activation rows
-    // The CTA's first unit is unit blockIdx.x; later ones are claimed from a
-    // counter in unit order (a CTA that runs faster takes more).  Each unit is
-    // resolved once and published with the FC1 x slice in one of two
-    // descriptor/row slots; a unit index of -1 ends the sequence.
-    uint32_t bs = 0;
-    uint32_t xuse0 = 0, xuse1 = 0;  // FC1 x copies per row buffer (phase of xbar)
-    DUnit U = U0;
-    int u = blockIdx.x;
-    bool have = u0_ok;
-    if (pre_row) {  // the first unit went out before the grid barrier
-      bs = 1;
-      xuse0 = 1;
-      have = false;
-    }
+    // The CTA's first two units are units blockIdx.x and blockIdx.x + G, so
+    // the second one's weights stream while the first computes, whatever the
+    // grid barrier is doing; later ones are claimed from a counter in unit
+    // order (a CTA that runs faster takes more), after the grid barrier (the
+    // counter is reset before it).  Each unit is resolved once and published
+    // with the FC1 x slice in one of two descriptor/row slots; a unit index
+    // of -1 ends the sequence.
+    uint32_t bs = x_pre ? 1 : 0;      // the first unit went out before the grid barrier
+    uint32_t xuse0 = x_pre ? 1 : 0, xuse1 = 0;  // FC1 x copies per row buffer (phase of xbar)
+    int taken = x_pre ? 1 : 0;        // static units taken
+    bool synced = false;            // grid_bar seen complete
+    DUnit U;
+    int u = 0;
     while (!ab.raised()) {
       // next valid unit: claims are issued one unit ahead of their use
+      bool have = false;
       while (!have) {
-        int t = 0;
-        if (lane == 0) t = atomicAdd(p.ticket, 1);
-        u = (int)gridDim.x + __shfl_sync(0xffffffffu, t, 0);
+        if (taken < 2) {
+          u = (int)blockIdx.x + taken * (int)gridDim.x;
+          ++taken;
+        } else {
+          if (!synced) {
+            if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 46))) break;
+            synced = true;
+          }
+          int t = 0;
+          if (lane == 0) t = atomicAdd(p.ticket, 1);
+          u = 2 * (int)gridDim.x + __shfl_sync(0xffffffffu, t, 0);
+        }
         if (u >= n_units) break;
         have = d_unit(p, u, U);
       }
+      if (ab.raised()) break;
       const uint32_t rb = bs & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&empty_b[rb], ((bs >> 1) & 1) ^ 1, ab, 33))) break;
       DDesc* dsc = s_desc + rb;
@@ -634,7 +672,6 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
         }
       }
       ++bs;
-      have = false;
     }
     if (ab.raised() && lane == 0) {  // let issued x copies land before the CTA exits
       for (int i = 0; i < 2; ++i) {
@@ -651,6 +688,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
 
   if (warp == 2 + kDComputeWarps) {
     // ------------------------------------------------------ output tiles
+    if (lane == 0) {
+      uint32_t* word = &cg::details::get_grid_workspace()->barrier;
+      if (grid_wait(word, grid_arrive(word), ab)) {
+        mbar_arrive(grid_bar);
+        d_trace_cta(p, 13);
+      }
+    }
     if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 42))) return;
     for (uint32_t es = 0;; ++es) {
       const uint32_t eb = es & 1;

@@ -1,8 +1,9 @@
-// The small-m kernels' per-thread stage arithmetic: 64 K elements of two
-// weight rows dequantised in registers and multiplied with the activation
-// slice on warp-level m16n8k16 MMAs.  Two forms: the register table lookup
-// with bf16 MMAs (the route-grouped kernel) and the hardware FP4 conversion
-// with f16 MMAs and block-diagonal activations (the per-route kernel).
+// The small-m kernels' per-thread stage arithmetic: weight rows dequantised in
+// registers and multiplied with the activation slice on warp-level m16n8k16
+// MMAs.  Here: the bf16 MMA and block-scale multiplier the route-grouped
+// kernel feeds from the register table lookup (dequant.cuh), and the
+// per-route kernel's stage: hardware FP4 conversion with f16 MMAs and
+// block-diagonal activations.
 #pragma once
 
 #include <cstdint>
@@ -32,47 +33,8 @@ __device__ __forceinline__ uint32_t d_scale(uint32_t b) {
   return FMT == 0 ? b * 0x00100010u + 0x58005800u : b * 0x00800080u + 0x1F801F80u;
 }
 
-// One thread's operands of one 64-wide stage: 8 code bytes (block t) of rows
-// r0 and r1, their two scale bytes, and the 16 activations of block t.
-struct StageIn {
-  uint2 c0, c1;
-  uint32_t b0, b1;
-  uint4 xa, xb;
-};
-
-template <int SB>
-__device__ __forceinline__ void load_stage(StageIn& in, const uint8_t* cs, const uint8_t* ss, const uint8_t* xr) {
-  in.c0 = *reinterpret_cast<const uint2*>(cs);
-  in.c1 = *reinterpret_cast<const uint2*>(cs + 8 * 16);
-  in.b0 = ss[0];
-  in.b1 = ss[8 * SB];
-  in.xa = *reinterpret_cast<const uint4*>(xr);
-  in.xb = *reinterpret_cast<const uint4*>(xr + 16);
-}
-
-// Dequantise the stage's 2 x 16 weights and run its four m16n8k16 MMAs
-// (pairs 2j, 2j+1 of block t feed MMA j) into two accumulators.
-template <int FMT>
-__device__ __forceinline__ void compute_stage(const StageIn& in, float (&d)[4], float (&e)[4]) {
-  const uint32_t sa = d_scale<FMT>(in.b0), sb = d_scale<FMT>(in.b1);
-  uint32_t a0[8], a1[8];
-  fp4x8_lookup(in.c0.x, a0[0], a0[1], a0[2], a0[3]);
-  fp4x8_lookup(in.c0.y, a0[4], a0[5], a0[6], a0[7]);
-  fp4x8_lookup(in.c1.x, a1[0], a1[1], a1[2], a1[3]);
-  fp4x8_lookup(in.c1.y, a1[4], a1[5], a1[6], a1[7]);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    a0[i] = bf16x2_mul(a0[i], sa);
-    a1[i] = bf16x2_mul(a1[i], sb);
-  }
-  mma_16816(d, a0[0], a1[0], a0[1], a1[1], in.xa.x, in.xa.y);
-  mma_16816(e, a0[2], a1[2], a0[3], a1[3], in.xa.z, in.xa.w);
-  mma_16816(d, a0[4], a1[4], a0[5], a1[5], in.xb.x, in.xb.y);
-  mma_16816(e, a0[6], a1[6], a0[7], a1[7], in.xb.z, in.xb.w);
-}
-
 // ------------------------------------------------------------------ f16 stage
-// The small-m kernels' dequantiser: E2M1 codes are converted by the hardware
+// The per-route small-m kernel's dequantiser: E2M1 codes are converted by the hardware
 // FP4 conversion (two codes of one byte -> one f16x2, exact), the weight
 // operand of f16 m16n8k16 MMAs.  The activation operand is block diagonal:
 // MMA column c is nonzero only for the K positions of block c, so after the
@@ -82,18 +44,10 @@ __device__ __forceinline__ void compute_stage(const StageIn& in, float (&d)[4], 
 // power of two per 128-wide slot, chosen so the slot's largest magnitude lands
 // in [2^14, 2^15): every bf16 value within 2^24 of it is exact in f16.
 
-// Serving-layout code word -> four bytes of two plain E2M1 nibbles each.  The
-// serving layout keeps (e0, m) of an element at bits [1:0] of its field and
-// (s, e1) at [5:4] (for the register table lookup of the grouped path), so in
-// every byte the bit pairs (2,3) and (4,5) are exchanged: byte 0 then holds
-// elements 0 (low nibble) and 2, byte 1 elements 1 and 3, byte 2 elements 4
-// and 6, byte 3 elements 5 and 7 of the word.
-__device__ __forceinline__ uint32_t serving_to_nibbles(uint32_t v) {
-  const uint32_t t = (v ^ (v >> 2)) & 0x0C0C0C0Cu;
-  return v ^ t ^ (t << 2);
-}
-
-// Four bytes of nibble pairs -> four f16x2 (low nibble -> low half).
+// A prepared code word (prepare.cu): four bytes of two plain E2M1 nibbles
+// each, byte 0 holding elements 0 (low nibble) and 2, byte 1 elements 1 and 3,
+// byte 2 elements 4 and 6, byte 3 elements 5 and 7 -> four f16x2 (low nibble
+// -> low half).
 __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t v, uint32_t& h0, uint32_t& h1, uint32_t& h2,
                                                 uint32_t& h3) {
   asm("{\n .reg .b8 c0, c1, c2, c3;\n mov.b32 {c0, c1, c2, c3}, %4;\n"
@@ -142,10 +96,10 @@ __device__ __forceinline__ void store_x4_f16(uint8_t* dst, float v0, float v1, f
 __device__ __forceinline__ void stage_mma_f16(const uint2& w0, const uint2& w1, const uint8_t* bp, float (&de)[4],
                                               float (&dq)[4]) {
   uint32_t a[4], b[4], c[4], d[4];
-  e2m1x8_to_f16x2(serving_to_nibbles(w0.x), a[0], a[1], a[2], a[3]);
-  e2m1x8_to_f16x2(serving_to_nibbles(w1.x), b[0], b[1], b[2], b[3]);
-  e2m1x8_to_f16x2(serving_to_nibbles(w0.y), c[0], c[1], c[2], c[3]);
-  e2m1x8_to_f16x2(serving_to_nibbles(w1.y), d[0], d[1], d[2], d[3]);
+  e2m1x8_to_f16x2(w0.x, a[0], a[1], a[2], a[3]);
+  e2m1x8_to_f16x2(w1.x, b[0], b[1], b[2], b[3]);
+  e2m1x8_to_f16x2(w0.y, c[0], c[1], c[2], c[3]);
+  e2m1x8_to_f16x2(w1.y, d[0], d[1], d[2], d[3]);
   const uint4 x01 = *reinterpret_cast<const uint4*>(bp);
   const uint4 x23 = *reinterpret_cast<const uint4*>(bp + 16);
   mma_16816_f16(de, a[0], b[0], a[1], b[1], x01.x, x01.y);

@@ -15,9 +15,12 @@
 //   or up row inter + t*64 + 16q + (l - 16) (l >= 16) -- gate and up rows of
 //   the same output column sit 16 lanes apart in one warp ("W13 rotation");
 // * rows and K are padded with zero codes and zero scales;
-// * every code word is re-encoded for the table-lookup dequantiser (see
-//   dequant_stage in moe_gemm.cu): pair j of a word (elements 2j, 2j+1) at
-//   shift {0, 2, 16, 18}[j], each element as (e0,m) and (s,e1) bit pairs;
+// * every 32-bit code word holds eight plain E2M1 nibbles (s, e1, e0, m) in
+//   the order the hardware FP4 conversion pairs them: byte 0 holds elements 0
+//   (low nibble) and 2, byte 1 elements 1 and 3, byte 2 elements 4 and 6,
+//   byte 3 elements 5 and 7 (element e sits in nibble e with bits 0 and 1
+//   swapped); the table-lookup dequantiser turns a word into its selectors
+//   with one bit-pair exchange (dequant.cuh);
 // * NVFP4 scales become b' with bf16 bits (b' << 4) + 0x5800 == scale * 2^63
 //   (b' = 0 for a zero scale); MXFP4 keeps e, decoded as (e + 63) << 7;
 // * a block with a zero scale stores zero codes; a negative E4M3 scale is
@@ -115,19 +118,14 @@ __global__ void prepare_kernel(const __grid_constant__ PrepareParams p) {
     uint8_t* dco = p.dst_codes + (((size_t)e * g.n_tiles + t) * g.k_stages + s) * kCodeBytesPerStage;
     for (int q = 0; q < 8; ++q) {
       uint32_t word = 0;
-      for (int j = 0; j < 4; ++j) {
-        const int sh = (j & 1) * 2 + (j >> 1) * 16;
-        for (int h = 0; h < 2; ++h) {
-          const int k = s * kBK + q * 8 + 2 * j + h;
-          const int b = (k - s * kBK) / group;
-          uint32_t c = crow ? src_code(crow, k, g.k_valid) : 0;
-          if (zero & (1u << b)) c = 0;
-          if (flip & (1u << b)) c ^= 8;
-          const uint32_t lo2 = c & 3;                            // (e0, m)
-          const uint32_t hi2 = ((c >> 3) << 1) | ((c >> 2) & 1);  // (s, e1)
-          word |= lo2 << (sh + 8 * h);
-          word |= hi2 << (sh + 8 * h + 4);
-        }
+      for (int el = 0; el < 8; ++el) {
+        const int k = s * kBK + q * 8 + el;
+        const int b = (k - s * kBK) / group;
+        uint32_t c = crow ? src_code(crow, k, g.k_valid) : 0;
+        if (zero & (1u << b)) c = 0;
+        if (flip & (1u << b)) c ^= 8;
+        const int nib = (el & 4) | ((el & 1) << 1) | ((el >> 1) & 1);  // bits 0 and 1 of el swapped
+        word |= c << (4 * nib);
       }
       const int chunk = q >> 2, w4 = q & 3;
       *reinterpret_cast<uint32_t*>(dco + chunk * 2048 + r * 16 + w4 * 4) = word;
