@@ -530,14 +530,17 @@ def kernel_source_hash(path):
 
 def kernel_family(b):
     """Which GEMM kernels serve the call: the per-route small-m kernel
-    (m <= 4, or m top_k <= E_local), the route-grouped small-m kernel, or the
+    (m <= 4, m top_k <= E_local, or up to 2 E_local and 256 routes), the
+    route-grouped small-m kernel, or the
     grouped weights-on-N / weights-on-M kernels (api.cu's dispatch rule)."""
     if b.decode:
         wl = b.wl
         if isinstance(b, LinearBench):
             per_route = b.m <= 2
         else:
-            per_route = b.m <= 4 or b.m * wl.top_k <= wl.num_local_experts
+            r = b.m * wl.top_k
+            e_l = wl.num_local_experts
+            per_route = b.m <= 4 or r <= e_l or (r <= 2 * e_l and r <= 256)
         return "decode" if per_route else "decode_grouped"
     wl = b.wl
     return "grouped_wn" if b.m * wl.top_k < 96 * wl.num_local_experts else "grouped"

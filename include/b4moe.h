@@ -68,9 +68,11 @@ typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activ
 
 /* Execution path of b4_fused_moe.  DECODE is the small-m path (accepted for
  * m <= B4_DECODE_MAX_M): one cooperative launch, a per-route kernel for
- * m <= 4 or m * top_k <= num_local_experts (few routes per expert), a
- * route-grouped kernel (an expert's weights streamed once per group of up to
- * 16 of its routes) otherwise.  GROUPED is the route-packed
+ * m <= 4 or m * top_k <= num_local_experts (few routes per expert; from m = 2
+ * with m * top_k >= num_local_experts its units take up to 4 routes of one
+ * expert), also up to m * top_k <= 2 * num_local_experts while that is at
+ * most 256 routes, and a route-grouped kernel (an expert's weights streamed
+ * once per group of up to 16 of its routes) otherwise.  GROUPED is the route-packed
  * tcgen05 path.  AUTO takes DECODE for m <= 16, and for m <= 64 while
  * m * top_k <= 2 * num_local_experts (at most two routes per expert on
  * average), GROUPED otherwise: the crossover flashinfer PR #4255 (Reviewer

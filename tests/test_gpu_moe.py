@@ -43,12 +43,15 @@ CASES = [
     ("small_s", "silu", 16), ("small_s", "silu", 64),
     ("prefill_s", "silu", 200), ("prefill_s", "relu2", 200), ("prefill_s", "silu", 37),
     ("mxfp4_s", "silu", 100), ("mxfp4_s", "relu2", 9),
+    # routes repeating experts on the per-route kernel: its grouped units (E8M0 scales)
+    ("mxfp4_s", "relu2", 4),
     # many routes per expert: the weights-on-M grouped kernel (m * top_k >= 96 * E_l)
     ("mxfp4_s", "silu", 300), ("tiny", "relu2", 512),
     ("decode_w", "relu2", 6), ("decode_w", "silu", 8), ("decode_w", "relu2", 9),
     # as many routes as local experts: the per-route kernel's boundary (m * top_k = E_l)
     ("decode_w", "relu2", 16),
-    # AUTO above m = 16 while an expert gets at most two routes: the small-m path
+    # AUTO above m = 16 while an expert gets at most two routes: the small-m
+    # path, on the per-route kernel's grouped units
     ("decode_w", "relu2", 24),
 ]
 

@@ -23,7 +23,7 @@ template <int MODE, int FMT>
 cudaError_t launch_gemm_wn(const GemmParams& p, int grid, bool pdl, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream);
-cudaError_t decode_occupancy(int fmt, int* blocks_per_sm);
+cudaError_t decode_occupancy(int fmt, bool grouped, int* blocks_per_sm);
 cudaError_t launch_decode_grouped(const SmallGroupParams& p, int fmt, int sets, int grid, cudaStream_t stream);
 cudaError_t decode_grouped_occupancy(int fmt, int sets, size_t smem, int* blocks_per_sm);
 size_t decode_grouped_smem(int fmt, int sets, int routes);
@@ -76,14 +76,18 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
 // calls, weights L2-cold): the small-m kernels beat the grouped GEMMs up to
 // m = 16 (decode E128 k8 m = 16: 195 vs 289 us; small-batch E64 k6 m = 16:
 // 91 vs 101 us), the grouped GEMMs win from m = 32 (small-batch m = 32).
-// Inside the small-m path the per-route kernel re-reads an expert's weights
-// for each route that selects it but streams about twice as fast (4.6 against
-// 2.1 TB/s): it wins while there are no more routes than local experts
-// (decode m = 16, 128 routes on 128 experts: 195 vs 271 us; small-batch m = 8,
-// 48 routes on 64 experts: 60 vs 66 us), the route-grouped kernel once experts
-// repeat (small-batch m = 16, 96 routes on 64 experts: 112 vs 91 us).
+// Inside the small-m path the per-route kernel streams about twice as fast as
+// the route-grouped one (4.6 against 2.1 TB/s); one route per unit it re-reads
+// an expert's weights for each route that selects it, which wins while there
+// are fewer routes than local experts (small-batch m = 8, 48 routes on 64
+// experts: 60 vs 66 us).  From m * top_k >= E_local its units take up to four
+// routes of one expert (decode m = 16, 128 routes on 128 experts: 163 us
+// grouped, 195 one route per unit, 271 route-grouped; m = 32, 256 routes: 266
+// against 373 route-grouped and 382 for the grouped GEMMs; small-batch m = 16,
+// 96 routes on 64 experts: 87 against 92 and 100).  At three routes per expert
+// the route-grouped kernel wins again (small-batch m = 32: 139 against 145).
 constexpr int kDecodeAutoMaxM = 16;  // AUTO takes a small-m kernel up to here
-constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while m top_k <= E_local
+constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while m top_k <= 2 E_local (grouped units)
 // b4_linear (N = K = 4096, back-to-back calls): the per-route kernel re-reads W
 // per token (m = 1 / 2 / 3 / 4: 9.8 / 13.2 / 16.3 / 18.8 us), the route-grouped
 // kernel reads it once per 8 tokens (14.4 - 14.7 us for m = 1..4, 15.6 at m = 8,
@@ -188,13 +192,13 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.dcnt = take(sizeof(int32_t) * (size_t)L.dec_rcap * nt1);
   const size_t small_end = off;
   // per-route decode path: K splits of about 256 units over the routes (a
-  // unit covers at most 128 K stages), FC1 partials with the splits
-  // innermost padded to a power of two, FC2 partials per split
+  // unit covers at most 128 K stages, a grouped unit 32), FC1 partials with
+  // the splits innermost padded to a power of two, FC2 partials per split
   off = region;
   int sp = 256 / L.dec_rcap;
   sp = sp < 1 ? 1 : (sp > kMaxSplits ? kMaxSplits : sp);
   const int kst = cdiv(cfg->hidden > L.inter_pad ? cfg->hidden : L.inter_pad, kBK);
-  const int need = (kst + 127) / 128;
+  const int need = (kst * kDecodeGroupMax + kDecodeMaxStages - 1) / kDecodeMaxStages;  // grouped units' length cap
   L.dec_splits = sp > need ? sp : need;
   int p_splits = 1;
   while (p_splits < L.dec_splits) p_splits <<= 1;
@@ -240,15 +244,17 @@ b4_status device_info(DevInfo& info) {
 // Decode schedule: K splits of FC1 and FC2 and the grid.  CTAs take their
 // first unit statically and claim the rest in unit order, so load balance is
 // dynamic; the splits aim at about two units per CTA of each GEMM with at
-// least 12 (or 20, below) K stages per unit (a unit holds at most 128; FC1
-// needs at most 4 splits below 512 K stages).  The FC1 partials
-// are stored with a power-of-two split stride of at most max_splits rounded
-// up.
+// least 12 (or 20, below) K stages per unit (a unit holds at most 128, a
+// grouped unit of up to group_max routes 128 / group_max; FC1 needs at most 4
+// splits below 512 K stages).  The planner counts routes, not groups: the
+// kernel has at most as many units.  The FC1 partials are stored with a
+// power-of-two split stride of at most max_splits rounded up.
 struct DecodePlan {
   int s1, s2, grid;
 };
 
-DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, int grid_cap, int max_splits) {
+DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, int grid_cap, int max_splits,
+                       int group_max) {
   int stride_cap = 1;
   while (stride_cap < max_splits) stride_cap <<= 1;
   // When FC1 has at most half as many (route, tile) pairs as CTAs (m = 1 on
@@ -261,7 +267,7 @@ DecodePlan plan_decode(int routes, const TensorGeom& g1, const TensorGeom& g2, i
     const int most = g.k_stages / min_stages > 1 ? g.k_stages / min_stages : 1;
     if (s > most) s = most;
     if (s > cap) s = cap;
-    const int least = (g.k_stages + 127) / 128;
+    const int least = (g.k_stages * group_max + kDecodeMaxStages - 1) / kDecodeMaxStages;  // unit length cap
     return s < least ? least : s;
   };
   DecodePlan plan;
@@ -491,15 +497,23 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   fp.out = out;
 
   cudaError_t e;
-  const bool per_route =
-      cfg->m <= kPerRouteMaxM || (long long)cfg->m * cfg->top_k <= (long long)cfg->num_local_experts;
+  const long long routes = (long long)cfg->m * cfg->top_k;
+  const bool per_route = cfg->m <= kPerRouteMaxM || routes <= cfg->num_local_experts ||
+                         (routes <= 2LL * cfg->num_local_experts && routes <= kDecodeGroupRoutes);
   if (decode && per_route) {
     // the per-route kernel: one unit per (route, tile, K split)
     const int R = cfg->m * cfg->top_k;
+    // grouped units once routes repeat experts (m * top_k >= E_local), while
+    // the group table fits and a grouped FC1 unit needs at most 4 K splits (an
+    // FC2 unit sums up to 4 per h element)
+    const int group_max = cfg->m >= 2 && R >= cfg->num_local_experts && R <= kDecodeGroupRoutes &&
+                                  g1.k_stages <= kDecodeMaxStages
+                              ? kDecodeGroupMax
+                              : 1;
     int occ = 0;
-    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if ((e = decode_occupancy(fmt, group_max > 1, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
     if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
-    const DecodePlan plan = plan_decode(R, g1, g2, occ * dev.sms, L.dec_splits);
+    const DecodePlan plan = plan_decode(R, g1, g2, occ * dev.sms, L.dec_splits, group_max);
     DecodeParams dp{};
     dp.w1_codes = w13;
     dp.w1_scales = s13;
@@ -529,6 +543,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     while (dp.s1_stride < plan.s1) dp.s1_stride <<= 1;
     dp.units1 = R * g1.n_tiles * plan.s1;
     dp.units2 = R * g2.n_tiles * plan.s2;
+    dp.group_max = group_max;
     dp.p = reinterpret_cast<float*>(ws + L.op);
     dp.q = reinterpret_cast<float*>(ws + L.oq);
     dp.p_floats = (size_t)R * fc1_natural_width(act, L.inter_pad) * dp.s1_stride;
@@ -706,7 +721,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
     // The fused small-m kernel: K-split GEMV units, then one output unit per
     // (token, 128 columns) that sums the split partials into out.
     int occ = 0;
-    if ((e = decode_occupancy(fmt, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if ((e = decode_occupancy(fmt, false, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
     if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
     // K splits: about two GEMV units per CTA, at least 8 stages each, at
     // most the partial buffer's split count (summing up to 8 partials per
@@ -721,6 +736,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
     if (s1 < least) s1 = least;
     const DecodePlan plan{s1, 1, 0};
     DecodeParams dp{};
+    dp.group_max = 1;
     dp.w1_codes = w;
     dp.w1_scales = sc;
     dp.gs1 = gs;

@@ -99,17 +99,44 @@ cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 
 namespace cg = cooperative_groups;
 
-constexpr int kDGroups = 1;           // K groups of 8 compute warps (128 weight rows each) per CTA
-constexpr int kDGroupWarps = 8;
-constexpr int kDComputeWarps = kDGroups * kDGroupWarps;
+constexpr int kDComputeWarps = 8;    // 16 weight rows each: a unit's 128-row tile
 constexpr int kDThreads = 32 * (3 + kDComputeWarps);  // weights, schedule, compute, output
-constexpr int kDMinBlocks = 2 / kDGroups;              // resident CTAs per SM
-constexpr int kDSlots = kDGroups == 1 ? 4 : 6;  // weight ring slots
-constexpr int kDSlotStages = 4;       // 64-wide K stages per slot (two copies of 16 KB + 2 KB: large copies stream faster)
-constexpr int kDMaxStages = 128;      // K stages of one unit (its activation row is in shared memory)
-constexpr int kDMaxSlots = kDMaxStages / 2;  // 128-wide slots of one unit's activation row
+constexpr int kDMinBlocks = 2;       // resident CTAs per SM
+constexpr int kDSlots = 4;           // weight ring slots
+constexpr int kDSlotStages = 4;      // 64-wide K stages per slot (two copies of 16 KB + 2 KB: large copies stream faster)
+constexpr int kDMaxStages = kDecodeMaxStages;  // K stages of one route's activation row (a row buffer)
+constexpr int kDMaxSlots = kDMaxStages / 2;  // 128-wide slots of one route's activation row
 constexpr int kDRowBytes = kDMaxStages * kBK * 2;
+// Grouped units: up to four routes of one local expert share a unit (and its
+// weight stream); each route's activation row takes a quarter of a row
+// buffer, so a grouped unit spans at most 32 K stages.
+constexpr int kDGroupMax = kDecodeGroupMax;
+constexpr int kDGroupRowBytes = kDRowBytes / kDGroupMax;
+constexpr int kDGroupSlots = kDMaxSlots / kDGroupMax;
+constexpr int kDGroupMaxRoutes = kDecodeGroupRoutes;  // grouping takes m * top_k <= this: its tables are in shared memory
 constexpr uint32_t kNotWritten = 0x7F800001u;  // signalling NaN: never an arithmetic result
+static_assert(kDGroupMaxRoutes <= kDThreads, "the group table is built with one thread per route");
+
+// A unit as passed between the warps of a CTA through shared memory.
+struct DDesc {
+  int u;          // unit index, or -1: no more units
+  int expert;     // local expert
+  float scale;    // FC1: gs; FC2 of a one-route unit: gs * router weight
+  uint32_t mask;  // FC2 of a one-route unit: the token's valid top-k slots
+  int nr;         // routes in the unit: 1, or 1 .. 4 for a grouped unit
+  uint32_t outs;  // grouped FC2 unit: bit i set when route i's token tile is summed after this unit
+  short route[kDGroupMax];  // grouped unit: its routes (-1 past nr)
+  float rw[kDGroupMax];     // grouped FC2 unit: gs * router weight of each route
+};
+static_assert(sizeof(DDesc) == 48, "unit descriptors are 48 bytes");
+
+// A token's 128-column output tile for the output warp.
+struct EDesc {
+  int tile, token;
+  uint32_t mask;  // the token's valid top-k slots
+  int end;        // nonzero: no more tiles
+};
+static_assert(sizeof(EDesc) == 16, "output descriptors are 16 bytes");
 
 template <int FMT>
 struct DSmem {
@@ -119,11 +146,16 @@ struct DSmem {
   static constexpr size_t rows = scales + (size_t)kDSlots * kDSlotStages * kScaleStage;
   static constexpr size_t bars = rows + 2 * (size_t)kDRowBytes;
   static constexpr size_t misc = bars + 8 * (2 * kDSlots + 14);  // 13 barriers besides the ring, one spare
-  static constexpr size_t desc = misc + 16;
-  static constexpr size_t xexp = desc + 4 * 16;            // four 16-byte unit descriptors
-  static constexpr size_t zero = xexp + 2 * kDMaxSlots * 4;  // per row buffer: prescale exponent of each slot
-  static constexpr size_t red = zero + 32;                   // 32 zero bytes: inactive activation columns
-  static constexpr size_t total = red + 2 * kTileRows * 4;   // per row buffer: the second K group's row sums
+  static constexpr size_t desc = misc + 16;                      // abort flag, group count
+  static constexpr size_t edesc = desc + 2 * sizeof(DDesc);      // two unit descriptors (with the rows)
+  static constexpr size_t xexp = edesc + 2 * sizeof(EDesc);      // two output descriptors
+  static constexpr size_t zero = xexp + 2 * kDMaxSlots * 4;      // per row buffer: prescale exponent of each slot
+  static constexpr size_t gexp = zero + 32;                      // 32 zero bytes: inactive activation columns
+  static constexpr size_t grp = gexp + 2 * kDGroupMaxRoutes;     // [R] local expert of each route (-1: none)
+  static constexpr size_t gtab = grp + 2 * kDGroupMaxRoutes;     // [R] group of each valid route
+  static constexpr size_t lastg = gtab + 8 * kDGroupMaxRoutes;   // [groups] the group's routes (-1 past its size)
+  static constexpr size_t tmask = lastg + 2 * kDGroupMaxRoutes;  // [m] last group (in unit order) of a token's routes
+  static constexpr size_t total = tmask + 4 * kDGroupMaxRoutes;  // [m] valid top-k slots of each token
 };
 
 __device__ __forceinline__ int d_local_expert(const DecodeParams& p, int route) {
@@ -135,25 +167,32 @@ __device__ __forceinline__ int d_local_expert(const DecodeParams& p, int route) 
 }
 
 struct DUnit {
-  int fc2, route, tile, split, kbeg, kend, expert;
+  int fc2;
+  int route;  // the route, or the group of a grouped unit
+  int tile, split, kbeg, kend, expert;
 };
 
-// A unit as passed between the warps of a CTA through shared memory.
-struct DDesc {
-  int u;          // unit index, or -1: no more units
-  int expert;     // local expert
-  float scale;    // gs * 2^63 (FC1) or gs * 2^63 * router weight (FC2)
-  uint32_t mask;  // FC2: the token's valid top-k slots
+// The routes of the call grouped by local expert (grouped units only): up to
+// four routes of one expert, in ascending route order, per group; groups in
+// the order of their first route.
+struct DGroups {
+  bool on;
+  int ng;              // groups
+  const short* gexp;   // [R] local expert of each route (-1: none)
+  const short* grp;    // [R] group of each valid route
+  const short* gtab;   // [ng][4] routes of each group (-1 past its size)
+  const short* lastg;  // [m] a token's last group
+  const uint32_t* tmask;  // [m] a token's valid top-k slots
 };
-static_assert(sizeof(DDesc) == 16, "unit descriptors are 16 bytes");
 
-// The arithmetic part of d_unit: route, tile, split and K range of unit u.
-__device__ __forceinline__ void d_unit_shape(const DecodeParams& p, int u, DUnit& U) {
+// The arithmetic part of d_unit: route (or group), tile, split and K range of
+// unit u; units [0, units1) are FC1 units.
+__device__ __forceinline__ void d_unit_shape(const DecodeParams& p, int units1, int u, DUnit& U) {
   int nt, ns, ks;
-  if (u < p.units1) {
+  if (u < units1) {
     U.fc2 = 0, nt = p.n_tiles1, ns = p.s1, ks = p.k_stages1;
   } else {
-    u -= p.units1;
+    u -= units1;
     U.fc2 = 1, nt = p.n_tiles2, ns = p.s2, ks = p.k_stages2;
   }
   const int per_route = nt * ns;
@@ -166,9 +205,9 @@ __device__ __forceinline__ void d_unit_shape(const DecodeParams& p, int u, DUnit
   U.expert = -1;
 }
 
-__device__ __forceinline__ bool d_unit(const DecodeParams& p, int u, DUnit& U) {
-  d_unit_shape(p, u, U);
-  U.expert = d_local_expert(p, U.route);
+__device__ __forceinline__ bool d_unit(const DecodeParams& p, const DGroups& G, int units1, int u, DUnit& U) {
+  d_unit_shape(p, units1, u, U);
+  U.expert = G.on ? G.gexp[G.gtab[4 * U.route]] : d_local_expert(p, U.route);
   return U.expert >= 0 && U.kend > U.kbeg;
 }
 
@@ -237,21 +276,97 @@ __device__ __forceinline__ float sum_splits(const float (&v)[S], int s1) {
   return a;
 }
 
-// FC1 activation row of one unit: lane 0 copies the token's bf16 x[k0 ..
-// k0 + kv) into the row buffer (one bulk copy, completing on xbar), positions
-// past the hidden size are zeroed; then the warp converts the row in place to
-// 128-wide f16 slots, each prescaled by a power of two (exps[j]).  Lane l
-// owns K positions 4l .. 4l+3 of a slot (block l / 4, quarter l % 4), whose
-// eight bytes are the same in the bf16 and the f16 row.
-__device__ __forceinline__ void issue_x_row(const DecodeParams& p, const DUnit& U, uint8_t* row, uint64_t* xbar) {
-  const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
-  const int kv = min(nk, p.hidden - k0);  // hidden is a multiple of 16: whole 32-byte pieces
-  mbar_arrive_expect_tx(xbar, (uint32_t)kv * 2);
-  bulk_g2s(row, p.x + (size_t)(U.route / p.top_k) * p.hidden + k0, (uint32_t)kv * 2, xbar);
+// Grouped units (m * top_k <= 256): every CTA builds the same group table,
+// one thread per route.  A valid route's rank is the number of earlier routes
+// of its local expert; ranks 0, 4, 8, ... open a group, which takes the next
+// three routes of that expert as well; a group's index is the number of groups
+// opened by earlier routes.  Then each token's last group (the largest index
+// among its valid routes) and its valid top-k slots.  Returns the number of
+// groups; scan[] takes one int per warp.
+__device__ int build_groups(const DecodeParams& p, int R, short* gexp, short* grp, short* gtab, short* lastg,
+                            uint32_t* tmask, int* scan) {
+  const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+  int e = -1;
+  if (i < R) {
+    e = d_local_expert(p, i);
+    gexp[i] = (short)e;
+  }
+  __syncthreads();
+  bool lead = false;
+  if (e >= 0) {
+    int rank = 0;
+    for (int j = 0; j < i; ++j) rank += gexp[j] == e;
+    lead = (rank & (kDGroupMax - 1)) == 0;
+  }
+  const uint32_t b = __ballot_sync(0xffffffffu, lead);
+  if (lane == 0) scan[warp] = __popc(b);
+  __syncthreads();
+  int before = 0, ng = 0;
+  for (int w = 0; w < kDThreads / 32; ++w) {
+    const int c = scan[w];
+    if (w < warp) before += c;
+    ng += c;
+  }
+  if (lead) {
+    const int g = before + __popc(b & ((1u << lane) - 1u));
+    short* mem = gtab + kDGroupMax * g;
+    mem[0] = (short)i;
+#pragma unroll
+    for (int k = 1; k < kDGroupMax; ++k) mem[k] = -1;
+    grp[i] = (short)g;
+    int c = 1;
+    for (int j = i + 1; j < R && c < kDGroupMax; ++j)
+      if (gexp[j] == e) {
+        mem[c++] = (short)j;
+        grp[j] = (short)g;
+      }
+  }
+  __syncthreads();
+  if (i < p.m) {
+    int lg = -1;
+    uint32_t mask = 0;
+    for (int k = 0; k < p.top_k; ++k) {
+      const int r = i * p.top_k + k;
+      if (gexp[r] >= 0) {
+        lg = max(lg, (int)grp[r]);
+        mask |= 1u << k;
+      }
+    }
+    lastg[i] = (short)lg;
+    tmask[i] = mask;
+  }
+  __syncthreads();
+  return ng;
 }
-__device__ __forceinline__ bool convert_x_row(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps,
-                                              uint64_t* xbar, uint32_t parity, int lane, const Abort& ab) {
-  if (!__all_sync(0xffffffffu, mbar_wait(xbar, parity, ab, 34))) return false;
+
+__device__ __forceinline__ int group_size(const DGroups& G, int g) {
+  int n = 1;
+  while (n < kDGroupMax && G.gtab[kDGroupMax * g + n] >= 0) ++n;
+  return n;
+}
+
+// FC1 activation rows of one unit: lane 0 copies each route's bf16 x[k0 ..
+// k0 + kv) (its token's row) into the row buffer, one bulk copy per route
+// completing on xbar (a grouped unit's route i at i * kDGroupRowBytes);
+// positions past the hidden size are zeroed by convert_x_rows.
+__device__ __forceinline__ void issue_x_rows(const DecodeParams& p, const DGroups& G, const DUnit& U, uint8_t* row,
+                                             uint64_t* xbar) {
+  const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
+  const uint32_t bytes = (uint32_t)min(nk, p.hidden - k0) * 2;  // hidden is a multiple of 16: whole 32-byte pieces
+  const int nr = G.on ? group_size(G, U.route) : 1;
+  mbar_arrive_expect_tx(xbar, bytes * nr);
+  for (int i = 0; i < nr; ++i) {
+    const int route = G.on ? G.gtab[kDGroupMax * U.route + i] : U.route;
+    bulk_g2s(row + i * kDGroupRowBytes, p.x + (size_t)(route / p.top_k) * p.hidden + k0, bytes, xbar);
+  }
+}
+
+// The warp converts an x row in place to 128-wide f16 slots, each prescaled
+// by a power of two (exps[j]).  Lane l owns K positions 4l .. 4l+3 of a slot
+// (block l / 4, quarter l % 4), whose eight bytes are the same in the bf16 and
+// the f16 row.
+__device__ __forceinline__ void convert_x_row(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps,
+                                              int lane) {
   const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
   for (int j = 0; 128 * j < nk; ++j) {
     const int i = 128 * j + 4 * lane;  // four positions: all below the hidden size or all past it
@@ -269,6 +384,15 @@ __device__ __forceinline__ bool convert_x_row(const DecodeParams& p, const DUnit
     store_x4_f16(dst, v[0], v[1], v[2], v[3], e);
     if (lane == 0) exps[j] = e;
   }
+}
+// Waits for a unit's x copies, then converts every route's row (a grouped
+// unit's route i: exps at i * kDGroupSlots).  False on timeout.
+__device__ __forceinline__ bool convert_x_rows(const DecodeParams& p, const DGroups& G, const DUnit& U, uint8_t* row,
+                                               int* exps, uint64_t* xbar, uint32_t parity, int lane,
+                                               const Abort& ab) {
+  if (!__all_sync(0xffffffffu, mbar_wait(xbar, parity, ab, 34))) return false;
+  const int nr = G.on ? group_size(G, U.route) : 1;
+  for (int i = 0; i < nr; ++i) convert_x_row(p, U, row + i * kDGroupRowBytes, exps + i * kDGroupSlots, lane);
   return true;
 }
 
@@ -337,48 +461,86 @@ __device__ __forceinline__ void store_h_slot(uint8_t* row, int* exps, int j, int
   if (lane == 0) exps[j] = e;
 }
 
-// FC2 activation row of one unit, built by the eight compute warps: h[i] =
-// bf16(act(sum of the FC1 split partials, ascending split order)), then the
-// slot's power-of-two prescale and f16 as in convert_x_row.  Warp w takes
-// slots w, w + 8, ...; one poll reads a SwiGLU slot's gate and up partials,
-// or two ReLU^2 slots (w + 16 i and w + 16 i + 8).  Returns false on timeout
-// (the abort flag is raised).
+// FC2 activation rows of one unit (one per route; a grouped unit's route i at
+// i * kDGroupRowBytes, exps at i * kDGroupSlots), built by the eight compute
+// warps: h[i] = bf16(act(sum of the FC1 split partials, ascending split
+// order)), then the slot's power-of-two prescale and f16 as in convert_x_row.
+// Warp w takes items w, w + 8, ... of the (route, 128-wide slot) list; one
+// poll reads a SwiGLU item's gate and up partials, or two ReLU^2 items (w +
+// 16 i and w + 16 i + 8).  Returns false on timeout (the abort flag is
+// raised).
 template <int S>
-__device__ __forceinline__ bool build_h_f16(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps, int cw,
-                                            int lane, int wnat, const Abort& ab) {
+__device__ __forceinline__ bool build_h_f16(const DecodeParams& p, const DGroups& G, const DUnit& U, uint8_t* row,
+                                            int* exps, int cw, int lane, int wnat, const Abort& ab) {
   const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
-  const float* gate = p.p + ((size_t)U.route * wnat + k0) * S;
+  const int ns = (nk + 127) / 128;  // activation slots per route
+  const int nr = G.on ? group_size(G, U.route) : 1;
+  const int items = nr * ns;
+  auto part = [&](int i) {  // route i's FC1 partials of this K range
+    const int route = G.on ? (int)G.gtab[kDGroupMax * U.route + i] : U.route;
+    return p.p + ((size_t)route * wnat + k0) * S;
+  };
   if (p.act == 0) {
-    const float* up = gate + (size_t)p.inter_pad * S;
-    for (int j = cw; 128 * j < nk; j += kDComputeWarps) {
-      const int i = 128 * j + 4 * lane;
-      const bool valid = i < nk;
-      const float* const src[2] = {gate + (valid ? (size_t)i * S : 0), up + (valid ? (size_t)i * S : 0)};
+    for (int f = cw; f < items; f += kDComputeWarps) {
+      const int i = f / ns, j = f - i * ns;
+      const int e = 128 * j + 4 * lane;
+      const bool valid = e < nk;
+      const float* gate = part(i) + (valid ? (size_t)e * S : 0);
+      const float* const src[2] = {gate, gate + (size_t)p.inter_pad * S};
       const bool vv[2] = {valid, valid};
       float gu[2][4];
       if (!poll_sum4<S, 2>(gu, src, vv, p.s1, ab)) return false;
       float h[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) h[c] = gu[0][c] / (1.0f + __expf(-gu[0][c])) * gu[1][c];
-      store_h_slot(row, exps, j, lane, valid, h);
+      store_h_slot(row + i * kDGroupRowBytes, exps + i * kDGroupSlots, j, lane, valid, h);
     }
   } else {
-    for (int j = cw; 128 * j < nk; j += 2 * kDComputeWarps) {
-      const int j2 = j + kDComputeWarps;
-      const int i0 = 128 * j + 4 * lane, i1 = 128 * j2 + 4 * lane;
-      const bool vv[2] = {i0 < nk, i1 < nk};
-      const float* const src[2] = {gate + (vv[0] ? (size_t)i0 * S : 0), gate + (vv[1] ? (size_t)i1 * S : 0)};
+    for (int f = cw; f < items; f += 2 * kDComputeWarps) {
+      const int f2 = f + kDComputeWarps;
+      const int i0 = f / ns, j0 = f - i0 * ns;
+      const int i1 = f2 / ns, j1 = f2 - i1 * ns;
+      const int e0 = 128 * j0 + 4 * lane, e1 = 128 * j1 + 4 * lane;
+      const bool vv[2] = {e0 < nk, f2 < items && e1 < nk};
+      const float* const src[2] = {part(i0) + (vv[0] ? (size_t)e0 * S : 0),
+                                   vv[1] ? part(i1) + (size_t)e1 * S : p.p};
       float hh[2][4];
       if (!poll_sum4<S, 2>(hh, src, vv, p.s1, ab)) return false;
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int c = 0; c < 4; ++c) hh[q][c] = hh[q][c] > 0.f ? hh[q][c] * hh[q][c] : 0.f;
-      store_h_slot(row, exps, j, lane, vv[0], hh[0]);
-      if (128 * j2 < nk) store_h_slot(row, exps, j2, lane, vv[1], hh[1]);
+      store_h_slot(row + i0 * kDGroupRowBytes, exps + i0 * kDGroupSlots, j0, lane, vv[0], hh[0]);
+      if (f2 < items) store_h_slot(row + i1 * kDGroupRowBytes, exps + i1 * kDGroupSlots, j1, lane, vv[1], hh[1]);
     }
   }
   return true;
+}
+
+// Lane 0 of warp 1: a unit's routes into its descriptor (one, or a group's
+// up to four), and for a grouped FC2 unit each route's output weight (gs *
+// router weight) and whether it triggers its token's output tile: the route
+// is its token's first in the token's last group.
+__device__ __forceinline__ void fill_routes(const DecodeParams& p, const DGroups& G, const DUnit& U, DDesc* d) {
+  int nr = 0;
+  uint32_t outs = 0;
+  const float gs = U.fc2 && G.on && p.gs2 ? __ldg(p.gs2 + U.expert) : 1.0f;
+  for (int i = 0; i < kDGroupMax; ++i) {
+    const int r = G.on ? (int)G.gtab[kDGroupMax * U.route + i] : (i == 0 ? U.route : -1);
+    d->route[i] = (short)r;
+    if (r < 0) continue;
+    nr = i + 1;
+    if (U.fc2 && G.on) {
+      d->rw[i] = gs * __ldg(p.topk_weights + r);
+      const int tk = r / p.top_k;
+      bool first = G.lastg[tk] == U.route;
+      for (int j = 0; j < i; ++j)
+        if (d->route[j] / p.top_k == tk) first = false;
+      if (first) outs |= 1u << i;
+    }
+  }
+  d->nr = nr;
+  d->outs = outs;
 }
 
 // Dense linear layer: out[token][n] = bf16(sum of the FC1 split partials of
@@ -410,7 +572,9 @@ __device__ __forceinline__ bool linear_out(const DecodeParams& p, const DUnit& U
 }
 
 // ------------------------------------------------------------------ fused
-template <int FMT>
+// GRP: grouped units (p.group_max > 1); the one-route kernel carries none of
+// their code.
+template <int FMT, bool GRP>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(const __grid_constant__ DecodeParams p) {
   using L = DSmem<FMT>;
   constexpr int SB = scale_bytes_per_row(FMT);
@@ -428,17 +592,20 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
   uint64_t* epi_empty = epi_full + 2;
   uint64_t* desc_full = epi_empty + 2;  // a unit descriptor is ready (for the weight stream)
   uint64_t* grid_bar = desc_full + 2;   // completes once every CTA has arrived at the grid barrier
-  uint64_t* xbar = grid_bar + 1;        // [2] the bf16 x slice of an FC1 unit has landed
+  uint64_t* xbar = grid_bar + 1;        // [2] the bf16 x slices of an FC1 unit have landed
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::misc);
-  DDesc* s_desc = reinterpret_cast<DDesc*>(smem + L::desc);  // [2] with the rows
-  DDesc* s_edesc = s_desc + 2;                                  // [2] for the output warp
+  DDesc* s_desc = reinterpret_cast<DDesc*>(smem + L::desc);    // [2] with the rows
+  EDesc* s_edesc = reinterpret_cast<EDesc*>(smem + L::edesc);  // [2] for the output warp
   int* s_xexp = reinterpret_cast<int*>(smem + L::xexp);        // [2][kDMaxSlots]
-  float* s_red = reinterpret_cast<float*>(smem + L::red);       // [2][128]
   uint8_t* s_zero = smem + L::zero;
+  short* s_gexp = reinterpret_cast<short*>(smem + L::gexp);
+  short* s_grp = reinterpret_cast<short*>(smem + L::grp);
+  short* s_gtab = reinterpret_cast<short*>(smem + L::gtab);
+  short* s_lastg = reinterpret_cast<short*>(smem + L::lastg);
+  uint32_t* s_tmask = reinterpret_cast<uint32_t*>(smem + L::tmask);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Abort ab{p.status, s_abort};
-  const int n_units = p.units1 + p.units2;
   const int R = p.m * p.top_k;
   if (threadIdx.x == 0) {
     d_trace(p, 2, 0);
@@ -470,14 +637,23 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     return;
   }
 
+  // Units are per route, or per group of up to four routes of one expert
+  // (the group table is built here, by every CTA alike; the exponent area is
+  // free scratch until the first x row is converted).
+  DGroups G{GRP, 0, s_gexp, s_grp, s_gtab, s_lastg, s_tmask};
+  if (G.on) G.ng = build_groups(p, R, s_gexp, s_grp, s_gtab, s_lastg, s_tmask, s_xexp);
+  const int base = G.on ? G.ng : R;
+  const int units1 = G.on ? base * p.n_tiles1 * p.s1 : p.units1;
+  const int n_units = units1 + (G.on ? base * p.n_tiles2 * p.s2 : p.units2);
+
   // The producers resolve the CTA's first unit and start its weight stream
-  // and (FC1) x slice before the grid barrier: neither touches the partial
+  // and (FC1) x slices before the grid barrier: neither touches the partial
   // buffers.
   DUnit U0;
-  const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, blockIdx.x, U0);
-  const bool x_pre = u0_ok && !U0.fc2;  // warp 0 issues the first unit's x slice
+  const bool u0_ok = warp < 2 && (int)blockIdx.x < n_units && d_unit(p, G, units1, blockIdx.x, U0);
+  const bool x_pre = u0_ok && !U0.fc2;  // warp 0 issues the first unit's x slices
   uint32_t pre_slots = 0;
-  if (warp == 0 && lane == 0 && x_pre) issue_x_row(p, U0, s_rows, &xbar[0]);  // ahead of the weights
+  if (warp == 0 && lane == 0 && x_pre) issue_x_rows(p, G, U0, s_rows, &xbar[0]);  // ahead of the weights
   if (warp == 0 && lane == 0 && u0_ok && !(U0.fc2 && p.linear)) {
     const size_t tile_id = (size_t)U0.expert * (U0.fc2 ? p.n_tiles2 : p.n_tiles1) + U0.tile;
     const int ks = U0.fc2 ? p.k_stages2 : p.k_stages1;
@@ -493,7 +669,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     }
     d_trace_cta(p, 14);
   }
-  // Warp 1 publishes the first unit and converts its x slice before the
+  // Warp 1 publishes the first unit and converts its x slices before the
   // CTA's grid-barrier arrival: the arriving atomic (a release at GPU scope)
   // made while the first copies are in flight delays them.
   if (warp == 1 && x_pre) {
@@ -502,8 +678,9 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
       s_desc[0].expert = U0.expert;
       mbar_arrive(&desc_full[0]);
       s_desc[0].scale = p.gs1 ? __ldg(p.gs1 + U0.expert) : 1.0f;
+      fill_routes(p, G, U0, &s_desc[0]);
     }
-    convert_x_row(p, U0, s_rows, s_xexp, &xbar[0], 0, lane, ab);
+    convert_x_rows(p, G, U0, s_rows, s_xexp, &xbar[0], 0, lane, ab);
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&full_b[0]);
@@ -538,9 +715,9 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
   // Every thread's fill precedes the CTA's arrival (a release at GPU scope),
   // which the output warp makes: the arriving atomic can hold its warp for
   // microseconds, and that warp has nothing to do before the first partials
-  // exist, while warp 1 goes on to publish the CTA's second unit.  It then waits for the other CTAs and completes grid_bar, which the
-  // first partial store or read of each warp and the first claimed unit wait
-  // on (acquire).
+  // exist, while warp 1 goes on to publish the CTA's second unit.  It then
+  // waits for the other CTAs and completes grid_bar, which the first partial
+  // store or read of each warp and the first claimed unit wait on (acquire).
   __syncthreads();
 
   if (warp == 0) {
@@ -554,7 +731,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
         const int u = s_desc[rb].u;
         if (u < 0) break;
         DUnit U;
-        d_unit_shape(p, u, U);
+        d_unit_shape(p, units1, u, U);
         if (U.fc2 && p.linear) continue;  // an output unit of the dense linear layer streams no weights
         U.expert = s_desc[rb].expert;
         const size_t tile_id = (size_t)U.expert * (U.fc2 ? p.n_tiles2 : p.n_tiles1) + U.tile;
@@ -593,12 +770,12 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     // grid barrier is doing; later ones are claimed from a counter in unit
     // order (a CTA that runs faster takes more), after the grid barrier (the
     // counter is reset before it).  Each unit is resolved once and published
-    // with the FC1 x slice in one of two descriptor/row slots; a unit index
+    // with the FC1 x slices in one of two descriptor/row slots; a unit index
     // of -1 ends the sequence.
-    uint32_t bs = x_pre ? 1 : 0;      // the first unit went out before the grid barrier
+    uint32_t bs = x_pre ? 1 : 0;                // the first unit went out before the grid barrier
     uint32_t xuse0 = x_pre ? 1 : 0, xuse1 = 0;  // FC1 x copies per row buffer (phase of xbar)
-    int taken = x_pre ? 1 : 0;        // static units taken
-    bool synced = false;            // grid_bar seen complete
+    int taken = x_pre ? 1 : 0;                  // static units taken
+    bool synced = false;                        // grid_bar seen complete
     DUnit U;
     int u = 0;
     while (!ab.raised()) {
@@ -618,7 +795,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
           u = 2 * (int)gridDim.x + __shfl_sync(0xffffffffu, t, 0);
         }
         if (u >= n_units) break;
-        have = d_unit(p, u, U);
+        have = d_unit(p, G, units1, u, U);
       }
       if (ab.raised()) break;
       const uint32_t rb = bs & 1;
@@ -638,22 +815,25 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
           dsc->u = u;
           dsc->expert = U.expert;
           mbar_arrive(&desc_full[rb]);  // the weight stream needs only the unit
-          issue_x_row(p, U, row, &xbar[rb]);
+          issue_x_rows(p, G, U, row, &xbar[rb]);
           dsc->scale = p.gs1 ? __ldg(p.gs1 + U.expert) : 1.0f;
+          fill_routes(p, G, U, dsc);
         }
         const uint32_t xu = rb ? xuse1 : xuse0;
-        convert_x_row(p, U, row, s_xexp + rb * kDMaxSlots, &xbar[rb], xu & 1, lane, ab);
+        convert_x_rows(p, G, U, row, s_xexp + rb * kDMaxSlots, &xbar[rb], xu & 1, lane, ab);
         if (rb) ++xuse1;
         else ++xuse0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_b[rb]);
-      } else if (p.linear) {
+      } else if (p.linear || G.on) {
+        // an output unit of the dense linear layer, or a grouped FC2 unit
         if (lane == 0) {
           dsc->u = u;
           dsc->expert = U.expert;
           mbar_arrive(&desc_full[rb]);
           dsc->scale = 1.0f;
           dsc->mask = 1u;
+          fill_routes(p, G, U, dsc);
           mbar_arrive(&full_b[rb]);
         }
       } else {
@@ -668,6 +848,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
         if (lane == 0) {
           dsc->scale = (p.gs2 ? __ldg(p.gs2 + U.expert) : 1.0f) * __ldg(p.topk_weights + U.route);
           dsc->mask = mask;
+          fill_routes(p, G, U, dsc);
           mbar_arrive(&full_b[rb]);
         }
       }
@@ -699,17 +880,15 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     for (uint32_t es = 0;; ++es) {
       const uint32_t eb = es & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&epi_full[eb], (es >> 1) & 1, ab, 37))) break;
-      const DDesc dsc = *(s_edesc + eb);
-      if (dsc.u < 0) break;
-      DUnit U;
-      d_unit_shape(p, dsc.u, U);
-      const int token = U.route / p.top_k;
-      const uint32_t mask = dsc.mask;
+      const EDesc ed = s_edesc[eb];
+      if (ed.end) break;
+      const int token = ed.token;
+      const uint32_t mask = ed.mask;
       // out = bf16(sum over valid routes and splits); each lane has 4 outputs
       // and 8 routes' partial loads are in flight at once.  Order: ascending
       // top-k slot within groups of 8, splits outer within a group.
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int nb = U.tile * kTileRows + lane;
+      const int nb = ed.tile * kTileRows + lane;
       for (int jb = 0; jb < p.top_k; jb += 8) {
         for (int sp = 0; sp < p.s2; ++sp) {
           float v[8][4];
@@ -752,23 +931,28 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
   }
 
   // --------------------------------------------------------- compute warps
-  // The sixteen compute warps share named barriers, so none of them leaves the
+  // The eight compute warps share named barriers, so none of them leaves the
   // unit loop alone: a failed (bounded) wait sets `bad`, the warp skips the
   // work but still passes every barrier, and the loop ends only by an OR
   // taken over all of them.
   const int cw = warp - 2;
-  const int grp = cw / kDGroupWarps;  // K group: the first or the second 128-wide half of every slot
   const int g = lane >> 2, t = lane & 3;
-  const int r0 = 16 * (cw % kDGroupWarps) + g, r1 = r0 + 8;
+  const int r0 = 16 * cw + g, r1 = r0 + 8;
   const int tid = threadIdx.x - 64;
   constexpr uint32_t kNC = 32 * kDComputeWarps;
   // this thread's 8 code bytes of row r0 (block t of the stage) and of row r1
   const uint32_t code_off = (t >> 1) * (kCodeBytesPerStage / 2) + r0 * 16 + (t & 1) * 8;
-  // accumulator columns 2t, 2t+1 hold the sums of blocks 2t, 2t+1 of a chunk
-  // (stage t >> 1 of it): their scale bytes
-  const uint32_t sc_off = (t >> 1) * kSS + (FMT == 0 ? r0 * SB + 2 * (t & 1) : r0 * SB + (t & 1));
-  // MMA column g is block g of a chunk: this thread's activation operand is
-  // nonzero in the chunk's first stage when g == t and in its second when g == t + 4
+  // Accumulator columns 2t, 2t+1 hold, in a one-route unit, the sums of blocks
+  // 2t, 2t+1 of a 128-wide chunk (stage t >> 1 of it); in a grouped unit, the
+  // sums of blocks 2(t&1), 2(t&1)+1 of every stage for route t >> 1 of the MMA
+  // half.  Their scale bytes:
+  const uint32_t scg_off = FMT == 0 ? r0 * SB + 2 * (t & 1) : r0 * SB + (t & 1);
+  const uint32_t sc_off = (t >> 1) * kSS + scg_off;
+  // One-route unit: MMA column g is block g of a chunk, so this thread's
+  // activation operand is nonzero in the chunk's first stage when g == t and
+  // in its second when g == t + 4.  Grouped unit: in every stage, columns 0-3
+  // of MMA half h are route 2h (this thread supplies it when g == t) and
+  // columns 4-7 route 2h + 1 (when g == t + 4).
   const bool col0 = g == t, col1 = g == t + 4;
   const int wnat = fc1_natural_width(p.act, p.inter_pad);
   uint32_t ws = 0, bs = 0, es = 0;
@@ -778,10 +962,11 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     const uint32_t rb = bs & 1;
     if (!bad && !__all_sync(0xffffffffu, mbar_wait(&full_b[rb], (bs >> 1) & 1, ab, 35))) bad = true;
     if (named_bar_or(3, kNC, bad || ab.raised())) break;
-    const DDesc dsc = *(s_desc + rb);
-    if (dsc.u < 0) break;
+    const DDesc* dp = s_desc + rb;
+    const int du = dp->u;
+    if (du < 0) break;
     DUnit U;
-    d_unit_shape(p, dsc.u, U);
+    d_unit_shape(p, units1, du, U);
     if (U.fc2 && !synced) {  // an FC2 or output unit reads other CTAs' partials
       if (!__all_sync(0xffffffffu, mbar_wait(grid_bar, 0, ab, 43))) bad = true;
       synced = true;
@@ -803,88 +988,155 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
     }
     uint8_t* row = s_rows + rb * kDRowBytes;
     int* xexp = s_xexp + rb * kDMaxSlots;
+    const int nr = dp->nr;
     if (U.fc2) {
       // h = act(sum over FC1 splits) for this unit's K range, as f16 slots
       if (!bad) {
         bool built;
         switch (p.s1_stride) {
-          case 1: built = build_h_f16<1>(p, U, row, xexp, cw, lane, wnat, ab); break;
-          case 2: built = build_h_f16<2>(p, U, row, xexp, cw, lane, wnat, ab); break;
-          default: built = build_h_f16<4>(p, U, row, xexp, cw, lane, wnat, ab); break;
+          case 1: built = build_h_f16<1>(p, G, U, row, xexp, cw, lane, wnat, ab); break;
+          case 2: built = build_h_f16<2>(p, G, U, row, xexp, cw, lane, wnat, ab); break;
+          default: built = build_h_f16<4>(p, G, U, row, xexp, cw, lane, wnat, ab); break;
         }
         bad = !built;
       }
       bad = named_bar_or(1, kNC, bad);
     }
     if (tid == 0) d_trace(p, 3, bs);
-    const uint8_t* xb0 = col0 ? row + g * 32 : s_zero;
-    const uint8_t* xb1 = col1 ? row + g * 32 : s_zero;
-    const int xstep0 = col0 ? 256 : 0, xstep1 = col1 ? 256 : 0;
-    float acc0 = 0.f, acc1 = 0.f;
-    for (int s = U.kbeg, k = 0; !bad && s < U.kend; s += kDSlotStages, ++ws, ++k) {
-      const uint32_t slot = ws % kDSlots;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (ws / kDSlots) & 1, ab, 36))) {
-        bad = true;
-        break;
-      }
-      if (tid == 0 && ws == 0) d_trace_cta(p, 15);
-      const int ns = min(kDSlotStages, U.kend - s);
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [MMA half][row r0, r1]
+    if (!GRP || nr == 1) {
+      const uint8_t* xb0 = col0 ? row + g * 32 : s_zero;
+      const uint8_t* xb1 = col1 ? row + g * 32 : s_zero;
+      const int xstep0 = col0 ? 256 : 0, xstep1 = col1 ? 256 : 0;
+      for (int s = U.kbeg, k = 0; !bad && s < U.kend; s += kDSlotStages, ++ws, ++k) {
+        const uint32_t slot = ws % kDSlots;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (ws / kDSlots) & 1, ab, 36))) {
+          bad = true;
+          break;
+        }
+        if (tid == 0 && ws == 0) d_trace_cta(p, 15);
+        const int ns = min(kDSlotStages, U.kend - s);
 #pragma unroll
-      for (int c = 2 * grp; c < kDSlotStages; c += 2 * kDGroups) {  // this group's 128-wide chunks of the slot
-        if (c >= ns) break;
-        const int j = 2 * k + c / 2;  // its activation slot
-        const bool two = ns - c >= 2;
-        const uint8_t* cs = s_codes + (slot * kDSlotStages + c) * kCodeBytesPerStage + code_off;
-        const uint8_t* ss = s_scales + (slot * kDSlotStages + c) * kSS + sc_off;
-        const int xe = xexp[j];
-        float de[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const uint2 w0 = *reinterpret_cast<const uint2*>(cs);
-          const uint2 w1 = *reinterpret_cast<const uint2*>(cs + 8 * 16);
-          stage_mma_f16(w0, w1, xb0 + j * xstep0, de, dq);
-        }
-        if (two) {
-          const uint2 w0 = *reinterpret_cast<const uint2*>(cs + kCodeBytesPerStage);
-          const uint2 w1 = *reinterpret_cast<const uint2*>(cs + kCodeBytesPerStage + 8 * 16);
-          stage_mma_f16(w0, w1, xb1 + j * xstep1, de, dq);
-        }
-        // columns of a missing second stage are zero and their scale bytes were not loaded
-        if (two || t < 2) {
-          if constexpr (FMT == 0) {
-            const uint32_t u0 = *reinterpret_cast<const uint16_t*>(ss);
-            const uint32_t u1 = *reinterpret_cast<const uint16_t*>(ss + 8 * SB);
-            acc0 = fmaf(de[0] + dq[0], f32_scale<0>(u0 & 0xFFu, xe), acc0);
-            acc0 = fmaf(de[1] + dq[1], f32_scale<0>(u0 >> 8, xe), acc0);
-            acc1 = fmaf(de[2] + dq[2], f32_scale<0>(u1 & 0xFFu, xe), acc1);
-            acc1 = fmaf(de[3] + dq[3], f32_scale<0>(u1 >> 8, xe), acc1);
-          } else {
-            acc0 = fmaf((de[0] + dq[0]) + (de[1] + dq[1]), f32_scale<1>(ss[0], xe), acc0);
-            acc1 = fmaf((de[2] + dq[2]) + (de[3] + dq[3]), f32_scale<1>(ss[8 * SB], xe), acc1);
+        for (int c = 0; c < kDSlotStages; c += 2) {  // the slot's 128-wide chunks
+          if (c >= ns) break;
+          const int j = 2 * k + c / 2;  // its activation slot
+          const bool two = ns - c >= 2;
+          const uint8_t* cs = s_codes + (slot * kDSlotStages + c) * kCodeBytesPerStage + code_off;
+          const uint8_t* ss = s_scales + (slot * kDSlotStages + c) * kSS + sc_off;
+          const int xe = xexp[j];
+          float de[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(cs);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(cs + 8 * 16);
+            stage_mma_f16(w0, w1, xb0 + j * xstep0, de, dq);
+          }
+          if (two) {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(cs + kCodeBytesPerStage);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(cs + kCodeBytesPerStage + 8 * 16);
+            stage_mma_f16(w0, w1, xb1 + j * xstep1, de, dq);
+          }
+          // columns of a missing second stage are zero and their scale bytes were not loaded
+          if (two || t < 2) {
+            if constexpr (FMT == 0) {
+              const uint32_t u0 = *reinterpret_cast<const uint16_t*>(ss);
+              const uint32_t u1 = *reinterpret_cast<const uint16_t*>(ss + 8 * SB);
+              acc[0][0] = fmaf(de[0] + dq[0], f32_scale<0>(u0 & 0xFFu, xe), acc[0][0]);
+              acc[0][0] = fmaf(de[1] + dq[1], f32_scale<0>(u0 >> 8, xe), acc[0][0]);
+              acc[0][1] = fmaf(de[2] + dq[2], f32_scale<0>(u1 & 0xFFu, xe), acc[0][1]);
+              acc[0][1] = fmaf(de[3] + dq[3], f32_scale<0>(u1 >> 8, xe), acc[0][1]);
+            } else {
+              acc[0][0] = fmaf((de[0] + dq[0]) + (de[1] + dq[1]), f32_scale<1>(ss[0], xe), acc[0][0]);
+              acc[0][1] = fmaf((de[2] + dq[2]) + (de[3] + dq[3]), f32_scale<1>(ss[8 * SB], xe), acc[0][1]);
+            }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_w[slot]);
+        if (tid == 0) {
+          d_trace(p, 1, ws);
+          if (ws == 0) d_trace_cta(p, 11);
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_w[slot]);
-      if (tid == 0) {
-        d_trace(p, 1, ws);
-        if (ws == 0) d_trace_cta(p, 11);
+      // row totals: the quad's four threads hold two blocks of each chunk each
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        acc[0][0] += __shfl_xor_sync(0xffffffffu, acc[0][0], o);
+        acc[0][1] += __shfl_xor_sync(0xffffffffu, acc[0][1], o);
       }
-    }
-    // row totals: the quad's four threads hold two blocks of each chunk each;
-    // the second K group hands its rows to the first (fixed order)
-    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
-    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
-    if constexpr (kDGroups == 2) {
-      float* red = s_red + rb * kTileRows;
-      if (grp == 1 && t < 2) red[t ? r1 : r0] = t ? acc1 : acc0;
-      bad = named_bar_or(2, kNC, bad);
-      if (t == 0) acc0 += red[r0];
-      if (t == 1) acc1 += red[r1];
     } else {
-      bad = named_bar_or(2, kNC, bad);
+      // grouped unit: the stage's codes are converted once and feed one MMA
+      // half (routes 0, 1) or two (routes 2, 3 as well); block scales and
+      // each route's activation prescale apply to every stage's sums
+      const int nh = nr > 2 ? 2 : 1;
+      const uint8_t* xh[2];
+      int xo_on[2], xeb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ri = 2 * h + (col0 ? 0 : 1);  // the route this thread supplies activations of
+        const bool live = (col0 || col1) && ri < nr;
+        xh[h] = live ? row + ri * kDGroupRowBytes + t * 32 : s_zero;
+        xo_on[h] = live ? 1 : 0;
+        const int ra = 2 * h + (t >> 1);  // the route of this thread's accumulator columns
+        xeb[h] = ra < nr ? ra * kDGroupSlots : -1;
+      }
+      for (int s = U.kbeg, k = 0; !bad && s < U.kend; s += kDSlotStages, ++ws, ++k) {
+        const uint32_t slot = ws % kDSlots;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (ws / kDSlots) & 1, ab, 36))) {
+          bad = true;
+          break;
+        }
+        if (tid == 0 && ws == 0) d_trace_cta(p, 15);
+        const int ns = min(kDSlotStages, U.kend - s);
+#pragma unroll
+        for (int c = 0; c < kDSlotStages; ++c) {  // the slot's stages
+          if (c >= ns) break;
+          const int j = 2 * k + (c >> 1);          // activation slot
+          const int xo = j * 256 + (c & 1) * 128;  // this stage's half of it
+          const uint8_t* cs = s_codes + (slot * kDSlotStages + c) * kCodeBytesPerStage + code_off;
+          const uint8_t* ss = s_scales + (slot * kDSlotStages + c) * kSS + scg_off;
+          F16Stage f;
+          dequant_stage_f16(*reinterpret_cast<const uint2*>(cs), *reinterpret_cast<const uint2*>(cs + 8 * 16), f);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h >= nh) break;
+            float de[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_stage_f16(f, xh[h] + (xo_on[h] ? xo : 0), de, dq);
+            const int xe = xeb[h] >= 0 ? xexp[xeb[h] + j] : 0;  // columns of a missing route are zero
+            if constexpr (FMT == 0) {
+              const uint32_t u0 = *reinterpret_cast<const uint16_t*>(ss);
+              const uint32_t u1 = *reinterpret_cast<const uint16_t*>(ss + 8 * SB);
+              acc[h][0] = fmaf(de[0] + dq[0], f32_scale<0>(u0 & 0xFFu, xe), acc[h][0]);
+              acc[h][0] = fmaf(de[1] + dq[1], f32_scale<0>(u0 >> 8, xe), acc[h][0]);
+              acc[h][1] = fmaf(de[2] + dq[2], f32_scale<0>(u1 & 0xFFu, xe), acc[h][1]);
+              acc[h][1] = fmaf(de[3] + dq[3], f32_scale<0>(u1 >> 8, xe), acc[h][1]);
+            } else {
+              acc[h][0] = fmaf((de[0] + dq[0]) + (de[1] + dq[1]), f32_scale<1>(ss[0], xe), acc[h][0]);
+              acc[h][1] = fmaf((de[2] + dq[2]) + (de[3] + dq[3]), f32_scale<1>(ss[8 * SB], xe), acc[h][1]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_w[slot]);
+        if (tid == 0) {
+          d_trace(p, 1, ws);
+          if (ws == 0) d_trace_cta(p, 11);
+        }
+      }
+      // row totals: threads t and t ^ 1 hold the two halves of a route's blocks
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        acc[h][0] += __shfl_xor_sync(0xffffffffu, acc[h][0], 1);
+        acc[h][1] += __shfl_xor_sync(0xffffffffu, acc[h][1], 1);
+      }
     }
+    bad = named_bar_or(2, kNC, bad);
+    // what the stores and output triggers need, before the descriptor slot is released
+    const float dscale = dp->scale;
+    const uint32_t dmask = dp->mask, douts = dp->outs;
+    int droute[kDGroupMax];
+#pragma unroll
+    for (int i = 0; i < kDGroupMax; ++i) droute[i] = dp->route[i];
+    const float drw0 = dp->rw[t >> 1], drw1 = dp->rw[2 + (t >> 1)];  // this thread's routes of halves 0 and 1
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_b[rb]);
     ++bs;
@@ -894,11 +1146,23 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
       synced = true;
       if (bad) continue;
     }
-    if (grp == 0 && t < 2) {
-      const int r = t ? r1 : r0;
-      const float v = (t ? acc1 : acc0) * dsc.scale;
+    // partial stores: FC1 in natural row order (splits innermost), times gs;
+    // FC2 times gs and the route's router weight
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int route, r;
+      float v;
+      if (!GRP || nr == 1) {
+        if (h > 0 || t >= 2) continue;
+        route = droute[0], r = t ? r1 : r0;
+        v = (t ? acc[0][1] : acc[0][0]) * (U.fc2 && G.on ? drw0 : dscale);
+      } else {
+        const int ri = 2 * h + (t >> 1);
+        if (ri >= nr) continue;
+        route = (t >> 1) ? droute[2 * h + 1] : droute[2 * h], r = (t & 1) ? r1 : r0;
+        v = ((t & 1) ? acc[h][1] : acc[h][0]) * (U.fc2 ? (h ? drw1 : drw0) : dscale);
+      }
       if (!U.fc2) {
-        // FC1 split partial in natural row order (splits innermost), times gs13
         int nat;
         if (p.act == 0) {
           const int i = U.tile * 64 + (r >> 5) * 16 + (r & 15);
@@ -907,76 +1171,102 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
           nat = U.tile * kTileRows + r;
           if (nat >= p.inter_pad) nat = -1;
         }
-        if (nat >= 0) p.p[((size_t)U.route * wnat + nat) * p.s1_stride + U.split] = v;
+        if (nat >= 0) p.p[((size_t)route * wnat + nat) * p.s1_stride + U.split] = v;
       } else {
-        // FC2 split partial times gs2 and the router weight
         const int n = U.tile * kTileRows + r;
-        if (n < p.hidden) p.q[((size_t)U.split * R + U.route) * p.hidden + n] = v;
+        if (n < p.hidden) p.q[((size_t)U.split * R + route) * p.hidden + n] = v;
       }
     }
     if (tid == 0) d_trace_cta(p, U.fc2 ? 6 : 7);
-    if (U.fc2 && U.split == p.s2 - 1 && (U.route % p.top_k) == 31 - __clz(dsc.mask)) {
-      // the token tile's last unit in unit order: the output warp sums it
-      const uint32_t eb = es & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 38))) {
-        bad = true;
-        continue;
+    if (U.fc2 && U.split == p.s2 - 1) {
+      // the output tiles this unit completes (in unit order): a one-route
+      // unit when its route is its token's last valid top-k slot, a grouped
+      // unit for the routes its descriptor marks
+      const int ntrig = G.on ? nr : 1;
+#pragma unroll
+      for (int i = 0; i < kDGroupMax; ++i) {
+        if (i >= ntrig) break;
+        int token;
+        uint32_t mask;
+        if (G.on) {
+          if (!((douts >> i) & 1u)) continue;
+          token = droute[i] / p.top_k;
+          mask = G.tmask[token];
+        } else {
+          if ((U.route % p.top_k) != 31 - __clz(dmask)) continue;
+          token = U.route / p.top_k;
+          mask = dmask;
+        }
+        const uint32_t eb = es & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 38))) {
+          bad = true;
+          break;
+        }
+        if (tid == 0) s_edesc[eb] = EDesc{U.tile, token, mask, 0};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&epi_full[eb]);
+        ++es;
       }
-      if (tid == 0) s_edesc[eb] = dsc;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&epi_full[eb]);
-      ++es;
+      if (bad) continue;
     }
     if (tid == 0) d_trace(p, 4, bs - 1);
   }
   // end of the output-tile sequence
   const uint32_t eb = es & 1;
   if (__all_sync(0xffffffffu, mbar_wait(&epi_empty[eb], ((es >> 1) & 1) ^ 1, ab, 39))) {
-    if (tid == 0) s_edesc[eb].u = -1;
+    if (tid == 0) s_edesc[eb].end = 1;
     __syncwarp();
     if (lane == 0) mbar_arrive(&epi_full[eb]);
   }
   if (tid == 0) d_trace_cta(p, 8);
 }
 
-template <int FMT>
+template <int FMT, bool GRP>
 cudaError_t launch_decode_fmt(const DecodeParams& p, int grid, cudaStream_t stream) {
-  auto kern = decode_moe_kernel<FMT>;
+  auto kern = decode_moe_kernel<FMT, GRP>;
   const size_t smem = DSmem<FMT>::total;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   return launch_cooperative(kern, grid, kDThreads, smem, stream, p);
 }
 
+const void* decode_kernel_ptr(int fmt, bool grouped) {
+  if (fmt == 0) return grouped ? reinterpret_cast<const void*>(decode_moe_kernel<0, true>)
+                               : reinterpret_cast<const void*>(decode_moe_kernel<0, false>);
+  return grouped ? reinterpret_cast<const void*>(decode_moe_kernel<1, true>)
+                 : reinterpret_cast<const void*>(decode_moe_kernel<1, false>);
+}
+
 // Resident CTAs per SM of the fused decode kernel on the current device: a
 // cooperative launch never exceeds the resident count, so every CTA runs at
 // once and a wait on another CTA's unit always ends (each wait is bounded as
-// well).  Kept per device, under a lock.
-cudaError_t decode_occupancy(int fmt, int* blocks_per_sm) {
+// well).  Kept per device and kernel, under a lock.
+cudaError_t decode_occupancy(int fmt, bool grouped, int* blocks_per_sm) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static std::mutex mu;
-  static int cached[64][2] = {};
+  static int cached[64][2][2] = {};
   std::lock_guard<std::mutex> lock(mu);
-  if (dev < 64 && cached[dev][fmt]) {
-    *blocks_per_sm = cached[dev][fmt];
+  if (dev < 64 && cached[dev][fmt][grouped]) {
+    *blocks_per_sm = cached[dev][fmt][grouped];
     return cudaSuccess;
   }
-  const void* k = fmt == 0 ? reinterpret_cast<const void*>(decode_moe_kernel<0>)
-                           : reinterpret_cast<const void*>(decode_moe_kernel<1>);
+  const void* k = decode_kernel_ptr(fmt, grouped);
   const size_t smem = fmt == 0 ? DSmem<0>::total : DSmem<1>::total;
   e = ensure_smem_limit(k, smem);
   int occ = 0;
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kDThreads, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 64) cached[dev][fmt] = occ;
+  if (dev < 64) cached[dev][fmt][grouped] = occ;
   *blocks_per_sm = occ;
   return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int fmt, int grid, cudaStream_t stream) {
-  return fmt == 0 ? launch_decode_fmt<0>(p, grid, stream) : launch_decode_fmt<1>(p, grid, stream);
+  const bool grouped = p.group_max > 1;
+  if (fmt == 0) return grouped ? launch_decode_fmt<0, true>(p, grid, stream) : launch_decode_fmt<0, false>(p, grid, stream);
+  return grouped ? launch_decode_fmt<1, true>(p, grid, stream) : launch_decode_fmt<1, false>(p, grid, stream);
 }
 
 }  // namespace b4

@@ -88,27 +88,38 @@ __device__ __forceinline__ void store_x4_f16(uint8_t* dst, float v0, float v1, f
   *reinterpret_cast<uint2*>(dst) = w;
 }
 
-// The four MMAs of one 64-wide stage for rows (r0, r0 + 8): codes w0 (row r0,
-// elements 0..7 and 8..15 of this thread's block) and w1 (row r1), the
-// activation slices at bp (quarters q = 0..3, 8 bytes each; zeros for a
-// thread whose column is not this stage's block).  Even quarters accumulate
-// into de, odd into dq.
-__device__ __forceinline__ void stage_mma_f16(const uint2& w0, const uint2& w1, const uint8_t* bp, float (&de)[4],
-                                              float (&dq)[4]) {
+// The f16 weight operand of one 64-wide stage for rows (r0, r0 + 8): codes
+// w0 (row r0, elements 0..7 and 8..15 of this thread's block) and w1 (row r1).
+struct F16Stage {
   uint32_t a[4], b[4], c[4], d[4];
-  e2m1x8_to_f16x2(w0.x, a[0], a[1], a[2], a[3]);
-  e2m1x8_to_f16x2(w1.x, b[0], b[1], b[2], b[3]);
-  e2m1x8_to_f16x2(w0.y, c[0], c[1], c[2], c[3]);
-  e2m1x8_to_f16x2(w1.y, d[0], d[1], d[2], d[3]);
-  const uint4 x01 = *reinterpret_cast<const uint4*>(bp);
-  const uint4 x23 = *reinterpret_cast<const uint4*>(bp + 16);
-  mma_16816_f16(de, a[0], b[0], a[1], b[1], x01.x, x01.y);
-  mma_16816_f16(dq, a[2], b[2], a[3], b[3], x01.z, x01.w);
-  mma_16816_f16(de, c[0], d[0], c[1], d[1], x23.x, x23.y);
-  mma_16816_f16(dq, c[2], d[2], c[3], d[3], x23.z, x23.w);
+};
+__device__ __forceinline__ void dequant_stage_f16(const uint2& w0, const uint2& w1, F16Stage& f) {
+  e2m1x8_to_f16x2(w0.x, f.a[0], f.a[1], f.a[2], f.a[3]);
+  e2m1x8_to_f16x2(w1.x, f.b[0], f.b[1], f.b[2], f.b[3]);
+  e2m1x8_to_f16x2(w0.y, f.c[0], f.c[1], f.c[2], f.c[3]);
+  e2m1x8_to_f16x2(w1.y, f.d[0], f.d[1], f.d[2], f.d[3]);
 }
 
-// fp32 block scale of a serving scale byte b, times 2^xe (the activations'
+// The four MMAs of one stage against the activation slices at bp (quarters
+// q = 0..3, 8 bytes each; zeros for a thread whose column is not this
+// stage's block).  Even quarters accumulate into de, odd into dq.
+__device__ __forceinline__ void mma_stage_f16(const F16Stage& f, const uint8_t* bp, float (&de)[4], float (&dq)[4]) {
+  const uint4 x01 = *reinterpret_cast<const uint4*>(bp);
+  const uint4 x23 = *reinterpret_cast<const uint4*>(bp + 16);
+  mma_16816_f16(de, f.a[0], f.b[0], f.a[1], f.b[1], x01.x, x01.y);
+  mma_16816_f16(dq, f.a[2], f.b[2], f.a[3], f.b[3], x01.z, x01.w);
+  mma_16816_f16(de, f.c[0], f.d[0], f.c[1], f.d[1], x23.x, x23.y);
+  mma_16816_f16(dq, f.c[2], f.d[2], f.c[3], f.d[3], x23.z, x23.w);
+}
+
+__device__ __forceinline__ void stage_mma_f16(const uint2& w0, const uint2& w1, const uint8_t* bp, float (&de)[4],
+                                              float (&dq)[4]) {
+  F16Stage f;
+  dequant_stage_f16(w0, w1, f);
+  mma_stage_f16(f, bp, de, dq);
+}
+
+// fp32 block scale of a prepared scale byte b, times 2^xe (the activations'
 // prescale): NVFP4 bits b * 2^20 + 0x38800000 are the E4M3 value, MXFP4 bits
 // b << 23 are 2^(b - 127).
 template <int FMT>

@@ -98,6 +98,14 @@ struct GemmParams {
 constexpr int kTraceLen = 2048;
 
 // The per-route decode path: one cooperative kernel (decode_moe.cu).
+// The per-route small-m kernel's grouped units: up to kDecodeGroupMax routes
+// of one local expert share a unit (and its weight stream) when m >= 2 and
+// m * top_k <= kDecodeGroupRoutes (the group table is in shared memory); a
+// grouped unit spans at most kDecodeMaxStages / kDecodeGroupMax K stages.
+constexpr int kDecodeGroupMax = 4;
+constexpr int kDecodeGroupRoutes = 256;
+constexpr int kDecodeMaxStages = 128;
+
 struct DecodeParams {
   const uint8_t* w1_codes;   // prepared W13 / W1
   const uint8_t* w1_scales;
@@ -120,7 +128,8 @@ struct DecodeParams {
   uint16_t* out;             // [m, H] bf16
   int s1, s2;                // K splits of FC1 and FC2
   int s1_stride;             // split stride of the FC1 partials: s1 rounded up to 1, 2, 4 or 8
-  int units1, units2;        // R * n_tiles1 * s1 and R * n_tiles2 * s2
+  int units1, units2;        // R * n_tiles1 * s1 and R * n_tiles2 * s2 (one route per unit)
+  int group_max;             // 1: one route per unit; kDecodeGroupMax: units of up to that many routes of one expert
   float* p;                  // FC1 split partials [R][N1 natural][s1_stride]
   float* q;                  // FC2 split partials [s2][R][H]
   size_t p_floats, q_floats; // sizes of p and q (filled with the not-yet-written marker)
