@@ -156,6 +156,7 @@ struct DSmem {
   static constexpr size_t lastg = gtab + 8 * kDGroupMaxRoutes;   // [groups] the group's routes (-1 past its size)
   static constexpr size_t tmask = lastg + 2 * kDGroupMaxRoutes;  // [m] last group (in unit order) of a token's routes
   static constexpr size_t total = tmask + 4 * kDGroupMaxRoutes;  // [m] valid top-k slots of each token
+  static_assert(gexp % 16 == 0, "the route experts are read 16 bytes at a time");
 };
 
 __device__ __forceinline__ int d_local_expert(const DecodeParams& p, int route) {
@@ -278,26 +279,47 @@ __device__ __forceinline__ float sum_splits(const float (&v)[S], int s1) {
 
 // Grouped units (m * top_k <= 256): every CTA builds the same group table,
 // one thread per route.  A valid route's rank is the number of earlier routes
-// of its local expert; ranks 0, 4, 8, ... open a group, which takes the next
-// three routes of that expert as well; a group's index is the number of groups
-// opened by earlier routes.  Then each token's last group (the largest index
-// among its valid routes) and its valid top-k slots.  Returns the number of
-// groups; scan[] takes one int per warp.
+// of its local expert (counted eight routes per shared-memory load, with the
+// last such route kept as its predecessor); ranks 0, 4, 8, ... open a group,
+// which the next three routes of that expert join (a member finds its group's
+// first route in at most three predecessor steps).  A group's index is the
+// number of groups opened by earlier routes.  Then each token's last group
+// (the largest index among its valid routes) and its valid top-k slots.
+// Returns the number of groups; scan[] takes one int per warp, and lastg[]
+// and tmask[] serve as scratch (predecessors, group of each opener) first.
 __device__ int build_groups(const DecodeParams& p, int R, short* gexp, short* grp, short* gtab, short* lastg,
                             uint32_t* tmask, int* scan) {
   const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+  short* prev = reinterpret_cast<short*>(tmask);  // [R] the route's predecessor of its expert (-1: none)
+  short* opener_group = lastg;                    // [R] group of a route that opens one
   int e = -1;
   if (i < R) {
     e = d_local_expert(p, i);
     gexp[i] = (short)e;
   }
+  if (i < kDGroupMaxRoutes && i >= R) gexp[i] = -2;  // past the routes: matches no expert
   __syncthreads();
-  bool lead = false;
+  int rank = 0, last = -1;
   if (e >= 0) {
-    int rank = 0;
-    for (int j = 0; j < i; ++j) rank += gexp[j] == e;
-    lead = (rank & (kDGroupMax - 1)) == 0;
+    const uint32_t key = (uint32_t)(uint16_t)e * 0x10001u;
+    for (int j = 0; j < i; j += 8) {
+      const uint4 w = *reinterpret_cast<const uint4*>(gexp + j);
+      const uint32_t m[4] = {__vcmpeq2(w.x, key), __vcmpeq2(w.y, key), __vcmpeq2(w.z, key), __vcmpeq2(w.w, key)};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int jj = j + 2 * q + hh;
+          if (jj < i && ((m[q] >> (16 * hh)) & 1u)) {
+            ++rank;
+            last = jj;
+          }
+        }
+      }
+    }
+    prev[i] = (short)last;
   }
+  const bool lead = e >= 0 && (rank & (kDGroupMax - 1)) == 0;
   const uint32_t b = __ballot_sync(0xffffffffu, lead);
   if (lane == 0) scan[warp] = __popc(b);
   __syncthreads();
@@ -309,17 +331,19 @@ __device__ int build_groups(const DecodeParams& p, int R, short* gexp, short* gr
   }
   if (lead) {
     const int g = before + __popc(b & ((1u << lane) - 1u));
-    short* mem = gtab + kDGroupMax * g;
-    mem[0] = (short)i;
-#pragma unroll
-    for (int k = 1; k < kDGroupMax; ++k) mem[k] = -1;
+    opener_group[i] = (short)g;
     grp[i] = (short)g;
-    int c = 1;
-    for (int j = i + 1; j < R && c < kDGroupMax; ++j)
-      if (gexp[j] == e) {
-        mem[c++] = (short)j;
-        grp[j] = (short)g;
-      }
+    gtab[kDGroupMax * g] = (short)i;
+#pragma unroll
+    for (int k = 1; k < kDGroupMax; ++k) gtab[kDGroupMax * g + k] = -1;
+  }
+  __syncthreads();
+  if (e >= 0 && !lead) {
+    int o = i;
+    for (int k = 0; k < (rank & (kDGroupMax - 1)); ++k) o = prev[o];
+    const int g = opener_group[o];
+    grp[i] = (short)g;
+    gtab[kDGroupMax * g + (rank & (kDGroupMax - 1))] = (short)i;
   }
   __syncthreads();
   if (i < p.m) {
@@ -364,25 +388,35 @@ __device__ __forceinline__ void issue_x_rows(const DecodeParams& p, const DGroup
 // The warp converts an x row in place to 128-wide f16 slots, each prescaled
 // by a power of two (exps[j]).  Lane l owns K positions 4l .. 4l+3 of a slot
 // (block l / 4, quarter l % 4), whose eight bytes are the same in the bf16 and
-// the f16 row.
+// the f16 row.  Four slots at a time, so their max-reductions overlap.
 __device__ __forceinline__ void convert_x_row(const DecodeParams& p, const DUnit& U, uint8_t* row, int* exps,
                                               int lane) {
   const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
-  for (int j = 0; 128 * j < nk; ++j) {
-    const int i = 128 * j + 4 * lane;  // four positions: all below the hidden size or all past it
-    uint8_t* dst = row + 256 * j + 8 * lane;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (i < nk && k0 + i < p.hidden) {
-      const uint2 w = *reinterpret_cast<const uint2*>(dst);
-      v[0] = __uint_as_float(w.x << 16), v[1] = __uint_as_float(w.x & 0xFFFF0000u);
-      v[2] = __uint_as_float(w.y << 16), v[3] = __uint_as_float(w.y & 0xFFFF0000u);
-    }
-    float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  const int ns = (nk + 127) / 128;
+  for (int j0 = 0; j0 < ns; j0 += 4) {
+    float v[4][4], a[4];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const int e = slot_prescale(a);
-    store_x4_f16(dst, v[0], v[1], v[2], v[3], e);
-    if (lane == 0) exps[j] = e;
+    for (int q = 0; q < 4; ++q) {
+      const int i = 128 * (j0 + q) + 4 * lane;  // four positions: all below the hidden size or all past it
+      v[q][0] = v[q][1] = v[q][2] = v[q][3] = 0.f;
+      if (j0 + q < ns && i < nk && k0 + i < p.hidden) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row + 256 * (j0 + q) + 8 * lane);
+        v[q][0] = __uint_as_float(w.x << 16), v[q][1] = __uint_as_float(w.x & 0xFFFF0000u);
+        v[q][2] = __uint_as_float(w.y << 16), v[q][3] = __uint_as_float(w.y & 0xFFFF0000u);
+      }
+      a[q] = fmaxf(fmaxf(fabsf(v[q][0]), fabsf(v[q][1])), fmaxf(fabsf(v[q][2]), fabsf(v[q][3])));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) a[q] = fmaxf(a[q], __shfl_xor_sync(0xffffffffu, a[q], o));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (j0 + q >= ns) break;
+      const int e = slot_prescale(a[q]);
+      store_x4_f16(row + 256 * (j0 + q) + 8 * lane, v[q][0], v[q][1], v[q][2], v[q][3], e);
+      if (lane == 0) exps[j0 + q] = e;
+    }
   }
 }
 // Waits for a unit's x copies, then converts every route's row (a grouped
@@ -466,52 +500,70 @@ __device__ __forceinline__ void store_h_slot(uint8_t* row, int* exps, int j, int
 // warps: h[i] = bf16(act(sum of the FC1 split partials, ascending split
 // order)), then the slot's power-of-two prescale and f16 as in convert_x_row.
 // Warp w takes items w, w + 8, ... of the (route, 128-wide slot) list; one
-// poll reads a SwiGLU item's gate and up partials, or two ReLU^2 items (w +
-// 16 i and w + 16 i + 8).  Returns false on timeout (the abort flag is
+// poll reads NS partial sources at once (4 for a split stride of 1,
+// else 2): the gate and up partials of NS / 2 SwiGLU items, or NS ReLU^2
+// items (w + 8 q for q < NS).  Returns false on timeout (the abort flag is
 // raised).
 template <int S>
 __device__ __forceinline__ bool build_h_f16(const DecodeParams& p, const DGroups& G, const DUnit& U, uint8_t* row,
                                             int* exps, int cw, int lane, int wnat, const Abort& ab) {
+  constexpr int NS = S == 1 ? 4 : 2;  // partial sources per poll (4 S floats each in registers)
   const int k0 = U.kbeg * kBK, nk = (U.kend - U.kbeg) * kBK;
   const int ns = (nk + 127) / 128;  // activation slots per route
   const int nr = G.on ? group_size(G, U.route) : 1;
   const int items = nr * ns;
-  auto part = [&](int i) {  // route i's FC1 partials of this K range
+  // item f: route f / ns, slot f % ns; the start of its partials, and whether
+  // this lane's four positions of it are inside the K range
+  auto item = [&](int f, bool& valid) {
+    const int i = f / ns, j = f - i * ns;
+    const int e = 128 * j + 4 * lane;
+    valid = f < items && e < nk;
+    if (!valid) return p.p;
     const int route = G.on ? (int)G.gtab[kDGroupMax * U.route + i] : U.route;
-    return p.p + ((size_t)route * wnat + k0) * S;
+    return p.p + ((size_t)route * wnat + k0 + e) * S;
+  };
+  auto store = [&](int f, bool valid, float (&h)[4]) {
+    const int i = f / ns, j = f - i * ns;
+    store_h_slot(row + i * kDGroupRowBytes, exps + i * kDGroupSlots, j, lane, valid, h);
   };
   if (p.act == 0) {
-    for (int f = cw; f < items; f += kDComputeWarps) {
-      const int i = f / ns, j = f - i * ns;
-      const int e = 128 * j + 4 * lane;
-      const bool valid = e < nk;
-      const float* gate = part(i) + (valid ? (size_t)e * S : 0);
-      const float* const src[2] = {gate, gate + (size_t)p.inter_pad * S};
-      const bool vv[2] = {valid, valid};
-      float gu[2][4];
-      if (!poll_sum4<S, 2>(gu, src, vv, p.s1, ab)) return false;
-      float h[4];
+    constexpr int NI = NS / 2;  // items per poll: gate and up of each
+    for (int f = cw; f < items; f += NI * kDComputeWarps) {
+      const float* src[NS];
+      bool vv[NS];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) h[c] = gu[0][c] / (1.0f + __expf(-gu[0][c])) * gu[1][c];
-      store_h_slot(row + i * kDGroupRowBytes, exps + i * kDGroupSlots, j, lane, valid, h);
+      for (int q = 0; q < NI; ++q) {
+        const float* gate = item(f + q * kDComputeWarps, vv[2 * q]);
+        vv[2 * q + 1] = vv[2 * q];
+        src[2 * q] = gate;
+        src[2 * q + 1] = vv[2 * q] ? gate + (size_t)p.inter_pad * S : p.p;
+      }
+      float gu[NS][4];
+      if (!poll_sum4<S, NS>(gu, src, vv, p.s1, ab)) return false;
+#pragma unroll
+      for (int q = 0; q < NI; ++q) {
+        if (f + q * kDComputeWarps >= items) break;
+        float h[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) h[c] = gu[2 * q][c] / (1.0f + __expf(-gu[2 * q][c])) * gu[2 * q + 1][c];
+        store(f + q * kDComputeWarps, vv[2 * q], h);
+      }
     }
   } else {
-    for (int f = cw; f < items; f += 2 * kDComputeWarps) {
-      const int f2 = f + kDComputeWarps;
-      const int i0 = f / ns, j0 = f - i0 * ns;
-      const int i1 = f2 / ns, j1 = f2 - i1 * ns;
-      const int e0 = 128 * j0 + 4 * lane, e1 = 128 * j1 + 4 * lane;
-      const bool vv[2] = {e0 < nk, f2 < items && e1 < nk};
-      const float* const src[2] = {part(i0) + (vv[0] ? (size_t)e0 * S : 0),
-                                   vv[1] ? part(i1) + (size_t)e1 * S : p.p};
-      float hh[2][4];
-      if (!poll_sum4<S, 2>(hh, src, vv, p.s1, ab)) return false;
+    for (int f = cw; f < items; f += NS * kDComputeWarps) {
+      const float* src[NS];
+      bool vv[NS];
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < NS; ++q) src[q] = item(f + q * kDComputeWarps, vv[q]);
+      float hh[NS][4];
+      if (!poll_sum4<S, NS>(hh, src, vv, p.s1, ab)) return false;
+#pragma unroll
+      for (int q = 0; q < NS; ++q) {
+        if (f + q * kDComputeWarps >= items) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c) hh[q][c] = hh[q][c] > 0.f ? hh[q][c] * hh[q][c] : 0.f;
-      store_h_slot(row + i0 * kDGroupRowBytes, exps + i0 * kDGroupSlots, j0, lane, vv[0], hh[0]);
-      if (f2 < items) store_h_slot(row + i1 * kDGroupRowBytes, exps + i1 * kDGroupSlots, j1, lane, vv[1], hh[1]);
+        store(f + q * kDComputeWarps, vv[q], hh[q]);
+      }
     }
   }
   return true;
