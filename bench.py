@@ -452,10 +452,10 @@ KERNEL_SOURCES = {
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
-    ("decode", "decode:relu2", 1): ("6afbab8cbd419728", 56_730_368 + 516_096),
-    ("decode_grouped", "small:silu", 16): ("fb6fd93ea1c81c44", 172_840_704 + 11_637_248),
-    ("grouped", "prefill:silu", 2048): ("7388b4351aa42727", 1_040_615_168 + 81_186_304 + 599_474_944 + 81_475_584),
-    ("grouped_wn", "small:silu", 64): ("56f8d50e964203f8", 180_107_776 + 4_443_904 + 90_863_616 + 293_888),
+    ("decode", "decode:relu2", 1): ("8874eb69c7851bbb", 56_734_976 + 464_128),
+    ("decode", "small:silu", 16): ("8874eb69c7851bbb", 170_994_688 + 4_823_808),
+    ("grouped", "prefill:silu", 2048): ("531af4956e9d4206", 1_040_424_448 + 81_145_856 + 599_408_640 + 81_539_328),
+    ("grouped_wn", "small:silu", 64): ("4085c3218d6bdfc4", 180_107_520 + 4_110_592 + 90_864_384 + 101_888),
 }
 
 

@@ -282,15 +282,19 @@ __device__ __forceinline__ float sum_splits(const float (&v)[S], int s1) {
 // of its local expert (counted eight routes per shared-memory load, with the
 // last such route kept as its predecessor); ranks 0, 4, 8, ... open a group,
 // which the next three routes of that expert join (a member finds its group's
-// first route in at most three predecessor steps).  A group's index is the
-// number of groups opened by earlier routes.  Then each token's last group
-// (the largest index among its valid routes) and its valid top-k slots.
+// first route in at most three predecessor steps).  Groups are ordered by
+// expert, then by rank, so that an expert's groups are neighbours in unit
+// order and its weights are re-read from L2: a group's index is the number of
+// groups of lower-numbered experts plus its rank / 4.  Then each token's last
+// group (the largest index among its valid routes) and its valid top-k slots.
 // Returns the number of groups; scan[] takes one int per warp, and lastg[]
-// and tmask[] serve as scratch (predecessors, group of each opener) first.
+// and tmask[] serve as scratch (predecessors, openers, group of each opener)
+// first.
 __device__ int build_groups(const DecodeParams& p, int R, short* gexp, short* grp, short* gtab, short* lastg,
                             uint32_t* tmask, int* scan) {
   const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
   short* prev = reinterpret_cast<short*>(tmask);  // [R] the route's predecessor of its expert (-1: none)
+  short* opens = prev + kDGroupMaxRoutes;          // [256] 0xFFFF where the route opens a group, else 0
   short* opener_group = lastg;                    // [R] group of a route that opens one
   int e = -1;
   if (i < R) {
@@ -320,17 +324,23 @@ __device__ int build_groups(const DecodeParams& p, int R, short* gexp, short* gr
     prev[i] = (short)last;
   }
   const bool lead = e >= 0 && (rank & (kDGroupMax - 1)) == 0;
+  if (i < kDGroupMaxRoutes) opens[i] = lead ? (short)-1 : (short)0;
   const uint32_t b = __ballot_sync(0xffffffffu, lead);
   if (lane == 0) scan[warp] = __popc(b);
   __syncthreads();
-  int before = 0, ng = 0;
-  for (int w = 0; w < kDThreads / 32; ++w) {
-    const int c = scan[w];
-    if (w < warp) before += c;
-    ng += c;
-  }
+  int ng = 0;
+  for (int w = 0; w < kDThreads / 32; ++w) ng += scan[w];
   if (lead) {
-    const int g = before + __popc(b & ((1u << lane) - 1u));
+    // groups of lower-numbered experts: openers with a smaller expert index
+    const uint32_t key = (uint32_t)(uint16_t)e * 0x10001u;
+    int bits = 0;  // 16 per opener
+    for (int j = 0; j < R; j += 8) {
+      const uint4 w = *reinterpret_cast<const uint4*>(gexp + j);
+      const uint4 o = *reinterpret_cast<const uint4*>(opens + j);
+      bits += __popc(__vcmpltu2(w.x, key) & o.x) + __popc(__vcmpltu2(w.y, key) & o.y) +
+              __popc(__vcmpltu2(w.z, key) & o.z) + __popc(__vcmpltu2(w.w, key) & o.w);
+    }
+    const int g = (bits >> 4) + rank / kDGroupMax;
     opener_group[i] = (short)g;
     grp[i] = (short)g;
     gtab[kDGroupMax * g] = (short)i;
