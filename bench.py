@@ -452,8 +452,8 @@ KERNEL_SOURCES = {
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
-    ("decode", "decode:relu2", 1): ("8874eb69c7851bbb", 56_734_976 + 464_128),
-    ("decode", "small:silu", 16): ("8874eb69c7851bbb", 170_994_688 + 4_823_808),
+    ("decode", "decode:relu2", 1): ("b4230ce056e0381b", 56_735_232 + 325_632),
+    ("decode", "small:silu", 16): ("b4230ce056e0381b", 171_003_904 + 4_829_952),
     ("grouped", "prefill:silu", 2048): ("531af4956e9d4206", 1_040_424_448 + 81_145_856 + 599_408_640 + 81_539_328),
     ("grouped_wn", "small:silu", 64): ("4085c3218d6bdfc4", 180_107_520 + 4_110_592 + 90_864_384 + 101_888),
 }
@@ -494,7 +494,7 @@ class LinearBench(Bench):
         # GEMM: with fewer (chunk, tile pair) units than SMs it splits K and adds
         # fp32 partials (events: memset + route pack, GEMM, rounding pass),
         # otherwise it stores bf16 (route pack, GEMM)
-        self.decode = m <= 16  # AUTO: the small-m kernels (per-route m <= 2, route-grouped above)
+        self.decode = m <= 16  # AUTO: the small-m kernels (per-route m <= 4, route-grouped above)
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         k_split = m < 96 and -(-m // 128) * ((-(-n // 128) + 1) // 2) < sms
         self.n_kernels = 1 if self.decode else (3 if k_split else 2)
@@ -536,7 +536,7 @@ def kernel_family(b):
     if b.decode:
         wl = b.wl
         if isinstance(b, LinearBench):
-            per_route = b.m <= 2
+            per_route = b.m <= 4
         else:
             r = b.m * wl.top_k
             e_l = wl.num_local_experts

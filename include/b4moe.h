@@ -77,7 +77,7 @@ typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activ
  * m * top_k <= 2 * num_local_experts (at most two routes per expert on
  * average), GROUPED otherwise: the crossover flashinfer PR #4255 (Reviewer
  * Notes) leaves to each card, as measured on GB300; b4_linear's AUTO takes the
- * small-m kernels for m <= 16 (the per-route kernel for m <= 2, the
+ * small-m kernels for m <= 16 (the per-route kernel for m <= 4, the
  * route-grouped one above). */
 typedef enum b4_path { B4_PATH_AUTO = 0, B4_PATH_DECODE = 1, B4_PATH_GROUPED = 2 } b4_path;
 
@@ -307,7 +307,7 @@ b4_status b4_fused_moe_noalloc(const b4_moe_config* cfg, const uint16_t* x, cons
  * cfg           m = tokens, hidden = K, inter = N, top_k = 1,
  *               num_global_experts = num_local_experts = 1, expert_map NULL,
  *               format, path (AUTO: the fused small-m kernels for m <= 16 --
- *               per-route for m <= 2, route-grouped above -- and the grouped
+ *               per-route for m <= 4, route-grouped above -- and the grouped
  *               tcgen05 GEMM beyond; DECODE is accepted for m <= B4_DECODE_MAX_M).
  * w, s          W prepared by b4_prepare_weights(cfg, which = 0,
  *               B4_ACT_RELU2, ...) -- the non-gated FC1 layout of one expert.

@@ -23,8 +23,8 @@ CASES = [
     # name, fmt, m, n, k, path ("auto" / "decode" / "grouped"), weights
     ("nv_m1_full", NV, 1, 4096, 4096, "auto", "random"),
     ("nv_m2", NV, 2, 768, 1536, "auto", "quantized"),      # per-route small-m kernel
-    ("nv_m3", NV, 3, 640, 1024, "auto", "quantized"),      # route-grouped small-m kernel
-    ("nv_m16", NV, 16, 384, 2048, "auto", "quantized"),
+    ("nv_m3", NV, 3, 640, 1024, "auto", "quantized"),      # per-route kernel, three tokens in one grouped unit
+    ("nv_m16", NV, 16, 384, 2048, "auto", "quantized"),    # route-grouped small-m kernel
     ("nv_m64", NV, 64, 256, 512, "auto", "quantized"),
     ("nv_m40_decode", NV, 40, 256, 1024, "decode", "quantized"),
     ("nv_m16_full", NV, 16, 4096, 4096, "auto", "random"),

@@ -88,13 +88,14 @@ b4_status cuda_fail(cudaError_t e, const char* what) {
 // the route-grouped kernel wins again (small-batch m = 32: 139 against 145).
 constexpr int kDecodeAutoMaxM = 16;  // AUTO takes a small-m kernel up to here
 constexpr int kPerRouteMaxM = 4;     // the per-route kernel up to here, and while m top_k <= 2 E_local (grouped units)
-// b4_linear (N = K = 4096, back-to-back calls): the per-route kernel re-reads W
-// per token (m = 1 / 2 / 3 / 4: 9.8 / 13.2 / 16.3 / 18.8 us), the route-grouped
-// kernel reads it once per 8 tokens (14.4 - 14.7 us for m = 1..4, 15.6 at m = 8,
-// 19.8 at m = 16) against the K-split grouped GEMM (21.9 us at m = 8 and 16, on
-// par from m = 32).
+// b4_linear (N = K = 4096, back-to-back calls): the per-route kernel reads W
+// once per token at m = 1 and once per four tokens from m = 2 (grouped units;
+// m = 1 / 2 / 3 / 4: 9.3 / 11.4 / 12.9 / 13.7 us), the route-grouped kernel once
+// per 8 tokens (15.2 - 15.4 us for m = 3..4, 15.9 at m = 8, 20.0 at m = 16;
+// the per-route kernel 18.7 / 27.2 there) against the K-split grouped GEMM
+// (21.9 us at m = 8 and 16, on par from m = 32).
 constexpr int kLinearSmallMaxM = 16;    // b4_linear's AUTO takes the small-m kernels up to here
-constexpr int kLinearPerRouteMaxM = 2;  // b4_linear's small-m path: the per-route kernel up to here
+constexpr int kLinearPerRouteMaxM = 4;  // b4_linear's small-m path: the per-route kernel up to here
 constexpr int kDecodeW0 = 4;        // small-m partition: a stage costs kDecodeW0 + its route column sets
 constexpr int kMaxSplits = 8;
 
@@ -719,24 +720,28 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
 
   if (small && m <= kLinearPerRouteMaxM) {
     // The fused small-m kernel: K-split GEMV units, then one output unit per
-    // (token, 128 columns) that sums the split partials into out.
+    // (token, 128 columns) that sums the split partials into out.  From m = 2
+    // its FC1 units take up to four tokens each (grouped units: every token
+    // goes to the one weight matrix, so there are ceil(m / 4) groups).
+    const int group_max = m >= 2 && g1.k_stages <= kDecodeMaxStages ? kDecodeGroupMax : 1;
+    const int groups = (m + group_max - 1) / group_max;
     int occ = 0;
-    if ((e = decode_occupancy(fmt, false, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
+    if ((e = decode_occupancy(fmt, group_max > 1, &occ)) != cudaSuccess) return cuda_fail(e, "decode occupancy");
     if (occ < 1) return fail(B4_ERR_CUDA, "the decode kernel does not fit on an SM");
     // K splits: about two GEMV units per CTA, at least 8 stages each, at
     // most the partial buffer's split count (summing up to 8 partials per
     // output is cheap here: no activation row is built from them).
     const int cap = occ * dev.sms;
-    const long long base = (long long)m * g1.n_tiles;
+    const long long base = (long long)groups * g1.n_tiles;
     int s1 = (int)((2LL * cap + base - 1) / base);
     const int most = g1.k_stages / 8 > 1 ? g1.k_stages / 8 : 1;
     if (s1 > most) s1 = most;
     if (s1 > L.dec_splits) s1 = L.dec_splits;
-    const int least = (g1.k_stages + 127) / 128;
+    const int least = (g1.k_stages * group_max + kDecodeMaxStages - 1) / kDecodeMaxStages;
     if (s1 < least) s1 = least;
     const DecodePlan plan{s1, 1, 0};
     DecodeParams dp{};
-    dp.group_max = 1;
+    dp.group_max = group_max;
     dp.w1_codes = w;
     dp.w1_scales = sc;
     dp.gs1 = gs;

@@ -208,7 +208,8 @@ __device__ __forceinline__ void d_unit_shape(const DecodeParams& p, int units1, 
 
 __device__ __forceinline__ bool d_unit(const DecodeParams& p, const DGroups& G, int units1, int u, DUnit& U) {
   d_unit_shape(p, units1, u, U);
-  U.expert = G.on ? G.gexp[G.gtab[4 * U.route]] : d_local_expert(p, U.route);
+  // a dense linear layer's output units stay one per route
+  U.expert = G.on && !(U.fc2 && p.linear) ? G.gexp[G.gtab[4 * U.route]] : d_local_expert(p, U.route);
   return U.expert >= 0 && U.kend > U.kbeg;
 }
 
@@ -706,7 +707,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
   if (G.on) G.ng = build_groups(p, R, s_gexp, s_grp, s_gtab, s_lastg, s_tmask, s_xexp);
   const int base = G.on ? G.ng : R;
   const int units1 = G.on ? base * p.n_tiles1 * p.s1 : p.units1;
-  const int n_units = units1 + (G.on ? base * p.n_tiles2 * p.s2 : p.units2);
+  const int n_units = units1 + (G.on && !p.linear ? base * p.n_tiles2 * p.s2 : p.units2);
 
   // The producers resolve the CTA's first unit and start its weight stream
   // and (FC1) x slices before the grid barrier: neither touches the partial
@@ -888,14 +889,15 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_moe_kernel(cons
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_b[rb]);
       } else if (p.linear || G.on) {
-        // an output unit of the dense linear layer, or a grouped FC2 unit
+        // an output unit of the dense linear layer (one route), or a grouped FC2 unit
         if (lane == 0) {
           dsc->u = u;
           dsc->expert = U.expert;
           mbar_arrive(&desc_full[rb]);
           dsc->scale = 1.0f;
           dsc->mask = 1u;
-          fill_routes(p, G, U, dsc);
+          if (p.linear) dsc->nr = 1;
+          else fill_routes(p, G, U, dsc);
           mbar_arrive(&full_b[rb]);
         }
       } else {
