@@ -129,14 +129,18 @@ def test_parity_full_size_sampled(b4, name, act, m):
     assert_parity(got[toks], ref, f"{name}/{act}/m={m} ({len(toks)} tokens)")
 
 
-FORCED = [("mxfp4", "silu", 4), ("mxfp4", "relu2", 4), ("mxfp4", "silu", 24), ("decode", "silu", 8)]
+FORCED = [("mxfp4", "silu", 4), ("mxfp4", "relu2", 4), ("mxfp4", "silu", 24), ("decode", "silu", 8),
+          ("decode", "relu2", 16), ("mxfp4", "silu", 12)]
 
 
 @pytest.mark.parametrize("name,act,m", FORCED, ids=[f"{n}-{a}-m{m}" for n, a, m in FORCED])
 def test_parity_full_size_decode_forced(b4, name, act, m):
     """Full-size shapes on the small-m path whatever AUTO would pick: the
     MXFP4 workload (E8M0 scales per 32, H = 2880 and I = 1440 not multiples of
-    128) on the per-route kernel (m = 4) and the route-grouped one (m = 24)."""
+    128, an expert_map dropping experts, invalid ids) on the per-route kernel
+    with one route per unit (m = 4), with grouped units (m = 12: 48 routes on
+    28 local experts) and on the route-grouped kernel (m = 24); the decode
+    workload with grouped units at m = 16 (128 routes on 128 experts)."""
     wl = W.WORKLOADS[name].with_act(act)
     hl = host_layer(wl, m, seed=13, weights="random")
     dl = DeviceLayer(hl, path=b4.PATH_DECODE)
