@@ -640,9 +640,11 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     pp->chunks = rp.chunks;
   }
   uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);
-  if (!make_tmap_bf16_2d(&p1.tmap_b, xp, (uint64_t)L.r_cap, (uint64_t)cfg->hidden, 32))
+  // B boxes: 32 rows for the weights-on-N kernel's operand stages, 80 for the
+  // weights-on-M kernel (two per 160-row stage)
+  if (!make_tmap_bf16_2d(&p1.tmap_b, xp, (uint64_t)L.r_cap, (uint64_t)cfg->hidden, weights_on_n ? 32 : 80))
     return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the packed-x map");
-  if (!make_tmap_bf16_2d(&p2.tmap_b, hbuf, (uint64_t)L.r_cap, (uint64_t)L.inter_pad, 32))
+  if (!make_tmap_bf16_2d(&p2.tmap_b, hbuf, (uint64_t)L.r_cap, (uint64_t)L.inter_pad, weights_on_n ? 32 : 80))
     return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the h map");
   p1.h_out = hbuf;
   p1.acc_out = acc;
@@ -913,7 +915,7 @@ b4_status b4_linear(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* 
   p1.sorted_routes = rp.sorted_routes;
   p1.chunk_count = rp.chunk_count;
   p1.chunks = rp.chunks;
-  if (!make_tmap_bf16_2d(&p1.tmap_b, x, (uint64_t)m, (uint64_t)K, 32))
+  if (!make_tmap_bf16_2d(&p1.tmap_b, x, (uint64_t)m, (uint64_t)K, weights_on_n ? 32 : 80))
     return fail(B4_ERR_CUDA, "cuTensorMapEncodeTiled rejected the x map");
   const bool direct = N == L.inter_pad;  // rows of h are rows of out
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.h);
