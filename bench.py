@@ -454,7 +454,7 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
     ("decode", "decode:relu2", 1): ("b4230ce056e0381b", 56_735_232 + 325_632),
     ("decode", "small:silu", 16): ("b4230ce056e0381b", 171_003_904 + 4_829_952),
-    ("grouped", "prefill:silu", 2048): ("531af4956e9d4206", 1_040_424_448 + 81_145_856 + 599_408_640 + 81_539_328),
+    ("grouped", "prefill:silu", 2048): ("b1b97e535c66c3b7", 1_040_458_496 + 80_837_120 + 599_910_400 + 81_796_352),
     ("grouped_wn", "small:silu", 64): ("4085c3218d6bdfc4", 180_107_520 + 4_110_592 + 90_864_384 + 101_888),
 }
 
