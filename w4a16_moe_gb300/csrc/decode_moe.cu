@@ -1,7 +1,7 @@
 // Small-m decode path of the fused W4A16 MoE layer (flashinfer PR #4255,
 // Description: "A tensor-core decode path for small batches on the packed
 // serving weights"): ONE cooperative persistent kernel for FC1, the
-// activation, FC2 and the top-k combine.
+// activation, FC2 and the top-k combine.  Two CTAs per SM, 11 warps each.
 //
 // With one route per work unit both GEMMs are matrix-vector products over the
 // expert's weights: HBM-bound at 4 bits per weight.  The kernel is built so
@@ -10,7 +10,9 @@
 //
 // Work units, in this order: FC1 units (route, 128-row tile, K split), then FC2
 // units (route, 128-row tile of H, K split).  CTA b's first two units are b and
-// b + G (G CTAs); later ones are claimed from a counter in unit order.
+// b + G (G CTAs); later ones are claimed from a counter in unit order.  In the
+// grouped instantiation (routes that repeat experts) a unit's "route" is a
+// group of up to four routes of one expert, which share its weight stream.
 //
 //   warp 0        streams the unit's packed codes and scales, four 64-wide K
 //                 stages per slot of a shared-memory ring (two copies of
@@ -19,22 +21,21 @@
 //                 stream (FC2 included) starts while this one computes.  It
 //                 also issues the CTA's first x slice, ahead of its weights.
 //   warp 1        resolves each unit once (expert, scale factors, the token's
-//                 valid top-k slots), copies an FC1 unit's bf16 x slice into
-//                 a row buffer (one bulk copy) and converts it there to the
-//                 f16 slots the compute warps read.
-//   warps 2..     compute warps, 16 weight rows each (two of a K group's
-//                 128): hardware E2M1 -> f16 conversion feeding warp-level
-//                 m16n8k16 f16 MMAs whose activation operand is block
-//                 diagonal, block scales applied to the fp32 block sums
-//                 (decode_stage.cuh); each unit ends with an fp32 split
-//                 partial store.  An FC2 unit first builds its h slice,
-//                 bf16(act(sum of the FC1 partials)), as f16 slots.  With two
-//                 K groups (one CTA per SM) the second group takes the second
-//                 half of every slot and hands its row sums to the first.
-//   last warp     makes the CTA's grid-barrier arrival and wait (below), then
+//                 valid top-k slots, a group's routes), copies an FC1 unit's
+//                 bf16 x slices into a row buffer (one bulk copy per route)
+//                 and converts them there to the f16 slots the compute warps
+//                 read.
+//   warps 2..9    compute warps, 16 weight rows each of the unit's 128:
+//                 hardware E2M1 -> f16 conversion feeding warp-level m16n8k16
+//                 f16 MMAs whose activation operand is block diagonal, block
+//                 scales applied to the fp32 block sums (decode_stage.cuh);
+//                 each unit ends with an fp32 split partial store per route.
+//                 An FC2 unit first builds its h slices, bf16(act(sum of the
+//                 FC1 partials)), as f16 slots.
+//   warp 10       makes the CTA's grid-barrier arrival and wait (below), then
 //                 stores the bf16 output of a token's 128-column tile: it sums
 //                 the FC2 partials of the token's valid routes (ascending
-//                 top-k slot, then split) for the tile's last unit in unit
+//                 top-k slot, then split) after the tile's last unit in unit
 //                 order.  Fixed orders: the output is bitwise reproducible.
 //
 // Hand-offs between CTAs without counters or fences: before one grid barrier
