@@ -51,8 +51,9 @@ CASES = [
     # as many routes as local experts: the per-route kernel's boundary (m * top_k = E_l)
     ("decode_w", "relu2", 16),
     # AUTO above m = 16 while an expert gets at most two routes: the small-m
-    # path, on the per-route kernel's grouped units
-    ("decode_w", "relu2", 24),
+    # path, on the per-route kernel's grouped units; m = 32 fills the group
+    # table (256 routes, one thread each)
+    ("decode_w", "relu2", 24), ("decode_w", "silu", 32),
 ]
 
 
