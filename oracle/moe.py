@@ -17,8 +17,15 @@ taken where the pages are silent:
   ReLU^2 is non-gated with W1 of I rows;
 * the FC1 global scale gs13 multiplies the FC1 accumulator before the
   activation; the FC2 global scale gs2 multiplies the FC2 accumulator;
-* silu(z) = z / (1 + exp(-z)), no clamp and no alpha (SiTU and swiglu-oai
-  are excluded by the Description);
+* silu(z) = z / (1 + exp(-z)), no clamp and no alpha;
+* "swiglu_oai" -- swiglu-oai, which the Description lists as not included
+  and the b12x PR's CodeRabbit summary alludes to ("SwiGLU parameters"),
+  defined by neither -- is read as the clamped swiglu of the gpt-oss models:
+  g' = min(gate, limit), u' = clip(up, -limit, limit),
+  h = g' * sigmoid(alpha * g') * (u' + beta), with alpha, beta and limit
+  given by the caller (gpt-oss: 1.702, 1, 7).  Gate and up are the same W13
+  row halves as for "silu".  SiTU is not built: neither the pages nor a
+  standard source fixes its formula;
 * the intermediate h is rounded to bf16 once, after the activation and
   before FC2 -- the one place the GPU rounds it;
 * the router weight multiplies each route's FC2 output in the combine (the
@@ -41,6 +48,8 @@ from .routing import local_experts
 
 SILU = "silu"
 RELU2 = "relu2"
+SWIGLU_OAI = "swiglu_oai"
+GATED = (SILU, SWIGLU_OAI)  # activations whose W13 holds gate and up rows
 
 
 def silu(z):
@@ -49,12 +58,32 @@ def silu(z):
         return z / (1.0 + np.exp(-z))
 
 
-def activation_fn(a, act, inter):
-    """Apply the FC1 epilogue activation to fp64 FC1 outputs a [..., N1]."""
+def swiglu_oai(gate, up, alpha, beta, limit):
+    """The clamped swiglu (the reading stated in the module docstring).
+
+    The gate is bounded above only, the up projection on both sides; a limit
+    of +inf leaves both as they are.
+    """
+    g = np.minimum(np.asarray(gate, dtype=np.float64), limit)
+    u = np.clip(np.asarray(up, dtype=np.float64), -limit, limit)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-alpha * g)) * (u + beta)
+
+
+def activation_fn(a, act, inter, swiglu=None):
+    """Apply the FC1 epilogue activation to fp64 FC1 outputs a [..., N1].
+
+    ``swiglu`` = (alpha, beta, limit), required for "swiglu_oai".
+    """
+    if act in GATED and a.shape[-1] != 2 * inter:
+        raise ValueError("a gated activation expects N1 = 2 * inter")
     if act == SILU:
-        if a.shape[-1] != 2 * inter:
-            raise ValueError("SwiGLU expects N1 = 2 * inter")
         return silu(a[..., :inter]) * a[..., inter:]
+    if act == SWIGLU_OAI:
+        if swiglu is None:
+            raise ValueError("swiglu_oai needs (alpha, beta, limit)")
+        alpha, beta, limit = swiglu
+        return swiglu_oai(a[..., :inter], a[..., inter:], alpha, beta, limit)
     if act == RELU2:
         if a.shape[-1] != inter:
             raise ValueError("ReLU^2 expects N1 = inter")
@@ -67,7 +96,7 @@ def _check_inputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act):
     e_l, n1, half_h = w13.shape
     if half_h * 2 != hidden:
         raise ValueError("w13 K dimension does not match hidden")
-    inter = n1 // 2 if act == SILU else n1
+    inter = n1 // 2 if act in GATED else n1
     if w2.shape != (e_l, hidden, inter // 2):
         raise ValueError(f"w2 shape {w2.shape} != {(e_l, hidden, inter // 2)}")
     g = GROUP[fmt]
@@ -80,7 +109,7 @@ def _check_inputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act):
     return m, hidden, inter, e_l
 
 
-def expert_route_outputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act, expert, rows):
+def expert_route_outputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act, expert, rows, swiglu=None):
     """FC1 -> activation -> bf16 -> FC2 for the routes of one local expert.
 
     x rows ``rows`` (token indices) -> y [len(rows), H] in float64, including
@@ -97,7 +126,7 @@ def expert_route_outputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act, expert, rows)
     a = xa @ wq13.T
     if g13 is not None:
         a = a * g13
-    h = bf16_rn(activation_fn(a, act, inter))
+    h = bf16_rn(activation_fn(a, act, inter, swiglu))
     y = h @ wq2.T
     if g2 is not None:
         y = y * g2
@@ -121,6 +150,7 @@ def fused_moe(
     expert_map=None,
     tokens=None,
     return_prerounded=False,
+    swiglu=None,
 ):
     """Reference output of the fused W4A16 MoE layer.
 
@@ -129,6 +159,8 @@ def fused_moe(
     experts.  topk_ids [m, k] int, topk_weights [m, k] float32.
     ``tokens`` optionally restricts the computation to a subset of rows (the
     output then has one row per listed token, in the given order).
+
+    ``swiglu`` = (alpha, beta, limit) of the "swiglu_oai" activation.
 
     Returns out [len(tokens), H] float64 holding bf16 values; with
     ``return_prerounded`` also the float64 combine before its bf16 rounding.
@@ -146,7 +178,7 @@ def fused_moe(
     for e in sorted({int(loc[t, j]) for t in toks for j in range(k) if loc[t, j] >= 0}):
         routes = [(int(t), j) for t in toks for j in range(k) if loc[t, j] == e]
         rows = np.array([t for t, _ in routes], dtype=np.int64)
-        y, _ = expert_route_outputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act, e, rows)
+        y, _ = expert_route_outputs(x, w13, s13, gs13, w2, s2, gs2, fmt, act, e, rows, swiglu)
         for (t, j), yr in zip(routes, y):
             y_of_route[(t, j)] = yr
 

@@ -13,7 +13,7 @@ E4M3_ONE = 0x38
 
 
 def _rand_layer(rng, e, hidden, inter, act, fmt=Q.NVFP4):
-    n1 = 2 * inter if act == M.SILU else inter
+    n1 = 2 * inter if act in M.GATED else inter
     w13 = rng.standard_normal((e, n1, hidden)) * 0.05
     w2 = rng.standard_normal((e, hidden, inter)) * 0.05
     c13, s13, g13 = Q.quantize(w13, fmt)
@@ -173,3 +173,97 @@ def test_route_pack_and_layer_agree_on_validity():
     c, o, s = R.route_pack(ids, 10, 6, em)
     loc = R.local_experts(ids, 10, 6, em)
     assert int(o[-1]) == int((loc >= 0).sum())
+
+
+# ---------------------------------------------------------------- swiglu-oai
+OAI = (1.702, 1.0, 7.0)
+
+
+def _torch_clamped_swiglu(gate, up, alpha, beta, limit):
+    """Independent form: g sigmoid(alpha g) = silu(alpha g) / alpha (torch's
+    silu and clamp), so no line of the oracle's formula is retyped."""
+    g = torch.clamp(torch.as_tensor(gate, dtype=torch.float64), max=limit)
+    u = torch.clamp(torch.as_tensor(up, dtype=torch.float64), min=-limit, max=limit)
+    return (torch.nn.functional.silu(alpha * g) / alpha * (u + beta)).numpy()
+
+
+def test_clamped_swiglu_matches_the_silu_identity():
+    rng = np.random.default_rng(11)
+    gate = rng.standard_normal(4096) * 6
+    up = rng.standard_normal(4096) * 6
+    for alpha, beta, limit in (OAI, (1.0, 0.0, np.inf), (0.5, -2.0, 3.0), (2.5, 1.0, 0.25)):
+        got = M.swiglu_oai(gate, up, alpha, beta, limit)
+        assert np.allclose(got, _torch_clamped_swiglu(gate, up, alpha, beta, limit), rtol=1e-13, atol=1e-300)
+
+
+def test_clamped_swiglu_without_clamp_is_swiglu():
+    """alpha 1, beta 0, no limit: silu(gate) * up, torch's silu."""
+    rng = np.random.default_rng(12)
+    gate, up = rng.standard_normal(1000) * 8, rng.standard_normal(1000) * 8
+    want = (torch.nn.functional.silu(torch.from_numpy(gate)) * torch.from_numpy(up)).numpy()
+    assert np.allclose(M.swiglu_oai(gate, up, 1.0, 0.0, np.inf), want, rtol=1e-14, atol=0)
+
+
+def test_clamped_swiglu_special_values():
+    alpha, beta, limit = OAI
+    f = lambda g, u: float(M.swiglu_oai(g, u, alpha, beta, limit))
+    # zero gate, and an up projection of exactly -beta, give exact zeros
+    assert f(0.0, 3.0) == 0.0 and f(2.0, -beta) == 0.0
+    # the gate saturates above the limit only
+    assert f(limit, 0.5) == f(3 * limit, 0.5) == f(1e30, 0.5)
+    assert f(-limit, 0.5) != f(-3 * limit, 0.5)
+    assert abs(f(-1e3, 0.5)) < 1e-300
+    # the up projection saturates on both sides
+    assert f(1.0, limit) == f(1.0, 50.0) and f(1.0, -limit) == f(1.0, -50.0)
+    # at the limit: limit * sigmoid(alpha limit) * (limit + beta), sigmoid from math.exp
+    import math
+    want = limit / (1 + math.exp(-alpha * limit)) * (limit + beta)
+    assert math.isclose(f(limit, limit), want, rel_tol=1e-15)
+    # NaN stays NaN
+    assert np.isnan(M.swiglu_oai(np.nan, 1.0, alpha, beta, limit))
+
+
+def test_activation_fn_gate_and_up_halves():
+    """Rows [0, I) are the gate and [I, 2I) the up projection, as for silu:
+    swapping the halves changes the result."""
+    rng = np.random.default_rng(13)
+    a = rng.standard_normal((3, 2 * 40)) * 5
+    got = M.activation_fn(a, M.SWIGLU_OAI, 40, OAI)
+    assert np.allclose(got, _torch_clamped_swiglu(a[:, :40], a[:, 40:], *OAI), rtol=1e-13)
+    assert not np.allclose(got, _torch_clamped_swiglu(a[:, 40:], a[:, :40], *OAI))
+    with pytest.raises(ValueError):
+        M.activation_fn(a, M.SWIGLU_OAI, 40)  # parameters are required
+
+
+@pytest.mark.parametrize("fmt", [Q.NVFP4, Q.MXFP4])
+def test_clamped_swiglu_layer_is_a_dense_mlp(fmt):
+    """E = 1, top-1, weight 1, with a limit the FC1 outputs cross: the layer
+    is a dense clamped-swiglu MLP (torch fp64, dequantised by table)."""
+    rng = np.random.default_rng(14)
+    hidden, inter, m = 64, 64, 9
+    c13, s13, g13, c2, s2, g2 = _rand_layer(rng, 1, hidden, inter, M.SWIGLU_OAI, fmt)
+    x = _bf16_x(rng, m, hidden) * 8
+    ids = np.zeros((m, 1), np.int32)
+    wts = np.ones((m, 1), np.float32)
+    params = (1.702, 1.0, 0.5)
+    out, pre = M.fused_moe(x, c13, s13, g13, c2, s2, g2, ids, wts, M.SWIGLU_OAI, fmt, 1, return_prerounded=True,
+                           swiglu=params)
+    table = torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6], dtype=torch.float64)
+    e4m3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+
+    def deq(c, s, g):
+        c = torch.from_numpy(c.astype(np.int64))
+        codes = torch.stack([c & 15, c >> 4], dim=-1).reshape(c.shape[0], -1)
+        s = torch.from_numpy(s.astype(np.int64))
+        if fmt == Q.NVFP4:
+            return table[codes] * e4m3[s].repeat_interleave(16, dim=1) * float(g)
+        return table[codes] * torch.pow(2.0, (s - 127).to(torch.float64)).repeat_interleave(32, dim=1)
+
+    W13 = deq(c13[0], s13[0], None if g13 is None else g13[0])
+    W2 = deq(c2[0], s2[0], None if g2 is None else g2[0])
+    a = torch.from_numpy(x) @ W13.T
+    assert (a[:, :inter] > params[2]).any() and (a[:, inter:].abs() > params[2]).any()  # the clamps act
+    h = torch.from_numpy(F.bf16_rn(_torch_clamped_swiglu(a[:, :inter], a[:, inter:], *params)))
+    y = h @ W2.T
+    assert np.allclose(pre, y.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, F.bf16_rn(y.numpy()))

@@ -48,11 +48,13 @@ class Workload:
     top_k: int
     hidden: int
     inter: int
-    act: str  # "silu" or "relu2"
+    act: str  # "silu", "relu2" or "swiglu_oai"
     ms: tuple
     hot_experts: int = 0
     drop_globals: tuple = ()
     invalid_frac: float = 0.0
+    # (alpha, beta, limit) of "swiglu_oai": the gpt-oss values by default
+    swiglu: tuple = (1.702, 1.0, 7.0)
 
     @property
     def group(self) -> int:
@@ -60,10 +62,12 @@ class Workload:
 
     @property
     def n1(self) -> int:
-        return 2 * self.inter if self.act == "silu" else self.inter
+        return 2 * self.inter if self.act in ("silu", "swiglu_oai") else self.inter
 
-    def with_act(self, act: str) -> "Workload":
-        return dataclasses.replace(self, act=act)
+    def with_act(self, act: str, swiglu=None) -> "Workload":
+        if swiglu is None:
+            return dataclasses.replace(self, act=act)
+        return dataclasses.replace(self, act=act, swiglu=tuple(swiglu))
 
     def scaled(self, hidden=None, inter=None, experts=None, top_k=None) -> "Workload":
         """Same structure, smaller sizes (for fast parity cases).
