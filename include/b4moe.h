@@ -63,8 +63,17 @@ typedef enum b4_format { B4_NVFP4_E4M3_K16 = 0, B4_MXFP4_E8M0_K32 = 1 } b4_forma
 /* FC1 epilogue activations (flashinfer PR #4255, Performance: relu2, silu).
  * SILU_SWIGLU: W13 has 2*inter rows, rows [0, inter) gate and [inter, 2*inter)
  *              up; h = silu(gate) * up.
- * RELU2:       W1 has inter rows; h = max(a, 0)^2. */
-typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1 } b4_activation;
+ * RELU2:       W1 has inter rows; h = max(a, 0)^2.
+ * SWIGLU_OAI:  the clamped swiglu of the gpt-oss models, which the pages name
+ *              (flashinfer PR #4255, Description: "swiglu-oai"; b12x PR, CodeRabbit
+ *              summary: "SwiGLU parameters") without defining it.  W13 as for
+ *              SILU_SWIGLU (gate rows first: a checkpoint that interleaves gate
+ *              and up rows is de-interleaved before b4_prepare_weights);
+ *              g' = min(gate, limit), u' = up clamped to [-limit, limit],
+ *              h = g' * sigmoid(alpha * g') * (u' + beta), with alpha, beta and
+ *              limit from b4_moe_config (gpt-oss: 1.702, 1, 7).  Prepared
+ *              weights are shared with SILU_SWIGLU. */
+typedef enum b4_activation { B4_ACT_SILU_SWIGLU = 0, B4_ACT_RELU2 = 1, B4_ACT_SWIGLU_OAI = 2 } b4_activation;
 
 /* Execution path of b4_fused_moe.  DECODE is the small-m path (accepted for
  * m <= B4_DECODE_MAX_M): one cooperative launch, a per-route kernel for
@@ -98,6 +107,12 @@ typedef struct b4_moe_config {
    * NULL means the identity (then E_g must equal E_l).  flashinfer PR #4255,
    * Tests: "covering expert_map, invalid expert ids". */
   const int32_t* expert_map;
+  /* B4_ACT_SWIGLU_OAI only (b4_fused_moe reads them for that activation and
+   * ignores them otherwise): alpha and beta finite, limit > 0 (+inf: no
+   * clamp); anything else is B4_ERR_INVALID_ARGUMENT. */
+  float swiglu_alpha;
+  float swiglu_beta;
+  float swiglu_limit;
 } b4_moe_config;
 
 /* Token capacity the packing and workspace are sized to: next_pow2(max(m, 1))
@@ -166,7 +181,8 @@ b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32
  * gs13          [E_l] fp32 global scales of FC1 (NVFP4); must be NULL for MXFP4.
  * w2, s2, gs2   the same for FC2 (which = 1).
  * topk_ids      [m, top_k] int32; topk_weights [m, top_k] fp32.
- * activation    b4_activation (must match the one the weights were prepared for).
+ * activation    b4_activation (of the layout the weights were prepared for:
+ *               SILU_SWIGLU and SWIGLU_OAI share one).
  * out           [m, H] bf16, written in full (tokens without a valid route get 0).
  * workspace     >= b4_workspace_bytes(cfg, activation) bytes, 256-byte aligned;
  *               its contents on entry do not matter.  It holds the status word

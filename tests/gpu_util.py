@@ -87,7 +87,7 @@ def host_layer(wl: W.Workload, m: int, seed: int, weights: str = "quantized") ->
 
 def oracle_out(hl: HostLayer, tokens=None):
     return M.fused_moe(hl.x, hl.c13, hl.s13, hl.g13, hl.c2, hl.s2, hl.g2, hl.ids, hl.wts, hl.wl.act, hl.wl.fmt,
-                       hl.wl.num_global_experts, expert_map=hl.em, tokens=tokens)
+                       hl.wl.num_global_experts, expert_map=hl.em, tokens=tokens, swiglu=hl.wl.swiglu)
 
 
 class DeviceLayer:
@@ -104,7 +104,8 @@ class DeviceLayer:
         self.cfg = b4.MoEConfig(
             m=hl.m, top_k=wl.top_k, num_global_experts=wl.num_global_experts,
             num_local_experts=wl.num_local_experts, hidden=wl.hidden, inter=wl.inter,
-            format=b4.FORMATS[wl.fmt], path=b4.PATH_AUTO if path is None else path, expert_map=self.em)
+            format=b4.FORMATS[wl.fmt], path=b4.PATH_AUTO if path is None else path, expert_map=self.em,
+            swiglu_alpha=wl.swiglu[0], swiglu_beta=wl.swiglu[1], swiglu_limit=wl.swiglu[2])
         self.x = dev(hl.x_bits).view(torch.bfloat16)
         self.ids = dev(hl.ids)
         self.wts = dev(hl.wts)

@@ -80,7 +80,16 @@ def test_config_struct_layout_matches_header(b4):
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"(\w+)\s*;", body)
     assert [f[0] for f in b4._Config._fields_] == fields
-    assert ctypes.sizeof(b4._Config) == 8 * 4 + 8
+    # eight int32, the expert_map pointer, three floats, tail padding to 8 bytes
+    assert b4._Config.swiglu_alpha.offset == 40 and b4._Config.swiglu_limit.offset == 48
+    assert ctypes.sizeof(b4._Config) == 8 * 4 + 8 + 3 * 4 + 4
+
+
+def test_activation_enum_matches_header(b4):
+    text = open(HEADER).read()
+    body = re.search(r"typedef enum b4_activation \{(.*?)\} b4_activation;", text, re.S).group(1)
+    values = {k: int(v) for k, v in re.findall(r"B4_ACT_(\w+)\s*=\s*(\d+)", body)}
+    assert values == {"SILU_SWIGLU": b4.SILU, "RELU2": b4.RELU2, "SWIGLU_OAI": b4.SWIGLU_OAI}
 
 
 def _cfg(b4, **kw):
@@ -95,6 +104,30 @@ def test_capacity_and_workspace_sizes_are_power_of_two_stable(b4):
     assert sizes[33] == sizes[40] == sizes[64] < sizes[65] == sizes[128]
     for m in range(0, 300, 7):
         assert b4.workspace_bytes(_cfg(b4, m=m), b4.SILU) <= b4.workspace_bytes(_cfg(b4, m=m + 7), b4.SILU)
+
+
+def test_clamped_swiglu_shares_the_gated_layout(b4):
+    for m in (1, 16, 300):
+        assert b4.workspace_bytes(_cfg(b4, m=m), b4.SWIGLU_OAI) == b4.workspace_bytes(_cfg(b4, m=m), b4.SILU)
+    for which in (0, 1):
+        assert b4.prepared_sizes(_cfg(b4), which, b4.SWIGLU_OAI) == b4.prepared_sizes(_cfg(b4), which, b4.SILU)
+    assert b4.prepared_sizes(_cfg(b4), 0, b4.SWIGLU_OAI) != b4.prepared_sizes(_cfg(b4), 0, b4.RELU2)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(swiglu_limit=0.0), dict(swiglu_limit=-7.0), dict(swiglu_limit=float("nan")),
+    dict(swiglu_alpha=float("inf")), dict(swiglu_alpha=float("nan")), dict(swiglu_beta=float("-inf")),
+])
+def test_clamped_swiglu_parameters_are_checked(b4, kw):
+    """Checked before anything else happens, so m = 0 (no pointers, no device) reaches the check."""
+    lib = b4.raw_lib()
+    bad = _cfg(b4, m=0, **kw)._c()
+    st = lib.b4_fused_moe(ctypes.byref(bad), *([None] * 9), b4.SWIGLU_OAI, None, None, 0, None)
+    assert st == b4.B4_ERR_INVALID_ARGUMENT and "swiglu" in b4.last_error()
+    # the other activations ignore the three fields
+    assert lib.b4_fused_moe(ctypes.byref(bad), *([None] * 9), b4.SILU, None, None, 0, None) == b4.B4_OK
+    good = _cfg(b4, m=0, swiglu_limit=float("inf"))._c()
+    assert lib.b4_fused_moe(ctypes.byref(good), *([None] * 9), b4.SWIGLU_OAI, None, None, 0, None) == b4.B4_OK
 
 
 def test_prepared_sizes(b4):

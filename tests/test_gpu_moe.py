@@ -10,6 +10,8 @@ and sum|gpu - oracle| / sum|oracle| <= 5e-3, per call.
   on 64 chosen tokens above (the most and least loaded experts, both sides of
   every route-chunk boundary); the MXFP4 shape at full size with the small-m
   path forced;
+* the clamped swiglu on every kernel, with a limit the FC1 outputs cross,
+  and at full size on the MXFP4 shape with the gpt-oss parameters;
 * tokens that select one expert in several top-k slots, on every path;
 * edge cases: m = 0, every route dropped, top-1 single expert, repeated
   calls with one workspace (capacity reuse), a workspace one byte short.
@@ -78,9 +80,35 @@ def test_parity_scaled(b4, name, act, m, path):
     assert_parity(got, ref, f"{name}/{act}/m={m}/{path}")
 
 
+# the clamped swiglu (swiglu-oai) on every kernel's gated epilogue: the
+# per-route small-m kernel with one-route units (decode_s m=1) and grouped
+# units (decode_s m=4, decode_w m=24), the route-grouped small-m kernel
+# (small_s m=16), the weights-on-N GEMMs (prefill_s m=37, mxfp4_s m=9 on the
+# grouped path) and the weights-on-M GEMMs (tiny m=512, mxfp4_s m=300).  The
+# limit is one the FC1 outputs of these sizes cross (their spread is about
+# 0.02 sqrt(H) = 0.3 .. 0.45), so both clamps act.
+OAI_PARAMS = (1.702, 1.0, 0.4)
+OAI_CASES = [("decode_s", 1), ("decode_s", 4), ("decode_w", 24), ("small_s", 16), ("prefill_s", 37),
+             ("tiny", 512), ("mxfp4_s", 9), ("mxfp4_s", 300)]
+
+
+@pytest.mark.parametrize("name,m", OAI_CASES, ids=[f"{n}-m{m}" for n, m in OAI_CASES])
+@pytest.mark.parametrize("path", ["auto", "decode", "grouped"])
+def test_parity_clamped_swiglu(b4, name, m, path):
+    if path == "decode" and m > b4.DECODE_MAX_M:
+        pytest.skip("decode path caps m")
+    wl = SCALED[name].with_act("swiglu_oai", OAI_PARAMS)
+    hl = host_layer(wl, m, seed=zlib.crc32(f"oai/{name}/{m}".encode()) % 1000)
+    dl = DeviceLayer(hl, path={"auto": b4.PATH_AUTO, "decode": b4.PATH_DECODE, "grouped": b4.PATH_GROUPED}[path])
+    dl.run()
+    assert_parity(dl.result(), oracle_out(hl), f"swiglu_oai {name}/m={m}/{path}")
+
+
 FULL = [("tiny", "silu", 4), ("decode", "relu2", 1), ("decode", "relu2", 2), ("decode", "relu2", 4),
         ("small", "silu", 16), ("small", "silu", 64), ("prefill", "silu", 2048), ("prefill", "relu2", 2048),
-        ("mxfp4", "silu", 512)]
+        ("mxfp4", "silu", 512),
+        # the gpt-oss-like MXFP4 shape with the gpt-oss clamped swiglu (1.702, 1, 7)
+        ("mxfp4", "swiglu_oai", 512)]
 
 
 def pick_tokens(hl, n=64, seed=11):
@@ -131,7 +159,7 @@ def test_parity_full_size_sampled(b4, name, act, m):
 
 
 FORCED = [("mxfp4", "silu", 4), ("mxfp4", "relu2", 4), ("mxfp4", "silu", 24), ("decode", "silu", 8),
-          ("decode", "relu2", 16), ("mxfp4", "silu", 12)]
+          ("decode", "relu2", 16), ("mxfp4", "silu", 12), ("mxfp4", "swiglu_oai", 12)]
 
 
 @pytest.mark.parametrize("name,act,m", FORCED, ids=[f"{n}-{a}-m{m}" for n, a, m in FORCED])

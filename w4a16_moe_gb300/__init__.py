@@ -32,13 +32,16 @@ NVFP4 = 0
 MXFP4 = 1
 SILU = 0
 RELU2 = 1
+SWIGLU_OAI = 2
 PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_GROUPED = 2
 DECODE_MAX_M = 64
 NOALLOC_SCRATCH_BYTES = 64 << 20
 FORMATS = {"nvfp4_e4m3_k16": NVFP4, "mxfp4_e8m0_k32": MXFP4}
-ACTIVATIONS = {"silu": SILU, "relu2": RELU2}
+ACTIVATIONS = {"silu": SILU, "relu2": RELU2, "swiglu_oai": SWIGLU_OAI}
+# the gpt-oss models' clamped-swiglu parameters (alpha, beta, limit)
+SWIGLU_OAI_DEFAULTS = (1.702, 1.0, 7.0)
 
 
 class B4Error(RuntimeError):
@@ -58,6 +61,9 @@ class _Config(ctypes.Structure):
         ("format", ctypes.c_int32),
         ("path", ctypes.c_int32),
         ("expert_map", ctypes.c_void_p),
+        ("swiglu_alpha", ctypes.c_float),
+        ("swiglu_beta", ctypes.c_float),
+        ("swiglu_limit", ctypes.c_float),
     ]
 
 
@@ -142,6 +148,10 @@ class MoEConfig:
     format: int = NVFP4
     path: int = PATH_AUTO
     expert_map: torch.Tensor | None = None  # int32 CUDA tensor [E_g] or None
+    # read for the SWIGLU_OAI activation only
+    swiglu_alpha: float = SWIGLU_OAI_DEFAULTS[0]
+    swiglu_beta: float = SWIGLU_OAI_DEFAULTS[1]
+    swiglu_limit: float = SWIGLU_OAI_DEFAULTS[2]
 
     def _c(self) -> _Config:
         em = 0
@@ -149,7 +159,8 @@ class MoEConfig:
             _need(self.expert_map, torch.int32, "expert_map")
             em = self.expert_map.data_ptr()
         return _Config(self.m, self.top_k, self.num_global_experts, self.num_local_experts,
-                       self.hidden, self.inter, self.format, self.path, em)
+                       self.hidden, self.inter, self.format, self.path, em,
+                       self.swiglu_alpha, self.swiglu_beta, self.swiglu_limit)
 
 
 def _need(t, dtype, name):

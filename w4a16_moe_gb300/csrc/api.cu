@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -107,6 +108,26 @@ int32_t next_pow2(int64_t n) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The kernels' FC1 activation of a b4_activation: 0 gated (SwiGLU and the
+// clamped swiglu share the W13 layout and the kernels' gated epilogue), 1
+// ReLU^2.
+int kernel_act(int32_t activation) { return activation == B4_ACT_RELU2 ? 1 : 0; }
+
+// Parameters of the gated epilogue: plain SwiGLU is alpha 1, beta 0, no clamp;
+// the clamped swiglu takes the config's three values, checked here.
+b4_status glu_params(const b4_moe_config* cfg, int32_t activation, GluParams* g) {
+  if (activation != B4_ACT_SWIGLU_OAI) {
+    *g = GluParams{1.0f, 0.0f, INFINITY};
+    return B4_OK;
+  }
+  if (!std::isfinite(cfg->swiglu_alpha) || !std::isfinite(cfg->swiglu_beta) || !(cfg->swiglu_limit > 0.0f))
+    return fail(B4_ERR_INVALID_ARGUMENT,
+                "swiglu_alpha = %g and swiglu_beta = %g must be finite and swiglu_limit = %g positive",
+                (double)cfg->swiglu_alpha, (double)cfg->swiglu_beta, (double)cfg->swiglu_limit);
+  *g = GluParams{cfg->swiglu_alpha, cfg->swiglu_beta, cfg->swiglu_limit};
+  return B4_OK;
+}
+
 // ------------------------------------------------------------ validation
 b4_status check_config(const b4_moe_config* cfg, int32_t act) {
   if (!cfg) return fail(B4_ERR_INVALID_ARGUMENT, "cfg is NULL");
@@ -124,7 +145,7 @@ b4_status check_config(const b4_moe_config* cfg, int32_t act) {
     return fail(B4_ERR_INVALID_ARGUMENT, "format = %d unknown", cfg->format);
   if (cfg->path < B4_PATH_AUTO || cfg->path > B4_PATH_GROUPED)
     return fail(B4_ERR_INVALID_ARGUMENT, "path = %d unknown", cfg->path);
-  if (act != B4_ACT_SILU_SWIGLU && act != B4_ACT_RELU2)
+  if (act != B4_ACT_SILU_SWIGLU && act != B4_ACT_RELU2 && act != B4_ACT_SWIGLU_OAI)
     return fail(B4_ERR_INVALID_ARGUMENT, "activation = %d unknown", act);
   const int g = cfg->format == B4_NVFP4_E4M3_K16 ? 16 : 32;
   if (cfg->hidden < g || cfg->hidden % g || cfg->hidden > (1 << 16))
@@ -161,7 +182,7 @@ WsLayout ws_layout(const b4_moe_config* cfg, int32_t act) {
   L.r_cap = L.t_cap * cfg->top_k;
   L.max_chunks = L.r_cap / kChunkRowsN + cfg->num_local_experts + 1;  // the smaller chunk size
   L.inter_pad = round_up(cfg->inter, kBK);
-  L.wnat = fc1_natural_width(act == B4_ACT_SILU_SWIGLU ? 0 : 1, L.inter_pad);
+  L.wnat = fc1_natural_width(kernel_act(act), L.inter_pad);
   L.decode_ok = L.t_cap <= B4_DECODE_MAX_M;
   L.dec_tcap = L.t_cap < B4_DECODE_MAX_M ? L.t_cap : B4_DECODE_MAX_M;
   L.dec_rcap = L.dec_tcap * cfg->top_k;
@@ -350,7 +371,7 @@ b4_status b4_prepared_sizes(const b4_moe_config* cfg, int32_t which, int32_t act
   if (st != B4_OK) return st;
   if (which != 0 && which != 1) return fail(B4_ERR_INVALID_ARGUMENT, "which = %d must be 0 (W13) or 1 (W2)", which);
   if (!code_bytes || !scale_bytes) return fail(B4_ERR_INVALID_ARGUMENT, "null output pointer");
-  const TensorGeom g = tensor_geom(which, activation, cfg->hidden, cfg->inter);
+  const TensorGeom g = tensor_geom(which, kernel_act(activation), cfg->hidden, cfg->inter);
   const size_t stages = (size_t)cfg->num_local_experts * g.n_tiles * g.k_stages;
   *code_bytes = stages * kCodeBytesPerStage;
   *scale_bytes = stages * scale_bytes_per_stage(cfg->format);
@@ -382,7 +403,7 @@ b4_status b4_prepare_weights(const b4_moe_config* cfg, int32_t which, int32_t ac
   p.dst_scales = dst_scales;
   p.num_experts = cfg->num_local_experts;
   p.which = which;
-  p.act = activation;
+  p.act = kernel_act(activation);
   p.fmt = cfg->format;
   p.hidden = cfg->hidden;
   p.inter = cfg->inter;
@@ -427,6 +448,8 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
                        void* workspace, size_t workspace_bytes, b4_stream_t stream) {
   b4_status st = check_config(cfg, activation);
   if (st != B4_OK) return st;
+  GluParams glu;
+  if ((st = glu_params(cfg, activation, &glu)) != B4_OK) return st;
   if (cfg->m == 0) return B4_OK;  // nothing to compute, nothing launched
   if (!x || !w13 || !s13 || !w2 || !s2 || !topk_ids || !topk_weights || !out || !workspace)
     return fail(B4_ERR_INVALID_ARGUMENT, "null pointer argument");
@@ -445,7 +468,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   DevInfo dev;
   if ((st = device_info(dev)) != B4_OK) return st;
 
-  const int act = activation == B4_ACT_SILU_SWIGLU ? 0 : 1;
+  const int act = kernel_act(activation);
   const int fmt = cfg->format;
   // AUTO: the small-m path up to m = 16, and up to B4_DECODE_MAX_M while an
   // expert receives at most two routes on average (decode E128 k8 m = 32:
@@ -471,6 +494,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   base.inter = cfg->inter;
   base.inter_pad = L.inter_pad;
   base.act = act;
+  base.glu = glu;
   base.topk_ids = topk_ids;
   base.topk_weights = topk_weights;
   base.expert_map = cfg->expert_map;
@@ -533,6 +557,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     dp.hidden = cfg->hidden;
     dp.inter_pad = L.inter_pad;
     dp.act = act;
+    dp.glu = glu;
     dp.topk_ids = topk_ids;
     dp.topk_weights = topk_weights;
     dp.expert_map = cfg->expert_map;
@@ -584,6 +609,7 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     dp.hidden = cfg->hidden;
     dp.inter_pad = L.inter_pad;
     dp.act = act;
+    dp.glu = glu;
     dp.topk_ids = topk_ids;
     dp.topk_weights = topk_weights;
     dp.expert_map = cfg->expert_map;

@@ -304,8 +304,6 @@ __device__ inline Phase make_phase(unsigned long long cost_total, int NT, int KS
   return ph;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
-
 // Timeline stamp (b4_set_trace): kinds 0 start, 1 group table built, 2 first
 // descriptor published, 3 first weight copy issued, 4 first slot computed,
 // 5 last FC1 unit stored, 6 first FC2 slot computed, 7 compute done,
@@ -404,7 +402,7 @@ __device__ __forceinline__ bool build_tile(const SmallGroupParams& p, const GDes
       if (p.act == 2) {
         p.out[(size_t)rr[b] * p.n_out + row[b]] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
       } else {
-        const float hv = p.act == 0 ? silu_f(a) * sum_first<S>(vb[b], u.npieces) : (a > 0.f ? a * a : 0.f);
+        const float hv = p.act == 0 ? gated_act(a, sum_first<S>(vb[b], u.npieces), p.glu) : (a > 0.f ? a * a : 0.f);
         p.h[(size_t)rr[b] * p.inter_pad + row[b]] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
       }
     }

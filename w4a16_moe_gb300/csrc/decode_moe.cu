@@ -557,7 +557,7 @@ __device__ __forceinline__ bool build_h_f16(const DecodeParams& p, const DGroups
         if (f + q * kDComputeWarps >= items) break;
         float h[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) h[c] = gu[2 * q][c] / (1.0f + __expf(-gu[2 * q][c])) * gu[2 * q + 1][c];
+        for (int c = 0; c < 4; ++c) h[c] = gated_act(gu[2 * q][c], gu[2 * q + 1][c], p.glu);
         store(f + q * kDComputeWarps, vv[2 * q], h);
       }
     }

@@ -50,6 +50,25 @@ __host__ __device__ inline TensorGeom tensor_geom(int which, int act, int hidden
   return g;
 }
 
+// Parameters of the gated FC1 activation (act 0):
+//   h = g' * sigmoid(alpha * g') * (u' + beta),
+//   g' = min(g, limit), u' = u clamped to [-limit, limit]
+// for the gate g and up u of one intermediate column.  Plain SwiGLU is
+// alpha = 1, beta = 0, limit = +inf (g' = g, u' = u, g sigmoid(g) = silu(g));
+// the clamped swiglu of the gpt-oss models is alpha 1.702, beta 1, limit 7.
+struct GluParams {
+  float alpha, beta, limit;
+};
+
+#ifdef __CUDACC__
+// The comparisons (not fminf/fmaxf) keep a NaN input a NaN.
+__device__ __forceinline__ float gated_act(float g, float u, const GluParams& a) {
+  const float gc = g > a.limit ? a.limit : g;
+  const float uc = u > a.limit ? a.limit : (u < -a.limit ? -a.limit : u);
+  return gc / (1.0f + __expf(-a.alpha * gc)) * (uc + a.beta);
+}
+#endif
+
 enum GemmMode : int { kFc1Grouped = 0, kFc2Grouped = 1 };
 
 struct GemmParams {
@@ -63,7 +82,8 @@ struct GemmParams {
   int n_tiles, k_stages;
   // layer shape
   int m, top_k, num_global_experts, num_local_experts, hidden, inter, inter_pad;
-  int act;              // 0 SwiGLU, 1 ReLU^2, 2 none (dense linear: h = the scaled accumulator)
+  int act;              // 0 gated (SwiGLU family), 1 ReLU^2, 2 none (dense linear: h = the scaled accumulator)
+  GluParams glu;        // act 0
   // routing inputs
   const int32_t* topk_ids;
   const float* topk_weights;  // or null (FC2: router weight 1, the dense linear layer)
@@ -115,7 +135,8 @@ struct DecodeParams {
   const float* gs2;
   int n_tiles1, k_stages1, n_tiles2, k_stages2;
   int m, top_k, num_global_experts, num_local_experts, hidden, inter_pad;
-  int act;                   // 0 SwiGLU, 1 ReLU^2
+  int act;                   // 0 gated (SwiGLU family), 1 ReLU^2
+  GluParams glu;             // act 0
   // Dense linear layer (E = 1, top-1, no activation, no FC2): the FC2 units
   // become output units (route, 128-column tile of N) that sum the FC1 split
   // partials into out [m, n_out] bf16; topk_ids, topk_weights, w2 and q are
@@ -149,7 +170,8 @@ struct SmallGroupParams {
   int n_tiles1, k_stages1;
   int n_tiles2, k_stages2;   // n_tiles2 = 0: no FC2 phase (the dense linear layer)
   int m, top_k, num_global_experts, num_local_experts, hidden, inter_pad;
-  int act;                   // 0 SwiGLU, 1 ReLU^2, 2 none (the dense linear layer: FC1 writes out)
+  int act;                   // 0 gated (SwiGLU family), 1 ReLU^2, 2 none (the dense linear layer: FC1 writes out)
+  GluParams glu;             // act 0
   int n_out;                 // the dense linear layer's N (out is [m, n_out])
   const int32_t* topk_ids;   // [m, top_k], or null: every route goes to local expert 0
   const float* topk_weights;

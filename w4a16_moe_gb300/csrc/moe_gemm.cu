@@ -151,7 +151,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // ------------------------------------------------------------------ kernel
 template <int MODE, int FMT>
@@ -435,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               const float g = is_up ? other[j] : mine[j];
               const float upv = is_up ? mine[j] : other[j];
               if (col < U.rows && i < p.inter_pad)
-                p.h_out[(size_t)(U.slot0 + col) * p.inter_pad + i] = float_to_bf16_bits(silu_f(g) * upv);
+                p.h_out[(size_t)(U.slot0 + col) * p.inter_pad + i] = float_to_bf16_bits(gated_act(g, upv, p.glu));
             }
           } else {
             const int i = U.tile * kTileRows + er;

@@ -148,7 +148,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // ------------------------------------------------------------------ kernel
 template <int MODE, int FMT>
@@ -428,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 for (int j = 0; j < 8; ++j) {
                   const float a0 = __uint_as_float(g[2 * j]) * gsv, a1 = __uint_as_float(g[2 * j + 1]) * gsv;
                   const float b0 = __uint_as_float(v[2 * j]) * gsv, b1 = __uint_as_float(v[2 * j + 1]) * gsv;
-                  o[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
+                  o[j] = pack_bf16x2(gated_act(a0, b0, p.glu), gated_act(a1, b1, p.glu));
                 }
                 uint4* dst = reinterpret_cast<uint4*>(p.h_out + (size_t)(U.slot0 + er) * p.inter_pad + i0);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
