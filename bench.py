@@ -452,10 +452,10 @@ KERNEL_SOURCES = {
     "grouped_wn": ["moe_gemm_wn.cu", "dequant.cuh", "tma.cuh", "ptx.cuh", "kernels.cuh"],
 }
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
-    ("decode", "decode:relu2", 1): ("b4230ce056e0381b", 56_735_232 + 325_632),
-    ("decode", "small:silu", 16): ("b4230ce056e0381b", 171_003_904 + 4_829_952),
-    ("grouped", "prefill:silu", 2048): ("b1b97e535c66c3b7", 1_040_458_496 + 80_837_120 + 599_910_400 + 81_796_352),
-    ("grouped_wn", "small:silu", 64): ("4085c3218d6bdfc4", 180_107_520 + 4_110_592 + 90_864_384 + 101_888),
+    ("decode", "decode:relu2", 1): ("f4762e7f1cc4ce5b", 56_734_720 + 302_080),
+    ("decode", "small:silu", 16): ("f4762e7f1cc4ce5b", 170_955_008 + 4_806_400),
+    ("grouped", "prefill:silu", 2048): ("f156d9e9c63c483d", 1_040_376_320 + 80_981_504 + 600_303_360 + 82_526_464),
+    ("grouped_wn", "small:silu", 64): ("f67e0adcb567f92f", 180_109_312 + 4_455_168 + 90_866_432 + 75_008),
 }
 
 

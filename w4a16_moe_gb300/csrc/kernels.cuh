@@ -61,11 +61,16 @@ struct GluParams {
 };
 
 #ifdef __CUDACC__
-// The comparisons (not fminf/fmaxf) keep a NaN input a NaN.
+// The comparisons (not fminf/fmaxf) keep a NaN input a NaN.  The sigmoid's
+// division is the approximate one (__fdividef, 2 ulp; 0 once 1 + e^-x passes
+// 2^126, where the exact quotient is below 2^-126 |g'| anyway): h is rounded
+// to bf16 next, and the pages' kernels take the same trade (flashinfer PR
+// #4255, review comments on moe_w4a16_fp4_helpers.py: silu_mul_32 forms the
+// sigmoid with an approximate reciprocal).
 __device__ __forceinline__ float gated_act(float g, float u, const GluParams& a) {
   const float gc = g > a.limit ? a.limit : g;
   const float uc = u > a.limit ? a.limit : (u < -a.limit ? -a.limit : u);
-  return gc / (1.0f + __expf(-a.alpha * gc)) * (uc + a.beta);
+  return __fdividef(gc, 1.0f + __expf(-a.alpha * gc)) * (uc + a.beta);
 }
 #endif
 
