@@ -454,7 +454,7 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {  # (kernel family, workload, m): (source hash, DRAM read + write bytes per call of the GEMM kernel(s))
     ("decode", "decode:relu2", 1): ("f4762e7f1cc4ce5b", 56_734_720 + 302_080),
     ("decode", "small:silu", 16): ("f4762e7f1cc4ce5b", 170_955_008 + 4_806_400),
-    ("grouped", "prefill:silu", 2048): ("f156d9e9c63c483d", 1_040_376_320 + 80_981_504 + 600_303_360 + 82_526_464),
+    ("grouped", "prefill:silu", 2048): ("8f4474bd57eddfdb", 1_040_493_056 + 81_164_032 + 600_330_496 + 81_992_704),
     ("grouped_wn", "small:silu", 64): ("f67e0adcb567f92f", 180_109_312 + 4_455_168 + 90_866_432 + 75_008),
 }
 

@@ -476,37 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// --------------------------------------------------------- permute x rows
-// xp[slot] = x[token of the route at packed slot], for the valid slots: the
-// FC1 B operand becomes contiguous per expert chunk.  One warp per row, 16-byte
-// copies; slots past the valid count are left untouched (never loaded).
-__global__ void permute_x_kernel(const __grid_constant__ GemmParams p) {
-  pdl_wait();  // sorted routes come from the route-pack kernel
-  pdl_launch_dependents();
-  const int valid = *p.valid_count;
-  const int chunks = p.hidden / 8;  // 16-byte pieces of a row
-  const int wpb = blockDim.x / 32;
-  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < valid; r += gridDim.x * wpb) {
-    const int tok = __ldg(p.sorted_routes + r) / p.top_k;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.hidden);
-    uint4* dst = reinterpret_cast<uint4*>(p.xp + (size_t)r * p.hidden);
-    for (int c = threadIdx.x & 31; c < chunks; c += 32) dst[c] = __ldg(src + c);
-  }
-}
-
-cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(4 * num_sms);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, permute_x_kernel, p);
-}
-
 // ----------------------------------------------------- host-side launchers
 template <int MODE, int FMT>
 cudaError_t launch_gemm(const GemmParams& p, int grid, bool pdl, cudaStream_t stream) {

@@ -30,12 +30,38 @@ constexpr int kPackThreads = 512;
 constexpr int kPackWarps = kPackThreads / 32;
 constexpr int kBatch = 8;  // 32-route groups whose keys a warp loads before using any
 
-__device__ __forceinline__ int pack_local_expert(const RoutePackParams& p, int r) {
-  if (!p.topk_ids) return 0;
-  const int id = __ldg(p.topk_ids + r);
-  if (id < 0 || id >= p.num_global_experts) return -1;
-  const int l = p.expert_map ? __ldg(p.expert_map + id) : id;
-  return (l >= 0 && l < p.num_local_experts) ? l : -1;
+// Local experts of the routes b0 + 32 i + lane (i < kBatch; -1 past `end` or
+// invalid).  The id loads, then the expert_map loads, are issued as one batch
+// each at clamped addresses, with the range checks applied afterwards: a
+// per-route branch around each load keeps the loads from overlapping (the
+// kernel then waits one L2 round trip per 32 routes).
+__device__ __forceinline__ void load_keys(const RoutePackParams& p, int b0, int end, int lane, int (&keys)[kBatch]) {
+  if (!p.topk_ids) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) keys[i] = b0 + 32 * i + lane < end ? 0 : -1;
+    return;
+  }
+  int id[kBatch];
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) {
+    const int r = b0 + 32 * i + lane;
+    id[i] = __ldg(p.topk_ids + (r < end ? r : b0));  // b0 < end: a valid address
+  }
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) {
+    const bool ok = b0 + 32 * i + lane < end && id[i] >= 0 && id[i] < p.num_global_experts;
+    id[i] = ok ? id[i] : -1;
+  }
+  if (p.expert_map) {
+    int l[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) l[i] = __ldg(p.expert_map + (id[i] >= 0 ? id[i] : 0));
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) keys[i] = id[i] >= 0 && l[i] >= 0 && l[i] < p.num_local_experts ? l[i] : -1;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) keys[i] = id[i] >= 0 && id[i] < p.num_local_experts ? id[i] : -1;
+  }
 }
 
 // In-place exclusive scan of s[0..n) (n <= 2 * kPackThreads) by the block;
@@ -91,11 +117,7 @@ __global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_c
   int* my_hist = s_whist + warp * E;
   for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
     int keys[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int r = b0 + 32 * i + lane;
-      keys[i] = r < end ? pack_local_expert(p, r) : -1;
-    }
+    load_keys(p, b0, end, lane, keys);
 #pragma unroll
     for (int i = 0; i < kBatch; ++i)
       if (keys[i] >= 0) atomicAdd(&my_hist[keys[i]], 1);
@@ -152,11 +174,7 @@ __global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_c
     int pos = s_cnt[e] + my_hist[e];
     for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
       int keys[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int r = b0 + 32 * i + lane;
-        keys[i] = r < end ? pack_local_expert(p, r) : -1;
-      }
+      load_keys(p, b0, end, lane, keys);
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         const bool hit = keys[i] == e;
