@@ -233,8 +233,8 @@ class Bench:
         # to m = 64 while there are at most two routes per local expert
         self.decode = self.path == b4.PATH_DECODE or (self.path == b4.PATH_AUTO and (
             m <= 16 or (m <= 64 and m * wl.top_k <= 2 * wl.num_local_experts)))
-        self.n_kernels = 1 if self.decode else 4  # timed intervals: decode kernel; pack, permute + FC1, FC2, finalize
-        self.launches = 1 if self.decode else 5  # this library's kernels per call
+        self.n_kernels = 1 if self.decode else 4  # timed intervals: decode kernel; pack (+ x copy), FC1, FC2, finalize
+        self.launches = 1 if self.decode else 4  # this library's kernels per call
 
     def flush_l2(self):
         """Evict L2: write a 512 MiB buffer (evicts everything) and read it back,

@@ -191,9 +191,10 @@ b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32
  * rounds h to bf16; FC2 accumulates in fp32, multiplies by gs2 and the router
  * weight and sums the routes of a token in fp32 before one bf16 rounding.
  * Enqueues 1 (the small-m path: one cooperative launch of one CTA per SM
- * for m > 4, grid no larger than the resident CTA count for m <= 4) or 5
- * (grouped: route pack, x permutation, FC1, FC2, finalize, chained by
- * programmatic dependent launch) launches on `stream`; no allocation, no
+ * for m > 4, grid no larger than the resident CTA count for m <= 4) or 4
+ * (grouped: route pack with the copy of x rows into packed-route order, FC1,
+ * FC2, finalize; the last three chained by programmatic dependent launch)
+ * launches on `stream`; no allocation, no
  * synchronisation.  The small-m path's output is bitwise reproducible (every
  * sum in a fixed order); the grouped path's top-k sum uses fp32 atomics. */
 b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_t* w13, const uint8_t* s13,
@@ -206,9 +207,8 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
  * b4_fused_moe call on this thread records events[0] on its stream before its
  * first kernel and events[i+1] after kernel i, as far as n reaches: the
  * decode path launches 1 kernel (FC1, FC2 and the top-k combine fused); the
- * grouped path records 5 (before route pack, after it, after the x
- * permutation and FC1, after FC2, after finalize), so 2 and 5 events cover
- * them.  b4_linear records 2 (small m), 4 (K-split GEMM: before the memset,
+ * grouped path records 5 (before route pack, after it, after FC1, after
+ * FC2, after finalize), so 2 and 5 events cover them.  b4_linear records 2 (small m), 4 (K-split GEMM: before the memset,
  * after the route pack, after the GEMM, after the rounding pass) or 3.  An event recorded between two kernels removes their programmatic
  * overlap, so timed calls can be slightly slower than untimed ones; use this
  * for measurement.

@@ -28,8 +28,9 @@ cudaError_t decode_occupancy(int fmt, bool grouped, int* blocks_per_sm);
 cudaError_t launch_decode_grouped(const SmallGroupParams& p, int fmt, int sets, int grid, cudaStream_t stream);
 cudaError_t decode_grouped_occupancy(int fmt, int sets, size_t smem, int* blocks_per_sm);
 size_t decode_grouped_smem(int fmt, int sets, int routes);
-cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream);
-cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream);
+// xp != null: the route pack also copies x rows into packed-route order
+cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream,
+                              const uint16_t* x = nullptr, uint16_t* xp = nullptr, int hidden = 0);
 size_t route_pack_smem_bytes(int num_local_experts);
 cudaError_t launch_prepare(const PrepareParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_self_test(uint32_t* status, unsigned long long limit_ns, cudaStream_t stream);
@@ -654,8 +655,9 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   const bool weights_on_n = (long long)cfg->m * cfg->top_k < 96LL * cfg->num_local_experts;
   rp.chunk_rows = weights_on_n ? kChunkRowsN : kChunkRowsM;
   rp.status = status;
+  uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);  // x rows in packed-route order, copied by the route pack
   if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
-  if ((e = launch_route_pack(rp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "route pack");
+  if ((e = launch_route_pack(rp, dev.sms, s, x, xp, cfg->hidden)) != cudaSuccess) return cuda_fail(e, "route pack");
   if ((e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
 
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.h);
@@ -665,7 +667,6 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
     pp->chunk_count = rp.chunk_count;
     pp->chunks = rp.chunks;
   }
-  uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);
   // B boxes: 32 rows for the weights-on-N kernel's operand stages, 80 for the
   // weights-on-M kernel (two per 160-row stage)
   if (!make_tmap_bf16_2d(&p1.tmap_b, xp, (uint64_t)L.r_cap, (uint64_t)cfg->hidden, weights_on_n ? 32 : 80))
@@ -679,10 +680,6 @@ b4_status b4_fused_moe(const b4_moe_config* cfg, const uint16_t* x, const uint8_
   p2.h = hbuf;
   p2.acc_out = acc;
   if (weights_on_n) p2.k_splits = -1;  // few units: split FC2's K (its epilogue adds fp32 partials)
-  GemmParams pp = p1;  // permute: x rows -> packed-route order
-  pp.xp = xp;
-  pp.valid_count = rp.offsets + cfg->num_local_experts;
-  if ((e = launch_permute_x(pp, dev.sms, s)) != cudaSuccess) return cuda_fail(e, "permute x");
   if ((e = launch_mode<kFc1Grouped>(fmt, weights_on_n, p1, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc1 grouped");
   if ((e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "timing event record");
   if ((e = launch_mode<kFc2Grouped>(fmt, weights_on_n, p2, dev.sms, true, s)) != cudaSuccess) return cuda_fail(e, "fc2 grouped");

@@ -104,8 +104,8 @@ struct GemmParams {
   int k_splits;
   // B operand sources
   const uint16_t* x;    // [m, H] bf16 (FC1)
-  uint16_t* xp;         // [R_cap, H] bf16: x rows in packed-route order (grouped FC1)
-  const int32_t* valid_count;  // number of valid routes (offsets[E_l] of the route pack)
+  uint16_t* xp;         // unused (the route pack copies x rows into packed-route order)
+  const int32_t* valid_count;  // unused
   const uint16_t* h;    // [R_cap, I_pad] bf16 (FC2 grouped)
   // outputs
   uint16_t* h_out;      // FC1 grouped

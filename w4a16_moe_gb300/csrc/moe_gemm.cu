@@ -6,7 +6,7 @@
 // epilogue"):
 //
 //   FC1  B = x rows of the routes of one expert chunk, copied into
-//        packed-route order by permute_x_kernel; the epilogue applies
+//        packed-route order by the route pack; the epilogue applies
 //        SiLU-SwiGLU or ReLU^2 (none for the dense linear layer, whose
 //        B rows are x itself) and stores bf16 h in the same order.
 //   FC2  B = h rows of the chunk; the epilogue multiplies by gs2 and the

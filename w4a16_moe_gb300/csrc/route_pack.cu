@@ -17,7 +17,13 @@
 // CTA 0 also writes counts, offsets, the grouped-GEMM chunk schedule (each
 // expert's routes cut into chunks of at most `chunk_rows`), the -1 tail of
 // the capacity and the cleared status word.  The ids are read a few times per
-// CTA; they stay in L2.
+// CTA; they stay in L2.  For the grouped path each CTA then copies the x rows
+// of its experts' routes into packed-route order (the FC1 B operand): it
+// knows those slots already, so no other launch or grid-wide wait is needed.
+// That launch has two CTAs per SM whatever the expert count: with fewer
+// experts than CTAs, Q = G / E replicas take each expert, every one of them
+// places the expert's routes (the same values into the same slots) and
+// copies every Q-th of its rows.
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -25,6 +31,14 @@
 namespace b4 {
 
 cudaError_t ensure_smem_limit(const void* func, size_t bytes);
+
+// Optional copy of x rows into packed-route order (the grouped FC1's B
+// operand): xp[slot] = x[token of the route at slot]; xp = null: none.
+struct PackCopy {
+  const uint16_t* x;
+  uint16_t* xp;
+  int hidden;
+};
 
 constexpr int kPackThreads = 512;
 constexpr int kPackWarps = kPackThreads / 32;
@@ -98,7 +112,11 @@ __device__ __forceinline__ int block_scan(int* s, int n, int* s_warp) {
   return total;
 }
 
-__global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_constant__ RoutePackParams p) {
+__global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_constant__ RoutePackParams p,
+                                                                 const __grid_constant__ PackCopy cp) {
+  // The grouped FC1 (launched with programmatic dependent launch) may start
+  // its set-up now; it waits for this grid to finish before it reads anything.
+  pdl_launch_dependents();
   extern __shared__ int s_mem[];
   const int E = p.num_local_experts;
   int* s_whist = s_mem;                   // [warps][E]: counts, then each warp's base within the expert
@@ -169,8 +187,17 @@ __global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_c
     for (int i = valid + threadIdx.x; i < p.route_cap; i += kPackThreads) p.sorted_routes[i] = -1;
   }
 
+  // this CTA's experts: b, b + G, ...; or, copying with fewer experts than
+  // CTAs, expert b % E as replica b / E of Q (CTAs from Q * E on take none)
+  int e0 = blockIdx.x, estep = gridDim.x, q = 0, Q = 1;
+  if (cp.xp && (int)gridDim.x > E) {
+    Q = (int)gridDim.x / E;
+    q = (int)blockIdx.x / E;
+    e0 = (int)blockIdx.x < Q * E ? (int)blockIdx.x % E : E;
+    estep = E;
+  }
   // the routes of this CTA's experts, in ascending flat index
-  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+  for (int e = e0; e < E; e += estep) {
     int pos = s_cnt[e] + my_hist[e];
     for (int b0 = beg; b0 < end; b0 += 32 * kBatch) {
       int keys[kBatch];
@@ -184,19 +211,46 @@ __global__ void __launch_bounds__(kPackThreads) route_pack_kernel(const __grid_c
       }
     }
   }
+  if (!cp.xp) return;
+
+  // xp[slot] = x[token of the route at slot] for this CTA's experts, one warp
+  // per row, four 16-byte loads in flight per lane before their stores.  The
+  // slots' routes were stored by this CTA: plain loads after the barrier.
+  constexpr int kLoads = 4;
+  __syncthreads();
+  const int chunks = cp.hidden / 8;  // 16-byte pieces of a row
+  for (int e = e0; e < E; e += estep) {
+    const int off = s_cnt[e], cnt = (e + 1 < E ? s_cnt[e + 1] : valid) - off;
+    for (int i = q * kPackWarps + warp; i < cnt; i += Q * kPackWarps) {
+      const int tok = p.sorted_routes[off + i] / p.top_k;
+      const uint4* src = reinterpret_cast<const uint4*>(cp.x + (size_t)tok * cp.hidden);
+      uint4* dst = reinterpret_cast<uint4*>(cp.xp + (size_t)(off + i) * cp.hidden);
+      for (int c = lane; c < chunks; c += 32 * kLoads) {
+        uint4 v[kLoads];
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k)
+          if (c + 32 * k < chunks) v[k] = __ldg(src + c + 32 * k);
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k)
+          if (c + 32 * k < chunks) dst[c + 32 * k] = v[k];
+      }
+    }
+  }
 }
 
 size_t route_pack_smem_bytes(int num_local_experts) {
   return (size_t)(kPackWarps + 3) * num_local_experts * sizeof(int);
 }
 
-cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_route_pack(const RoutePackParams& p, int num_sms, cudaStream_t stream, const uint16_t* x,
+                              uint16_t* xp, int hidden) {
   const size_t smem = route_pack_smem_bytes(p.num_local_experts);
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(route_pack_kernel), smem);
   if (e != cudaSuccess) return e;
-  int grid = p.num_local_experts < 2 * num_sms ? p.num_local_experts : 2 * num_sms;
+  // one CTA per expert up to two per SM; copying x rows, always two per SM
+  int grid = p.num_local_experts < 2 * num_sms && !xp ? p.num_local_experts : 2 * num_sms;
   if (grid < 1) grid = 1;
-  route_pack_kernel<<<grid, kPackThreads, smem, stream>>>(p);
+  route_pack_kernel<<<grid, kPackThreads, smem, stream>>>(p, PackCopy{x, xp, hidden});
   return cudaGetLastError();
 }
 

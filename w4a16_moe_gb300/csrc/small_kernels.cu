@@ -1,6 +1,6 @@
-// Small kernels of the grouped path of the fused W4A16 MoE layer: the copy of
-// x rows into packed-route order (the FC1 B operand) and the final conversion
-// of the fp32 top-k accumulator into the bf16 output.
+// Small kernels of the grouped path of the fused W4A16 MoE layer: the final
+// conversion of the fp32 top-k accumulator into the bf16 output (the copy of x
+// rows into packed-route order is part of the route pack, route_pack.cu).
 
 #include <cuda_bf16.h>
 
@@ -11,49 +11,6 @@ namespace b4 {
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-
-// --------------------------------------------------------- permute x rows
-// xp[slot] = x[token of the route at packed slot], for the valid slots: the
-// FC1 B operand becomes contiguous per expert chunk.  One warp per row, 16-byte
-// copies, four loads in flight per lane before their stores (a store to a
-// buffer that might alias the source keeps later loads behind it); slots past
-// the valid count are left untouched (never loaded).
-__global__ void permute_x_kernel(const __grid_constant__ GemmParams p) {
-  constexpr int kLoads = 4;
-  pdl_wait();  // sorted routes come from the route-pack kernel
-  pdl_launch_dependents();
-  const int valid = *p.valid_count;
-  const int chunks = p.hidden / 8;  // 16-byte pieces of a row
-  const int wpb = blockDim.x / 32;
-  const int lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < valid; r += gridDim.x * wpb) {
-    const int tok = __ldg(p.sorted_routes + r) / p.top_k;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.hidden);
-    uint4* dst = reinterpret_cast<uint4*>(p.xp + (size_t)r * p.hidden);
-    for (int c = lane; c < chunks; c += 32 * kLoads) {
-      uint4 v[kLoads];
-#pragma unroll
-      for (int k = 0; k < kLoads; ++k)
-        if (c + 32 * k < chunks) v[k] = __ldg(src + c + 32 * k);
-#pragma unroll
-      for (int k = 0; k < kLoads; ++k)
-        if (c + 32 * k < chunks) dst[c + 32 * k] = v[k];
-    }
-  }
-}
-
-cudaError_t launch_permute_x(const GemmParams& p, int num_sms, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(4 * num_sms);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, permute_x_kernel, p);
 }
 
 // ------------------------------------------------------------- finalize
