@@ -38,6 +38,9 @@ SCALED = {
     "mxfp4_s": W.WORKLOADS["mxfp4"].scaled(hidden=352, inter=160, experts=7),
     # many experts, few routes each: the small-m path's per-route kernel above m = 4
     "decode_w": W.WORKLOADS["decode"].scaled(hidden=256, inter=192, experts=128),
+    # more local experts than the route pack's 2 x 152 CTAs: CTAs that place and
+    # copy the rows of several experts each
+    "many_e": W.WORKLOADS["decode"].scaled(hidden=128, inter=64, experts=320),
 }
 CASES = [
     ("tiny", "silu", 4), ("tiny", "silu", 1),
@@ -56,6 +59,7 @@ CASES = [
     # path, on the per-route kernel's grouped units; m = 32 fills the group
     # table (256 routes, one thread each)
     ("decode_w", "relu2", 24), ("decode_w", "silu", 32),
+    ("many_e", "silu", 100),
 ]
 
 
