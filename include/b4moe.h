@@ -169,7 +169,10 @@ b4_status b4_prepare_weights(const b4_moe_config* cfg, int32_t which, int32_t ac
  *   sorted_routes [R_cap]   int32, R_cap = b4_route_capacity_tokens(m) * top_k:
  *                 sorted_routes[offsets[l] + i] = i-th valid route of expert l in
  *                 ascending r (stable); entries past offsets[E_l] are -1.
- * One launch on `stream`; no allocation, no synchronisation (capture-safe). */
+ * One launch on `stream`; no allocation, no synchronisation (capture-safe).
+ * The kernel lets a next kernel launched with programmatic dependent launch
+ * start early; such a kernel must wait for it (griddepcontrol.wait) before
+ * it reads the outputs. */
 b4_status b4_route_pack(const b4_moe_config* cfg, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
                         int32_t* sorted_routes, b4_stream_t stream);
 
