@@ -3,7 +3,7 @@
  *
  * The layer: 4-bit FP4 weights (NVFP4 or MXFP4), bf16 activations, route
  * packing, a grouped FC1 GEMM with in-kernel dequantisation and a fused
- * SiLU-SwiGLU or ReLU^2 epilogue, and a grouped FC2 GEMM whose store folds in
+ * SiLU-SwiGLU, clamped swiglu or ReLU^2 epilogue, and a grouped FC2 GEMM whose store folds in
  * the top-k weighted sum, plus a separate small-m decode path.  It is the
  * layer described by flashinfer PR #4255, "feat(moe): sync SM12x W4A16 fused
  * MoE family to b12x HEAD" (Description), restated for GB300.
