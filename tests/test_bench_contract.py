@@ -73,6 +73,25 @@ def test_traffic_hash_ignores_comments():
         assert len(bench.kernel_source_hash(fam)) == 16
 
 
+def test_traffic_table_families_follow_the_dispatch_rule():
+    """Each recorded ncu traffic figure is keyed by the kernel family that
+    serves its workload under AUTO (the small-m path up to m = 16, and up to
+    m = 64 while m * top_k <= 2 E_local; within it the per-route kernel for
+    m <= 4, m * top_k <= E_local, or <= 2 E_local and <= 256 routes; else the
+    grouped GEMMs, weights on N below 96 routes per local expert)."""
+    from types import SimpleNamespace
+
+    for (fam, key, m) in bench.NCU_TRAFFIC:
+        name, act = key.split(":")
+        wl = W.WORKLOADS[name].with_act(act)
+        r, e = m * wl.top_k, wl.num_local_experts
+        decode = m <= 16 or (m <= 64 and r <= 2 * e)
+        b = SimpleNamespace(decode=decode, wl=wl, m=m)
+        assert bench.kernel_family(b) == fam, (fam, key, m)
+        if not decode:
+            assert (fam == "grouped_wn") == (r < 96 * e)
+
+
 def _rank_main(rank, world, port, q):
     import torch.distributed as dist
 
