@@ -41,6 +41,8 @@ SCALED = {
     # more local experts than the route pack's 2 x 152 CTAs: CTAs that place and
     # copy the rows of several experts each
     "many_e": W.WORKLOADS["decode"].scaled(hidden=128, inter=64, experts=320),
+    # the largest top_k the layer takes (32 routes per token)
+    "topk32": W.WORKLOADS["decode"].scaled(hidden=128, inter=128, experts=64, top_k=32),
 }
 CASES = [
     ("tiny", "silu", 4), ("tiny", "silu", 1),
@@ -60,6 +62,9 @@ CASES = [
     # table (256 routes, one thread each)
     ("decode_w", "relu2", 24), ("decode_w", "silu", 32),
     ("many_e", "silu", 100),
+    # top_k = 32: per-route grouped units (m = 2 and 4: 64 and 128 routes), the
+    # route-grouped kernel (m = 16: 512 routes), the grouped GEMMs (m = 80)
+    ("topk32", "relu2", 2), ("topk32", "silu", 4), ("topk32", "relu2", 16), ("topk32", "silu", 80),
 ]
 
 
